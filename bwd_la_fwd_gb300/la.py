@@ -1,0 +1,158 @@
+"""Thin ctypes binding over the C ABI declared in include/la.h.
+
+Argument marshalling only: every step of the computation runs in the CUDA library.  PyTorch supplies
+device memory and the current stream.  If the compiled library is missing, ``load_library`` raises;
+there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LA_F32 = 0
+LA_BF16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libla_gb300.so"
+_lock = threading.Lock()
+_lib = None
+
+_STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_WORKSPACE", 4: "LA_ERR_CUDA",
+           5: "LA_ERR_TIMEOUT", 6: "LA_ERR_BOUNDS"}
+
+
+class LAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {la_status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, LIB_NAME)
+
+
+def load_library():
+    """Load the compiled CUDA library (built by ``bwd_la_fwd_gb300.build``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing: run `python -m bwd_la_fwd_gb300.build` "
+                               "(or __graft_entry__.build()); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.la_version.argtypes = []
+        lib.la_version.restype = i
+        lib.la_status_string.argtypes = [i]
+        lib.la_status_string.restype = ctypes.c_char_p
+        lib.la_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+        lib.la_workspace_bytes.restype = sz
+        lib.la_forward.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, sz, vp]
+        lib.la_forward.restype = i
+        lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+        lib.la_backward.restype = i
+        lib.la_get_status.argtypes = [vp, vp]
+        lib.la_get_status.restype = i
+        _lib = lib
+        return lib
+
+
+def la_status_string(status: int) -> str:
+    if _lib is not None:
+        return _lib.la_status_string(int(status)).decode()
+    return _STATUS.get(int(status), "LA_UNKNOWN_STATUS")
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LA_BF16
+    if t.dtype == torch.float32:
+        return LA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _shape(Q):
+    if Q.dim() != 4:
+        raise ValueError(f"expected a [B, H, N, D] tensor, got shape {tuple(Q.shape)}")
+    return tuple(int(s) for s in Q.shape)
+
+
+def _check_like(Q, *others):
+    for t in others:
+        if t is None:
+            continue
+        if t.shape != Q.shape or t.dtype != Q.dtype or t.device != Q.device:
+            raise ValueError("all [B,H,N,D] tensors must share shape, dtype and device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B,H,N,D]")
+
+
+def la_workspace_bytes(B: int, H: int, N: int, D: int, causal: bool, dtype: int, backward: bool) -> int:
+    return int(load_library().la_workspace_bytes(B, H, N, D, int(bool(causal)), int(dtype), int(bool(backward))))
+
+
+def new_workspace(B: int, H: int, N: int, D: int, causal: bool, dtype: int, backward: bool, device="cuda"):
+    """Zero-filled device workspace of the size the library asks for (torch owns it)."""
+    import torch
+    n = la_workspace_bytes(B, H, N, D, causal, dtype, backward)
+    if n == 0:
+        raise LAError(1, "la_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def la_forward(Q, K, V, causal: bool, O=None, normaliser=None, workspace=None, stream=None):
+    """O, g = la_forward(Q, K, V, causal): normalised linear attention forward on [B,H,N,D] tensors."""
+    import torch
+    B, H, N, D = _shape(Q)
+    _check_like(Q, K, V, O)
+    dt = _dtype_code(Q)
+    if O is None:
+        O = torch.empty_like(Q)
+    if normaliser is None:
+        normaliser = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        workspace = new_workspace(B, H, N, D, causal, dt, False, Q.device)
+    st = load_library().la_forward(_ptr(Q), _ptr(K), _ptr(V), int(bool(causal)), _ptr(O), _ptr(normaliser), B, H, N,
+                                   D, dt, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream_ptr(stream))
+    if st != 0:
+        raise LAError(st, "la_forward")
+    return O, normaliser
+
+
+def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspace=None, stream=None):
+    """dQ, dK, dV = la_backward(Q, K, V, O, dO, causal): gradients of sum(dO * O)."""
+    import torch
+    B, H, N, D = _shape(Q)
+    _check_like(Q, K, V, O, dO, dQ, dK, dV)
+    dt = _dtype_code(Q)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(Q) if dK is None else dK
+    dV = torch.empty_like(Q) if dV is None else dV
+    if workspace is None:
+        workspace = new_workspace(B, H, N, D, causal, dt, True, Q.device)
+    st = load_library().la_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                    int(bool(causal)), B, H, N, D, dt, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if st != 0:
+        raise LAError(st, "la_backward")
+    return dQ, dK, dV
+
+
+def la_get_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status recorded in the workspace."""
+    return int(load_library().la_get_status(_ptr(workspace), _stream_ptr(stream)))

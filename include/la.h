@@ -1,0 +1,106 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) normalised linear-attention library.
+ *
+ * Operation.  "Transformer Based Linear Attention with Optimized GPU Kernel Implementation"
+ * (A. Gerami, R. Duraiswami, arXiv 2510.21956) describes a linear-attention (LA) head over N tokens,
+ * each embedded in a D-dimensional head (shd-paper.top page, abstract), with a forward/backward
+ * formulation, a normalisation scheme and analytical gradients, in O(N D^2) time and O(N D) memory
+ * (sciencestack.ai page, TL;DR).  The pages print no formula; this library computes, for every
+ * (batch b, head h) independently and with rows i, j = 0..N-1:
+ *
+ *   W_ij = m_ij (1 + q_i . k_j),  m_ij = [j <= i] if causal else 1
+ *   g_i  = sum_j W_ij                                  (the normaliser)
+ *   O_i  = sum_j W_ij v_j / g_i
+ *
+ * and the exact gradients of L = sum_i dO_i . O_i with respect to Q, K and V.  The N x N weights are
+ * never formed: the kernels carry D x D running states, as the O(N D^2) / O(N D) claims require.
+ *
+ * Layout.  Q, K, V, O, dO, dQ, dK, dV are dense, contiguous [B, H, N, D] tensors of one element
+ * type (LA_F32 = float, LA_BF16 = bfloat16), element (b, h, i, d) at ((b H + h) N + i) D + d.  The
+ * normaliser is float [B, H, N].  All accumulation is in fp32.  Supported: B, H >= 1 (B*H < 2^31),
+ * N >= 1 (B*H*N*D < 2^40), D in {16, 32, 64, 128, 256}.
+ *
+ * Memory.  Every pointer is a DEVICE pointer except where stated.  The caller owns every buffer; the
+ * library never allocates device or host memory and never synchronises the stream (except
+ * la_get_status).  Scratch comes from the caller's workspace, whose size is la_workspace_bytes().
+ * The workspace must be 256-byte aligned and zero-filled before its first use (cudaMemset or
+ * torch.zeros); the library keeps it in a reusable state afterwards.  One workspace must not be used
+ * by two calls that can run at the same time.  Outputs must not alias inputs or each other.
+ *
+ * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL means the legacy default stream) and
+ * the call returns without waiting for it.
+ *
+ * Errors.  Every entry point returns an la_status.  Argument errors are found on the host before any
+ * work is enqueued (nothing is launched).  A launch failure returns LA_ERR_CUDA.  Conditions found on
+ * the device (a bounded wait that ran out, an index check) are recorded in a sticky status word inside
+ * the workspace and reported by la_get_status().  Nothing is thrown across the ABI.
+ */
+#ifndef LA_GB300_H
+#define LA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, aliasing outputs */
+    LA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. an unsupported D) */
+    LA_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than la_workspace_bytes() */
+    LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    LA_ERR_TIMEOUT = 5,     /* device: a bounded inter-block wait gave up (reported by la_get_status) */
+    LA_ERR_BOUNDS = 6       /* device: an internal index check failed (reported by la_get_status) */
+} la_status;
+
+typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
+
+/* Library ABI version (major * 100 + minor). */
+int la_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *la_status_string(int status);
+
+/*
+ * Bytes of device workspace that la_forward (backward = 0) or la_backward (backward = 1) needs for
+ * this problem.  Host-only, never touches the GPU.  Returns 0 for an invalid or unsupported request.
+ * A workspace sized with backward = 1 also serves la_forward on the same shape.
+ */
+size_t la_workspace_bytes(int B, int H, int N, int D, int causal, int dtype, int backward);
+
+/*
+ * Forward pass (sciencestack.ai page, TL;DR: the LA forward pass with its normalisation scheme).
+ *   Q, K, V     in : [B,H,N,D] of `dtype`
+ *   causal      in : nonzero selects the causal mask j <= i
+ *   O           out: [B,H,N,D] of `dtype`, O_i = sum_j W_ij v_j / g_i, rounded once (nearest-even)
+ *   normaliser  out: float [B,H,N] with g_i, or NULL to skip it
+ *   workspace   in/out: device scratch of workspace_bytes >= la_workspace_bytes(..., backward = 0)
+ * Pointers must be 16-byte aligned.
+ */
+int la_forward(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B, int H,
+               int N, int D, int dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward pass (sciencestack.ai page, TL;DR: analytical gradients of the LA head).
+ *   Q, K, V, O, dO  in : [B,H,N,D] of `dtype`; O is the forward output, dO = dL/dO
+ *   dQ, dK, dV      out: [B,H,N,D] of `dtype`, the gradients of L = sum dO . O
+ *   causal          in : must match the forward call
+ *   workspace       in/out: workspace_bytes >= la_workspace_bytes(..., backward = 1)
+ * The normaliser is recomputed, not read.  Pointers must be 16-byte aligned.
+ */
+int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
+                void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the sticky device status recorded in `workspace`
+ * by earlier calls (LA_OK, LA_ERR_TIMEOUT or LA_ERR_BOUNDS), or LA_ERR_CUDA if the stream failed.
+ */
+int la_get_status(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_GB300_H */

@@ -1,0 +1,435 @@
+"""Benchmark: LA forward + backward throughput on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: the paper's standalone shape (B=4, H=16, N=4096, D=128, bf16 storage, fp32 accumulation;
+"Transformer Based Linear Attention with Optimized GPU Kernel Implementation", sciencestack.ai page,
+Figures 2 and 3), synthetic Gaussian inputs (Q, K ~ N(0, 1/D), V, dO ~ N(0, 1)).  One step is one pass
+of the whole hot path over one batch: causal forward + backward, then non-causal forward + backward,
+so a step processes 2 * B * N tokens.  Every input tensor (67 MB) and the set of them (268 MB) is larger
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs resident in HBM; `e2e` is the
+same metric through the public API with pinned host buffers copied in and results copied out inside
+the timed region; `roofline` is for the call that takes the largest share of the step; `cpu_baseline`
+is the fp64 oracle on a bounded sample of heads on this host's cores.  `--impl reference` times that
+oracle alone, on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, H, N, D = 4, 16, 4096, 128
+ELEM = 2  # bf16
+METRIC = "LA fwd+bwd tokens/s and TFLOP/s, % of roofline, at B=4 H=16 D=128 N=4096"
+WORKLOAD = "LA fwd+bwd (causal + non-causal) B=4 H=16 N=4096 D=128 bf16"
+PASSES = ("causal", "noncausal")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+
+
+def config_dict():
+    return {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "passes_per_step": list(PASSES),
+            "tokens_per_step": 2 * B * N, "l2": "inputs larger than L2 (4 x 67 MB per step), no flush",
+            "seed": 1}
+
+
+def alg_bytes(kind: str) -> int:
+    """Algorithmic HBM bytes of one call: fwd reads Q,K,V and writes O and the fp32 normaliser; bwd reads
+    Q,K,V,O,dO and writes dQ,dK,dV."""
+    t = B * H * N * D * ELEM
+    return 4 * t + 4 * B * H * N if kind == "fwd" else 8 * t
+
+
+def alg_flops(kind: str) -> int:
+    """Algorithmic flops of one call: 4 D^2 per head-row forward (state update + read-out), 10 D^2 backward."""
+    return (4 if kind == "fwd" else 10) * D * D * B * H * N
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bwd_la_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons while the GPU is loaded."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- CPU baseline ---
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_step(host, n_heads: int) -> float:
+    """The explicit fp64 oracle, as it stands, on the first n_heads heads of the batch: causal and
+    non-causal forward + backward.  The 4 * n_heads calls (one head each, single-threaded) run
+    concurrently, one per core.  Returns seconds."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from bwd_la_fwd_gb300 import inputs
+    f = {k: inputs.to_f64(v.reshape(B * H, N, D)[:n_heads], "bf16") for k, v in host.items()}
+    tasks = []
+    for h in range(n_heads):
+        q, k, v, do = (f[n][h].reshape(1, 1, N, D) for n in ("Q", "K", "V", "dO"))
+        for causal in (True, False):
+            tasks.append((oracle.forward, (q, k, v, causal), {"threads": 1}))
+            tasks.append((oracle.backward, (q, k, v, do, causal), {"threads": 1}))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=len(tasks)) as ex:
+        for fut in [ex.submit(fn, *a, **kw) for fn, a, kw in tasks]:
+            fut.result()
+    return time.perf_counter() - t0
+
+
+def sample_heads(cores: int) -> int:
+    """Heads per oracle sample: four single-threaded calls per head, at most one call per core."""
+    return max(1, min(B * H, cores // 4))
+
+
+def sample_tokens(n_heads: int) -> float:
+    """Tokens covered by a sample of n_heads head-sequences over both passes (a token spans H heads)."""
+    return 2.0 * n_heads * N / H
+
+
+def cpu_baseline(host):
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    n_heads = sample_heads(cores)
+    dt = oracle_sample_step(host, n_heads)
+    return {"value": sample_tokens(n_heads) / dt, "unit": "tokens/s", "cores": min(cores, 4 * n_heads),
+            "kind": "oracle",
+            "sample": f"explicit fp64 oracle, causal + non-causal fwd+bwd on {n_heads} of {B * H} heads, one call per core "
+                      f"(N={N}, D={D}); {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------------- our arm ---
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from bwd_la_fwd_gb300 import inputs, la
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    la.load_library()
+
+    host = inputs.generate(B, H, N, D, seed=1, dtype="bf16")
+    pinned = {k: torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).pin_memory() for k, v in host.items()}
+    Q, K, V, dO = (pinned[n].to(dev) for n in ("Q", "K", "V", "dO"))
+    ws = la.new_workspace(B, H, N, D, True, la.LA_BF16, True, dev)
+    outs = {p: {"O": torch.empty_like(Q), "g": torch.empty(B, H, N, device=dev), "dQ": torch.empty_like(Q),
+                "dK": torch.empty_like(Q), "dV": torch.empty_like(Q)} for p in PASSES}
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for p in PASSES:
+            o = outs[p]
+            causal = p == "causal"
+            if evs is not None:
+                evs[p + "_fwd"][0].record(stream)
+            la.la_forward(Q, K, V, causal, O=o["O"], normaliser=o["g"], workspace=ws)
+            if evs is not None:
+                evs[p + "_fwd"][1].record(stream)
+                evs[p + "_bwd"][0].record(stream)
+            la.la_backward(Q, K, V, o["O"], dO, causal, dQ=o["dQ"], dK=o["dK"], dV=o["dV"], workspace=ws)
+            if evs is not None:
+                evs[p + "_bwd"][1].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_spin = time.time()
+    while time.time() - t_spin < 1.0:  # bring clocks up before warm-up (untimed)
+        step()
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = la.la_get_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {la.la_status_string(st)}")
+
+    calls = [p + s for p in PASSES for s in ("_fwd", "_bwd")]
+    per_call = {c: 0.0 for c in calls}
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = la.la_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev_start.record(stream)
+    evsets = []
+    for _ in range(args.steps):
+        evs = {c: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for c in calls}
+        step(evs)
+        evsets.append(evs)
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    launches = la.la_launch_count() - launches0
+    sampler.stop()
+    st = la.la_get_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timed region: {la.la_status_string(st)}")
+    ms = ev_start.elapsed_time(ev_end) / args.steps
+    for evs in evsets:
+        for c in calls:
+            per_call[c] += evs[c][0].elapsed_time(evs[c][1]) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * 2 * B * N / (ms * 1e-3)
+    clocks = sampler.summary(t_spin, t_wall1)
+    clocks["window"] = "spin-up + warm-up + timed region"
+
+    # end to end through the public API: pinned host inputs in, every result out, each step
+    host_out = {p: {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs[p].items()}
+                for p in PASSES}
+
+    def e2e_step():
+        for n, t in (("Q", Q), ("K", K), ("V", V), ("dO", dO)):
+            t.copy_(pinned[n], non_blocking=True)
+        step()
+        for p in PASSES:
+            for k, v in outs[p].items():
+                host_out[p][k].copy_(v, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    tb = B * H * N * D * ELEM
+    h2d = 4 * tb
+    d2h = sum(v.numel() * v.element_size() for p in PASSES for v in outs[p].values())
+
+    # peak device memory of one causal fwd + bwd against the O(BHND) I/O floor
+    del host_out
+    peak = peak_memory(dev)
+
+    if rank != 0:
+        return None
+    hbm, tfl, peak_kind = measured_peaks()
+    dom = max(per_call, key=per_call.get)
+    kind = "fwd" if dom.endswith("_fwd") else "bwd"
+    achieved = alg_bytes(kind) / (per_call[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "call": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "traffic": traffic_for(dom), "peak_source": peak_kind,
+            "alg_bytes_per_launch": alg_bytes(kind), "avg_us": per_call[dom] * 1e3}
+    flops = sum(alg_flops("fwd" if c.endswith("_fwd") else "bwd") for c in calls)
+    roof_time = sum(max(alg_bytes(k) / (hbm * 1e9), alg_flops(k) / (tfl * 1e12))
+                    for k in ("fwd", "bwd", "fwd", "bwd"))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(),
+        "tflops": flops / (ms * 1e-3) / 1e12,
+        "roofline_frac_step": roof_time / (ms * 1e-3),
+        "calls_us": {c: per_call[c] * 1e3 for c in calls},
+        "roofline": roof,
+        "e2e": {"value": world * 2 * B * N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "peak_memory": peak,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(host)
+    return line
+
+
+def peak_memory(dev):
+    import torch
+
+    from bwd_la_fwd_gb300 import la
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    Q, K, V, dO = (torch.randn(B, H, N, D, device=dev, dtype=torch.bfloat16) for _ in range(4))
+    ws = la.new_workspace(B, H, N, D, True, la.LA_BF16, True, dev)
+    O, g = la.la_forward(Q, K, V, True, workspace=ws)
+    grads = la.la_backward(Q, K, V, O, dO, True, workspace=ws)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    floor = 8 * B * H * N * D * ELEM + 4 * B * H * N
+    del Q, K, V, dO, ws, O, g, grads
+    return {"bytes": int(peak), "floor": int(floor), "ratio": peak / floor,
+            "what": "causal fwd+bwd, all tensors and workspace allocated by torch"}
+
+
+def traffic_for(call: str):
+    """DRAM bytes per launch of this call from the committed ncu summary, if taken on the current source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    if t.get("source_hash") != kernel_source_hash():
+        return None
+    return t.get("calls", {}).get(call)
+
+
+# ---------------------------------------------------------------------------- reference arm ---
+
+def run_reference(args):
+    from bwd_la_fwd_gb300 import inputs
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    host = inputs.generate(B, H, N, D, seed=1, dtype="bf16")
+    cores = host_cores()
+    n_heads = args.ref_heads or sample_heads(cores)
+    for _ in range(args.warmup):
+        oracle_sample_step(host, n_heads)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample_step(host, n_heads)
+    sec = total / args.steps
+    value = sample_tokens(n_heads) / sec
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, 4 * n_heads),
+                             "kind": "oracle", "sample": f"each step: explicit fp64 oracle, causal + non-causal fwd+bwd on "
+                                       f"{n_heads} of {B * H} heads (N={N}, D={D})"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-heads", type=int, default=0, help="heads per reference step (default: one per core)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    rank, world, _ = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -4,8 +4,8 @@ The compute lives in ``csrc/`` (hand-written CUDA, C ABI in ``include/la.h``); `
 ctypes binding over that ABI.  The library is loaded on first use and a missing or stale build raises
 an error: there is no CPU fallback.
 """
-from .la import (LA_BF16, LA_F32, LAError, la_backward, la_forward, la_get_status, la_status_string,
+from .la import (LA_BF16, LA_F32, LAError, la_backward, la_forward, la_get_status, la_launch_count, la_status_string,
                  la_workspace_bytes, library_path, load_library)
 
-__all__ = ["LA_BF16", "LA_F32", "LAError", "la_backward", "la_forward", "la_get_status", "la_status_string",
+__all__ = ["LA_BF16", "LA_F32", "LAError", "la_backward", "la_forward", "la_get_status", "la_launch_count", "la_status_string",
            "la_workspace_bytes", "library_path", "load_library"]

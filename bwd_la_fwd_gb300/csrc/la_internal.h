@@ -1,0 +1,50 @@
+// la_internal.h -- declarations shared by the CUDA translation units of the library (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace la {
+
+// Device status codes written into the workspace's sticky status word (same values as la_status).
+enum : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBounds = 6 };
+
+// Workspace header: the first 256 bytes of every workspace.
+struct WsHeader {
+    uint32_t status;      // sticky device status (first error wins); cleared by la_get_status
+    uint32_t info[7];     // where the first error happened (kernel id, block, step), for debugging
+    uint32_t ticket[8];   // per-kernel ticket counters (reset by the last block of each launch)
+    uint32_t done[8];     // per-kernel completion counters
+    uint32_t epoch[8];    // per-kernel launch epochs (flags compare against these)
+};
+static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
+
+// How one call splits each head's N rows into segments whose D x D states are carried in the
+// workspace.  Chosen on the host from (N, D) only, so la_workspace_bytes and the launch agree.
+struct Plan {
+    int B, H, N, D, causal, dtype;
+    int BH;
+    int seg_len;        // rows per segment
+    int nseg;           // segments per head
+    long long stride;   // floats per segment state (S or P: D*D, then two D-vectors), padded
+    size_t off_states;  // byte offsets of the workspace regions
+    size_t off_flags;
+    size_t off_rowstats;
+    size_t bytes_fwd;   // workspace bytes for the forward / for the backward
+    size_t bytes_bwd;
+    bool use_tc;        // tcgen05 kernels (bf16) rather than the SIMT kernels
+};
+
+// Host-side count of kernels launched by the library (la_launch_count).
+void count_launches(unsigned n);
+
+bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p);
+
+// SIMT path (fp32 FFMA, any supported D, fp32 or bf16 storage).
+cudaError_t simt_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
+                         unsigned char *ws, cudaStream_t s);
+cudaError_t simt_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
+                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s);
+
+}  // namespace la

@@ -1,0 +1,469 @@
+// la_simt.cu -- fp32-FFMA (CUDA-core) path of the normalised linear attention, for every supported D
+// and for fp32 or bf16 storage.  It is the path for fp32 I/O (tf32 tensor cores cannot reach a 1e-5
+// relative error) and for shapes the tensor-core kernels do not take.
+//
+// Method ("Transformer Based Linear Attention with Optimized GPU Kernel Implementation", sciencestack.ai
+// page, TL;DR: O(N D^2) time, O(N D) memory, normalisation, analytical gradients), per head:
+//   forward : S_i = sum_{j<=i} k_j v_j^T, z_i = sum k_j, a_i = sum v_j, n_i = i + 1
+//             g_i = n_i + q_i . z_i,  O_i = (a_i + S_i^T q_i) / g_i            (c = 1)
+//   backward: dOt_i = dO_i / g_i, dt_i = (dO_i . O_i) / g_i
+//             dQ_i = S_i dOt_i - dt_i z_i
+//             P_j = sum_{i>=j} q_i dOt_i^T, y_j = sum dt_i q_i, e_j = sum dOt_i
+//             dK_j = P_j v_j - y_j,  dV_j = e_j + P_j^T k_j
+// (non-causal: every sum runs over all rows).  Each head is cut into segments; a first kernel forms
+// each segment's own D x D sum, a second turns those into exclusive prefix (or suffix) sums, and a third
+// re-walks each segment row by row from its carried-in state.
+#include <cuda_bf16.h>
+
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float load_f(const T *p);
+template <>
+__device__ __forceinline__ float load_f<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+template <typename T>
+__device__ __forceinline__ void store_f(T *p, float x);
+template <>
+__device__ __forceinline__ void store_f<float>(float *p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void store_f<__nv_bfloat16>(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Thread layout over a D x EB block of a state X[r][col]: thread t owns column col = t % EB and the
+// reduction indices r = p + NP * m (p = t / EB, m < RPT).
+template <int D>
+struct Cfg {
+    static constexpr int EB = D < 64 ? D : 64;  // output columns per block
+    static constexpr int NP = kThreads / EB;     // parts of the reduction dimension
+    static constexpr int RPT = D / NP;           // state entries per thread
+    static constexpr int RB = D >= 256 ? 16 : 32;  // rows staged in shared memory per batch
+    static constexpr int NBLK = D / EB;
+    static_assert(RPT >= 1 && NP * RPT == D, "bad SIMT layout");
+};
+
+enum Mode : int { kFwdO = 0, kBwdDQ = 1, kBwdDK = 2, kBwdDV = 3 };
+enum AggMode : int { kAggFwd = 0, kAggRev = 1 };
+
+struct Args {
+    const void *Q, *K, *V, *O, *dO;
+    void *out;          // O, dQ, dK or dV
+    float *g_out;       // forward: optional normaliser output
+    float *rs_g;        // workspace row statistics: g_i and delta_i, [BH * N]
+    float *rs_delta;
+    float *states;      // workspace segment states, [BH][nseg][stride]
+    long long N;
+    long long stride;
+    int nseg, seg_len, causal;
+};
+
+// ------------------------------------------------------------------------------------------------
+// Segment aggregate: for segment s of head bh, X = sum over its rows of u w^T plus two vector sums.
+//   kAggFwd: u = k, w = v           -> S block, z = sum k, a = sum v
+//   kAggRev: u = q, w = dO / g      -> P block, y = sum (delta/g) q, e = sum dO / g
+// grid = (nseg * BH, NBLK); the vector sums are written by column block 0.
+// ------------------------------------------------------------------------------------------------
+template <typename T, int D, int AM>
+__global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
+    using C = Cfg<D>;
+    extern __shared__ float smem[];
+    float *sU = smem;                  // [RB][D]
+    float *sW = sU + C::RB * D;        // [RB][D]
+    float *sSc = sW + C::RB * D;       // [RB] 1/g   (rev)
+    float *sDt = sSc + C::RB;          // [RB] delta/g (rev)
+
+    const int t = threadIdx.x, col = t % C::EB, p = t / C::EB;
+    const int colg = blockIdx.y * C::EB + col;
+    const long long bh = blockIdx.x / a.nseg;
+    const int s = blockIdx.x % a.nseg;
+    const long long r0 = (long long)s * a.seg_len;
+    const long long r1 = min((long long)a.N, r0 + a.seg_len);
+    const T *U = (const T *)(AM == kAggFwd ? a.K : a.Q) + bh * a.N * D;
+    const T *W = (const T *)(AM == kAggFwd ? a.V : a.dO) + bh * a.N * D;
+
+    float X[C::RPT];
+#pragma unroll
+    for (int m = 0; m < C::RPT; ++m) X[m] = 0.f;
+    float vu = 0.f, vw = 0.f;  // vector sums for index t (t < D), block 0 only
+
+    for (long long b0 = r0; b0 < r1; b0 += C::RB) {
+        const int nb = (int)min((long long)C::RB, r1 - b0);
+        if (AM == kAggRev && t < nb) {
+            const float gi = a.rs_g[bh * a.N + b0 + t];
+            sSc[t] = 1.f / gi;
+            sDt[t] = a.rs_delta[bh * a.N + b0 + t] / gi;
+        }
+        if (AM == kAggRev) __syncthreads();
+        for (int idx = t; idx < C::RB * D; idx += kThreads) {
+            const int r = idx / D, d = idx % D;
+            float u = 0.f, w = 0.f;
+            if (r < nb) {
+                u = load_f(U + (b0 + r) * D + d);
+                w = load_f(W + (b0 + r) * D + d);
+                if (AM == kAggRev) w *= sSc[r];
+            }
+            sU[idx] = u;
+            sW[idx] = w;
+        }
+        __syncthreads();
+        for (int r = 0; r < nb; ++r) {
+            const float wv = sW[r * D + colg];
+#pragma unroll
+            for (int m = 0; m < C::RPT; ++m) X[m] = fmaf(sU[r * D + p + C::NP * m], wv, X[m]);
+        }
+        if (blockIdx.y == 0 && t < D) {
+            for (int r = 0; r < nb; ++r) {
+                if (AM == kAggFwd) {
+                    vu += sU[r * D + t];
+                } else {
+                    vu = fmaf(sDt[r], sU[r * D + t], vu);
+                }
+                vw += sW[r * D + t];
+            }
+        }
+        __syncthreads();
+    }
+    float *st = a.states + (bh * a.nseg + s) * a.stride;
+#pragma unroll
+    for (int m = 0; m < C::RPT; ++m) st[(long long)(p + C::NP * m) * D + colg] = X[m];
+    if (blockIdx.y == 0 && t < D) {
+        st[(long long)D * D + t] = vu;
+        st[(long long)D * D + D + t] = vw;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Segment scan, in place over the segments of each head, for each float of the state:
+//   causal, forward direction: exclusive prefix (segment s gets the sum of segments 0..s-1)
+//   causal, reverse direction: exclusive suffix (segment s gets the sum of segments s+1..)
+//   non-causal: every segment gets the total.
+// grid = (ceil(used / 256), BH).
+// ------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) simt_scan(float *states, int nseg, long long stride, long long used,
+                                                      int causal, int reverse) {
+    const long long x = (long long)blockIdx.x * kThreads + threadIdx.x;
+    if (x >= used) return;
+    float *base = states + (long long)blockIdx.y * nseg * stride + x;
+    if (!causal) {
+        float tot = 0.f;
+        for (int s = 0; s < nseg; ++s) tot += base[s * stride];
+        for (int s = 0; s < nseg; ++s) base[s * stride] = tot;
+        return;
+    }
+    float run = 0.f;
+    for (int k = 0; k < nseg; ++k) {
+        const int s = reverse ? nseg - 1 - k : k;
+        const float v = base[s * stride];
+        base[s * stride] = run;
+        run += v;
+    }
+}
+
+
+__device__ __forceinline__ float warp_dot(const float *x, const float *y, int D, int lane) {
+    float acc = 0.f;
+    for (int d = lane; d < D; d += 32) acc = fmaf(x[d], y[d], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Row walk of one segment from its carried-in state (workspace, after simt_scan).  Thread (col, p)
+// keeps its RPT entries of the state in registers; the state is updated row by row (causal only) and
+// read out through a shared-memory reduction over the NP parts.
+//   kFwdO : X[d][e] = S,  u = k,      w = v,      t = q        -> O = (a + X^T q) / g
+//   kBwdDQ: X[e][d] = S,  u = v,      w = k,      t = dO/g     -> dQ = X^T t - (delta/g) z
+//   kBwdDK: X[e][d] = P,  u = dO/g,   w = q,      t = v        -> dK = X^T t - y      (rows reversed)
+//   kBwdDV: X[d][e] = P,  u = q,      w = dO/g,   t = k        -> dV = e + X^T t      (rows reversed)
+// kBwdDQ also writes g_i and delta_i = dO_i . O_i to the workspace for kAggRev, kBwdDK and kBwdDV.
+// grid = (nseg * BH, NBLK).
+// ------------------------------------------------------------------------------------------------
+template <typename T, int D, int MODE>
+__global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
+    using C = Cfg<D>;
+    constexpr int RB = C::RB;
+    constexpr bool REV = (MODE == kBwdDK || MODE == kBwdDV);
+    extern __shared__ float smem[];
+    float *sA = smem;             // u rows [RB][D]
+    float *sB = sA + RB * D;      // w rows
+    float *sT = sB + RB * D;      // t rows
+    float *sX = sT + RB * D;      // dQ: O rows
+    float *sY = sX + RB * D;      // dQ: q rows
+    float *sRun = sY + RB * D;    // running vector after each row: z, z, y or e
+    float *sRun2 = sRun + RB * D; // forward: running a
+    float *sRed = sRun2 + RB * D; // [RB][NP][EB]
+    float *sG = sRed + RB * kThreads;
+    float *sDt = sG + RB;
+
+    const int t = threadIdx.x, col = t % C::EB, p = t / C::EB;
+    const int lane = t & 31, warp = t >> 5;
+    const int colg = blockIdx.y * C::EB + col;
+    const long long N = a.N;
+    const long long bh = blockIdx.x / a.nseg;
+    const int s = blockIdx.x % a.nseg;
+    const long long r0 = (long long)s * a.seg_len;
+    const long long r1 = min(N, r0 + a.seg_len);
+    const long long hoff = bh * N * D;
+    const T *Qh = (const T *)a.Q + hoff, *Kh = (const T *)a.K + hoff, *Vh = (const T *)a.V + hoff;
+    const T *Oh = (const T *)a.O + hoff, *dOh = (const T *)a.dO + hoff;
+    const float *st = a.states + (bh * a.nseg + s) * a.stride;
+
+    float X[C::RPT];
+#pragma unroll
+    for (int m = 0; m < C::RPT; ++m) {
+        const int r = p + C::NP * m;
+        X[m] = (MODE == kFwdO || MODE == kBwdDV) ? st[(long long)r * D + colg] : st[(long long)colg * D + r];
+    }
+    float run1 = 0.f, run2 = 0.f;
+    if (t < D) {
+        run1 = (MODE == kBwdDV) ? st[(long long)D * D + D + t] : st[(long long)D * D + t];
+        if (MODE == kFwdO) run2 = st[(long long)D * D + D + t];
+    }
+
+    const int nbatch = (int)((r1 - r0 + RB - 1) / RB);
+    for (int bi = 0; bi < nbatch; ++bi) {
+        const long long b0 = REV ? max(r0, r1 - (long long)(bi + 1) * RB) : r0 + (long long)bi * RB;
+        const int nb = (int)(REV ? (r1 - (long long)bi * RB) - b0 : min((long long)RB, r1 - b0));
+        if (REV) {
+            if (t < nb) {
+                const float gi = a.rs_g[bh * N + b0 + t];
+                sG[t] = gi;
+                sDt[t] = a.rs_delta[bh * N + b0 + t] / gi;
+            }
+            __syncthreads();
+        }
+        // phase 1: stage the batch's rows as fp32
+        for (int idx = t; idx < RB * D; idx += kThreads) {
+            const int r = idx / D, d = idx % D;
+            const bool ok = r < nb;
+            const long long o = (b0 + r) * D + d;
+            if (MODE == kFwdO) {
+                sA[idx] = ok ? load_f(Kh + o) : 0.f;
+                sB[idx] = ok ? load_f(Vh + o) : 0.f;
+                sT[idx] = ok ? load_f(Qh + o) : 0.f;
+            } else if (MODE == kBwdDQ) {
+                sA[idx] = ok ? load_f(Vh + o) : 0.f;
+                sB[idx] = ok ? load_f(Kh + o) : 0.f;
+                sT[idx] = ok ? load_f(dOh + o) : 0.f;
+                sX[idx] = ok ? load_f(Oh + o) : 0.f;
+                sY[idx] = ok ? load_f(Qh + o) : 0.f;
+            } else if (MODE == kBwdDK) {
+                sA[idx] = ok ? load_f(dOh + o) / sG[r] : 0.f;
+                sB[idx] = ok ? load_f(Qh + o) : 0.f;
+                sT[idx] = ok ? load_f(Vh + o) : 0.f;
+            } else {
+                sA[idx] = ok ? load_f(Qh + o) : 0.f;
+                sB[idx] = ok ? load_f(dOh + o) / sG[r] : 0.f;
+                sT[idx] = ok ? load_f(Kh + o) : 0.f;
+            }
+        }
+        __syncthreads();
+        // phase 2: running vectors, in processing order
+        if (t < D) {
+            for (int k = 0; k < nb; ++k) {
+                const int r = REV ? nb - 1 - k : k;
+                if (a.causal) {
+                    if (MODE == kFwdO) {
+                        run1 += sA[r * D + t];
+                        run2 += sB[r * D + t];
+                    } else if (MODE == kBwdDQ) {
+                        run1 += sB[r * D + t];
+                    } else if (MODE == kBwdDK) {
+                        run1 = fmaf(sDt[r], sB[r * D + t], run1);
+                    } else {
+                        run1 += sB[r * D + t];
+                    }
+                }
+                sRun[r * D + t] = run1;
+                if (MODE == kFwdO) sRun2[r * D + t] = run2;
+            }
+        }
+        __syncthreads();
+        // per-row scalars of the forward-direction walks
+        if (!REV) {
+            for (int r = warp; r < nb; r += kThreads / 32) {
+                const float n = a.causal ? (float)(b0 + r + 1) : (float)N;
+                if (MODE == kFwdO) {
+                    const float gi = n + warp_dot(sT + r * D, sRun + r * D, D, lane);
+                    if (lane == 0) {
+                        sG[r] = gi;
+                        if (a.g_out && blockIdx.y == 0) a.g_out[bh * N + b0 + r] = gi;
+                    }
+                } else {
+                    const float gi = n + warp_dot(sY + r * D, sRun + r * D, D, lane);
+                    const float delta = warp_dot(sT + r * D, sX + r * D, D, lane);
+                    if (lane == 0) {
+                        sG[r] = gi;
+                        sDt[r] = delta / gi;
+                        if (blockIdx.y == 0) {
+                            a.rs_g[bh * N + b0 + r] = gi;
+                            a.rs_delta[bh * N + b0 + r] = delta;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            if (MODE == kBwdDQ) {
+                for (int idx = t; idx < nb * D; idx += kThreads) sT[idx] = sT[idx] / sG[idx / D];
+                __syncthreads();
+            }
+        }
+        // phase 3: state update and partial read-out
+        for (int k = 0; k < nb; ++k) {
+            const int r = REV ? nb - 1 - k : k;
+            if (a.causal) {
+                const float wv = sB[r * D + colg];
+#pragma unroll
+                for (int m = 0; m < C::RPT; ++m) X[m] = fmaf(sA[r * D + p + C::NP * m], wv, X[m]);
+            }
+            float part = 0.f;
+#pragma unroll
+            for (int m = 0; m < C::RPT; ++m) part = fmaf(sT[r * D + p + C::NP * m], X[m], part);
+            sRed[(r * C::NP + p) * C::EB + col] = part;
+        }
+        __syncthreads();
+        // phase 4: finish the rows r = p (mod NP)
+        for (int r = p; r < nb; r += C::NP) {
+            float tot = 0.f;
+#pragma unroll 4
+            for (int q = 0; q < C::NP; ++q) tot += sRed[(r * C::NP + q) * C::EB + col];
+            float v;
+            if (MODE == kFwdO) {
+                v = (sRun2[r * D + colg] + tot) / sG[r];
+            } else if (MODE == kBwdDQ) {
+                v = tot - sDt[r] * sRun[r * D + colg];
+            } else if (MODE == kBwdDK) {
+                v = tot - sRun[r * D + colg];
+            } else {
+                v = sRun[r * D + colg] + tot;
+            }
+            store_f((T *)a.out + hoff + (b0 + r) * D + colg, v);
+        }
+        __syncthreads();
+    }
+}
+
+template <int D>
+constexpr size_t agg_smem() { return (size_t)(2 * Cfg<D>::RB * D + 2 * Cfg<D>::RB) * sizeof(float); }
+template <int D>
+constexpr size_t rows_smem() {
+    return (size_t)(7 * Cfg<D>::RB * D + Cfg<D>::RB * kThreads + 2 * Cfg<D>::RB) * sizeof(float);
+}
+
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+Args make_args(const Plan &p, const void *Q, const void *K, const void *V, const void *O, const void *dO,
+               unsigned char *ws) {
+    Args a{};
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.dO = dO;
+    a.states = (float *)(ws + p.off_states);
+    a.rs_g = (float *)(ws + p.off_rowstats);
+    a.rs_delta = a.rs_g + (size_t)p.BH * p.N;
+    a.N = p.N;
+    a.stride = p.stride;
+    a.nseg = p.nseg;
+    a.seg_len = p.seg_len;
+    a.causal = p.causal;
+    return a;
+}
+
+template <typename T, int D>
+cudaError_t forward_impl(const Plan &p, Args a, void *O, float *g, cudaStream_t s) {
+    using C = Cfg<D>;
+    const dim3 grid((unsigned)(p.nseg * p.BH), C::NBLK);
+    const long long used = (long long)D * D + 2 * D;
+    cudaError_t e;
+    if ((e = allow_smem(simt_aggregate<T, D, kAggFwd>, agg_smem<D>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, D, kFwdO>, rows_smem<D>())) != cudaSuccess) return e;
+    simt_aggregate<T, D, kAggFwd><<<grid, kThreads, agg_smem<D>(), s>>>(a);
+    simt_scan<<<dim3((unsigned)((used + kThreads - 1) / kThreads), p.BH), kThreads, 0, s>>>(
+        a.states, p.nseg, p.stride, used, p.causal, 0);
+    a.out = O;
+    a.g_out = g;
+    simt_rows<T, D, kFwdO><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(3);
+    return e;
+}
+
+template <typename T, int D>
+cudaError_t backward_impl(const Plan &p, Args a, void *dQ, void *dK, void *dV, cudaStream_t s) {
+    using C = Cfg<D>;
+    const dim3 grid((unsigned)(p.nseg * p.BH), C::NBLK);
+    const long long used = (long long)D * D + 2 * D;
+    const dim3 sgrid((unsigned)((used + kThreads - 1) / kThreads), p.BH);
+    cudaError_t e;
+    if ((e = allow_smem(simt_aggregate<T, D, kAggFwd>, agg_smem<D>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_aggregate<T, D, kAggRev>, agg_smem<D>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, D, kBwdDQ>, rows_smem<D>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, D, kBwdDK>, rows_smem<D>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, D, kBwdDV>, rows_smem<D>())) != cudaSuccess) return e;
+    simt_aggregate<T, D, kAggFwd><<<grid, kThreads, agg_smem<D>(), s>>>(a);
+    simt_scan<<<sgrid, kThreads, 0, s>>>(a.states, p.nseg, p.stride, used, p.causal, 0);
+    a.out = dQ;
+    simt_rows<T, D, kBwdDQ><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    simt_aggregate<T, D, kAggRev><<<grid, kThreads, agg_smem<D>(), s>>>(a);
+    simt_scan<<<sgrid, kThreads, 0, s>>>(a.states, p.nseg, p.stride, used, p.causal, 1);
+    a.out = dK;
+    simt_rows<T, D, kBwdDK><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    a.out = dV;
+    simt_rows<T, D, kBwdDV><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(7);
+    return e;
+}
+
+template <typename T>
+cudaError_t forward_t(const Plan &p, Args a, void *O, float *g, cudaStream_t s) {
+    switch (p.D) {
+        case 16: return forward_impl<T, 16>(p, a, O, g, s);
+        case 32: return forward_impl<T, 32>(p, a, O, g, s);
+        case 64: return forward_impl<T, 64>(p, a, O, g, s);
+        case 128: return forward_impl<T, 128>(p, a, O, g, s);
+        case 256: return forward_impl<T, 256>(p, a, O, g, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t backward_t(const Plan &p, Args a, void *dQ, void *dK, void *dV, cudaStream_t s) {
+    switch (p.D) {
+        case 16: return backward_impl<T, 16>(p, a, dQ, dK, dV, s);
+        case 32: return backward_impl<T, 32>(p, a, dQ, dK, dV, s);
+        case 64: return backward_impl<T, 64>(p, a, dQ, dK, dV, s);
+        case 128: return backward_impl<T, 128>(p, a, dQ, dK, dV, s);
+        case 256: return backward_impl<T, 256>(p, a, dQ, dK, dV, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t simt_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
+                         unsigned char *ws, cudaStream_t s) {
+    Args a = make_args(p, Q, K, V, nullptr, nullptr, ws);
+    return p.dtype == 1 ? forward_t<__nv_bfloat16>(p, a, O, g, s) : forward_t<float>(p, a, O, g, s);
+}
+
+cudaError_t simt_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
+                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s) {
+    Args a = make_args(p, Q, K, V, O, dO, ws);
+    return p.dtype == 1 ? backward_t<__nv_bfloat16>(p, a, dQ, dK, dV, s) : backward_t<float>(p, a, dQ, dK, dV, s);
+}
+
+}  // namespace la

@@ -46,6 +46,8 @@ def load_library():
         vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
         lib.la_version.argtypes = []
         lib.la_version.restype = i
+        lib.la_launch_count.argtypes = []
+        lib.la_launch_count.restype = ctypes.c_ulonglong
         lib.la_status_string.argtypes = [i]
         lib.la_status_string.restype = ctypes.c_char_p
         lib.la_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
@@ -99,6 +101,11 @@ def _check_like(Q, *others):
             raise ValueError("all [B,H,N,D] tensors must share shape, dtype and device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous [B,H,N,D]")
+
+
+def la_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load_library().la_launch_count())
 
 
 def la_workspace_bytes(B: int, H: int, N: int, D: int, causal: bool, dtype: int, backward: bool) -> int:

@@ -59,6 +59,11 @@ typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
 /* Library ABI version (major * 100 + minor). */
 int la_version(void);
 
+/* Number of CUDA kernels this library has launched in this process (all devices, all calls).  Host
+ * counter, incremented at each successful launch; lets a caller count the library's launches inside a
+ * timed region. */
+unsigned long long la_launch_count(void);
+
 /* Human-readable name of a status code; never NULL. */
 const char *la_status_string(int status);
 

@@ -1,0 +1,102 @@
+"""The C ABI without a GPU: the library loads, exports every symbol include/la.h declares, sizes its
+workspace, and rejects bad arguments on the host before any work is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "la.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bwd_la_fwd_gb300 import build, la
+    build.build()
+    return la.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("la_forward", "la_backward", "la_workspace_bytes", "la_get_status", "la_status_string",
+              "la_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings(lib):
+    assert lib.la_version() >= 100
+    for code, name in [(0, "LA_OK"), (1, "LA_ERR_INVALID_ARG"), (2, "LA_ERR_UNSUPPORTED"),
+                       (3, "LA_ERR_WORKSPACE"), (4, "LA_ERR_CUDA"), (5, "LA_ERR_TIMEOUT"), (6, "LA_ERR_BOUNDS")]:
+        assert lib.la_status_string(code).decode() == name
+    assert lib.la_status_string(99).decode() == "LA_UNKNOWN_STATUS"
+
+
+def test_workspace_sizes(lib):
+    ws = lib.la_workspace_bytes
+    # the standard shape: carried states stay small next to the 8 tensor volumes of fwd + bwd
+    floor = 8 * 4 * 16 * 4096 * 128 * 2 + 4 * 4 * 16 * 4096
+    for causal in (0, 1):
+        b = ws(4, 16, 4096, 128, causal, 1, 1)
+        assert 0 < b <= 0.2 * floor
+        assert ws(4, 16, 4096, 128, causal, 1, 0) <= b
+        assert b % 256 == 0
+    for D in (16, 32, 64, 128, 256):
+        assert ws(1, 2, 1, D, 1, 0, 1) > 0
+    assert ws(1, 1, 1, 48, 1, 1, 1) == 0     # unsupported D
+    assert ws(0, 1, 8, 64, 1, 1, 1) == 0     # empty batch
+    assert ws(1, 1, 8, 64, 1, 7, 1) == 0     # bad dtype
+    # long sequences keep at most 64 segments per head
+    assert ws(4, 16, 65536, 128, 1, 1, 1) <= 0.2 * 16 * (8 * 4 * 16 * 65536 * 128 * 2)
+
+
+def _fwd(lib, Q=0x1000, K=0x2000_0000, V=0x4000_0000, O=0x6000_0000, g=0, B=1, H=1, N=8, D=64, dt=1,
+         ws=0x8000_0000, wsb=1 << 30):
+    vp = ctypes.c_void_p
+    return lib.la_forward(vp(Q), vp(K), vp(V), 1, vp(O), vp(g), B, H, N, D, dt, vp(ws), wsb, vp(0))
+
+
+def test_forward_rejects_bad_arguments_on_host(lib):
+    # every case below returns before any CUDA call, so no GPU is touched
+    assert _fwd(lib, D=48) == 2                       # unsupported head size
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, dt=3) == 1
+    assert _fwd(lib, Q=0) == 1                        # null input
+    assert _fwd(lib, K=0x2000_0008) == 1              # misaligned
+    assert _fwd(lib, ws=0) == 3                       # no workspace
+    assert _fwd(lib, ws=0x8000_0010) == 3             # misaligned workspace
+    assert _fwd(lib, wsb=16) == 3                     # workspace too small
+    assert _fwd(lib, O=0x1000) == 1                   # output aliases Q
+    assert _fwd(lib, g=0x6000_0000 + 64) == 1         # normaliser inside O
+
+
+def test_backward_rejects_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+    base = [0x1000_0000 * (i + 1) for i in range(8)]
+
+    def call(ptrs=base, D=64, ws=0xA000_0000, wsb=1 << 30):
+        return lib.la_backward(*[vp(p) for p in ptrs], 1, 1, 2, 16, D, 1, vp(ws), wsb, vp(0))
+
+    assert call(D=24) == 2
+    bad = list(base)
+    bad[4] = 0
+    assert call(bad) == 1
+    bad = list(base)
+    bad[6] = base[7]                                  # dK == dV
+    assert call(bad) == 1
+    bad = list(base)
+    bad[5] = base[0] + 16                             # dQ overlaps Q
+    assert call(bad) == 1
+    assert call(wsb=100) == 3

@@ -41,13 +41,16 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     if (BH * p->nseg >= (1LL << 31)) return false;
     p->stride = (long long)round_up((size_t)D * D + 2 * (size_t)D, 64);
     p->use_tc = false;
-    const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * sizeof(float);
+    p->acc_bytes = dtype == LA_F32 ? 8 : 4;
+    const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
     const size_t flags = (size_t)BH * p->nseg * sizeof(uint32_t);
     p->off_states = 256;
     p->off_flags = round_up(p->off_states + states, 256);
     p->off_rowstats = round_up(p->off_flags + flags, 256);
     p->bytes_fwd = p->off_rowstats;
-    p->bytes_bwd = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
+    // g, delta and up to four per-column-block partial sums of delta
+    const size_t nblk = D > 64 ? (size_t)D / 64 : 1;
+    p->bytes_bwd = round_up(p->off_rowstats + (2 + nblk) * (size_t)BH * N * p->acc_bytes, 256);
     return true;
 }
 

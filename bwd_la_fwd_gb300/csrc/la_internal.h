@@ -27,7 +27,8 @@ struct Plan {
     int BH;
     int seg_len;        // rows per segment
     int nseg;           // segments per head
-    long long stride;   // floats per segment state (S or P: D*D, then two D-vectors), padded
+    long long stride;   // elements per segment state (S or P: D*D, then two D-vectors), padded
+    int acc_bytes;      // accumulator element size: 4 (bf16 storage) or 8 (fp32 storage)
     size_t off_states;  // byte offsets of the workspace regions
     size_t off_flags;
     size_t off_rowstats;

@@ -1,6 +1,9 @@
-// la_simt.cu -- fp32-FFMA (CUDA-core) path of the normalised linear attention, for every supported D
-// and for fp32 or bf16 storage.  It is the path for fp32 I/O (tf32 tensor cores cannot reach a 1e-5
-// relative error) and for shapes the tensor-core kernels do not take.
+// la_simt.cu -- CUDA-core path of the normalised linear attention, for every supported D and for fp32
+// or bf16 storage.  bf16 storage accumulates in fp32; fp32 storage accumulates (and carries its
+// segment states) in fp64, because the gradients are differences of terms as large as the result
+// (dQ_i = S_i dOt_i - dt_i z_i), so fp32 accumulation leaves ~1e-4 relative error on the smaller
+// elements while fp64 leaves only the final rounding to fp32.  It is the path for fp32 I/O (tf32
+// tensor cores are far from 1e-5) and for shapes the tensor-core kernels do not take.
 //
 // Method ("Transformer Based Linear Attention with Optimized GPU Kernel Implementation", sciencestack.ai
 // page, TL;DR: O(N D^2) time, O(N D) memory, normalisation, analytical gradients), per head:
@@ -22,43 +25,42 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <typename T>
-__device__ __forceinline__ float load_f(const T *p);
-template <>
-__device__ __forceinline__ float load_f<float>(const float *p) { return *p; }
-template <>
-__device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load_f(const float *p) { return *p; }
+__device__ __forceinline__ float load_f(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 
-template <typename T>
-__device__ __forceinline__ void store_f(T *p, float x);
-template <>
-__device__ __forceinline__ void store_f<float>(float *p, float x) { *p = x; }
-template <>
-__device__ __forceinline__ void store_f<__nv_bfloat16>(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+// Rounds once, to nearest even, from the accumulator type to the storage type.
+__device__ __forceinline__ void store_f(float *p, double x) { *p = __double2float_rn(x); }
+__device__ __forceinline__ void store_f(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_f(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float fma_acc(float a, float b, float c) { return fmaf(a, b, c); }
+__device__ __forceinline__ double fma_acc(double a, double b, double c) { return fma(a, b, c); }
 
 // Thread layout over a D x EB block of a state X[r][col]: thread t owns column col = t % EB and the
 // reduction indices r = p + NP * m (p = t / EB, m < RPT).
-template <int D>
+template <int D, typename Acc>
 struct Cfg {
     static constexpr int EB = D < 64 ? D : 64;  // output columns per block
     static constexpr int NP = kThreads / EB;     // parts of the reduction dimension
     static constexpr int RPT = D / NP;           // state entries per thread
-    static constexpr int RB = D >= 256 ? 16 : 32;  // rows staged in shared memory per batch
+    static constexpr int RB = sizeof(Acc) == 8 ? (D >= 256 ? 8 : 16) : (D >= 256 ? 16 : 32);  // staged rows
     static constexpr int NBLK = D / EB;
     static_assert(RPT >= 1 && NP * RPT == D, "bad SIMT layout");
 };
 
-enum Mode : int { kFwdO = 0, kBwdDQ = 1, kBwdDK = 2, kBwdDV = 3 };
+enum Mode : int { kFwdO = 0, kBwdDQ = 1, kBwdDK = 2, kBwdDV = 3, kFwdDelta = 4 };
 enum AggMode : int { kAggFwd = 0, kAggRev = 1 };
 
 struct Args {
     const void *Q, *K, *V, *O, *dO;
     void *out;          // O, dQ, dK or dV
     float *g_out;       // forward: optional normaliser output
-    float *rs_g;        // workspace row statistics: g_i and delta_i, [BH * N]
-    float *rs_delta;
-    float *states;      // workspace segment states, [BH][nseg][stride]
+    void *rs_g;         // workspace row statistics g_i and delta_i, [BH * N] of the accumulator type
+    void *rs_delta;
+    void *rs_dpart;     // per-column-block partial sums of dO_i . O_i, [NBLK][BH * N]
+    void *states;       // workspace segment states, [BH][nseg][stride] of the accumulator type
     long long N;
+    long long BHN;
     long long stride;
     int nseg, seg_len, causal;
 };
@@ -69,14 +71,14 @@ struct Args {
 //   kAggRev: u = q, w = dO / g      -> P block, y = sum (delta/g) q, e = sum dO / g
 // grid = (nseg * BH, NBLK); the vector sums are written by column block 0.
 // ------------------------------------------------------------------------------------------------
-template <typename T, int D, int AM>
+template <typename T, typename Acc, int D, int AM>
 __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
-    using C = Cfg<D>;
-    extern __shared__ float smem[];
-    float *sU = smem;                  // [RB][D]
-    float *sW = sU + C::RB * D;        // [RB][D]
-    float *sSc = sW + C::RB * D;       // [RB] 1/g   (rev)
-    float *sDt = sSc + C::RB;          // [RB] delta/g (rev)
+    using C = Cfg<D, Acc>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Acc *sU = reinterpret_cast<Acc *>(smem_raw);  // [RB][D]
+    Acc *sW = sU + C::RB * D;                     // [RB][D]
+    Acc *sSc = sW + C::RB * D;                    // [RB] 1/g   (rev)
+    Acc *sDt = sSc + C::RB;                       // [RB] delta/g (rev)
 
     const int t = threadIdx.x, col = t % C::EB, p = t / C::EB;
     const int colg = blockIdx.y * C::EB + col;
@@ -86,26 +88,27 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
     const long long r1 = min((long long)a.N, r0 + a.seg_len);
     const T *U = (const T *)(AM == kAggFwd ? a.K : a.Q) + bh * a.N * D;
     const T *W = (const T *)(AM == kAggFwd ? a.V : a.dO) + bh * a.N * D;
+    const Acc *rs_g = (const Acc *)a.rs_g, *rs_delta = (const Acc *)a.rs_delta;
 
-    float X[C::RPT];
+    Acc X[C::RPT];
 #pragma unroll
-    for (int m = 0; m < C::RPT; ++m) X[m] = 0.f;
-    float vu = 0.f, vw = 0.f;  // vector sums for index t (t < D), block 0 only
+    for (int m = 0; m < C::RPT; ++m) X[m] = Acc(0);
+    Acc vu = Acc(0), vw = Acc(0);  // vector sums for index t (t < D), block 0 only
 
     for (long long b0 = r0; b0 < r1; b0 += C::RB) {
         const int nb = (int)min((long long)C::RB, r1 - b0);
         if (AM == kAggRev && t < nb) {
-            const float gi = a.rs_g[bh * a.N + b0 + t];
-            sSc[t] = 1.f / gi;
-            sDt[t] = a.rs_delta[bh * a.N + b0 + t] / gi;
+            const Acc gi = rs_g[bh * a.N + b0 + t];
+            sSc[t] = Acc(1) / gi;
+            sDt[t] = rs_delta[bh * a.N + b0 + t] / gi;
         }
         if (AM == kAggRev) __syncthreads();
         for (int idx = t; idx < C::RB * D; idx += kThreads) {
             const int r = idx / D, d = idx % D;
-            float u = 0.f, w = 0.f;
+            Acc u = Acc(0), w = Acc(0);
             if (r < nb) {
-                u = load_f(U + (b0 + r) * D + d);
-                w = load_f(W + (b0 + r) * D + d);
+                u = (Acc)load_f(U + (b0 + r) * D + d);
+                w = (Acc)load_f(W + (b0 + r) * D + d);
                 if (AM == kAggRev) w *= sSc[r];
             }
             sU[idx] = u;
@@ -113,23 +116,23 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
         }
         __syncthreads();
         for (int r = 0; r < nb; ++r) {
-            const float wv = sW[r * D + colg];
+            const Acc wv = sW[r * D + colg];
 #pragma unroll
-            for (int m = 0; m < C::RPT; ++m) X[m] = fmaf(sU[r * D + p + C::NP * m], wv, X[m]);
+            for (int m = 0; m < C::RPT; ++m) X[m] = fma_acc(sU[r * D + p + C::NP * m], wv, X[m]);
         }
         if (blockIdx.y == 0 && t < D) {
             for (int r = 0; r < nb; ++r) {
                 if (AM == kAggFwd) {
                     vu += sU[r * D + t];
                 } else {
-                    vu = fmaf(sDt[r], sU[r * D + t], vu);
+                    vu = fma_acc(sDt[r], sU[r * D + t], vu);
                 }
                 vw += sW[r * D + t];
             }
         }
         __syncthreads();
     }
-    float *st = a.states + (bh * a.nseg + s) * a.stride;
+    Acc *st = (Acc *)a.states + (bh * a.nseg + s) * a.stride;
 #pragma unroll
     for (int m = 0; m < C::RPT; ++m) st[(long long)(p + C::NP * m) * D + colg] = X[m];
     if (blockIdx.y == 0 && t < D) {
@@ -145,30 +148,31 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
 //   non-causal: every segment gets the total.
 // grid = (ceil(used / 256), BH).
 // ------------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) simt_scan(float *states, int nseg, long long stride, long long used,
+template <typename Acc>
+__global__ void __launch_bounds__(kThreads) simt_scan(Acc *states, int nseg, long long stride, long long used,
                                                       int causal, int reverse) {
     const long long x = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (x >= used) return;
-    float *base = states + (long long)blockIdx.y * nseg * stride + x;
+    Acc *base = states + (long long)blockIdx.y * nseg * stride + x;
     if (!causal) {
-        float tot = 0.f;
+        Acc tot = Acc(0);
         for (int s = 0; s < nseg; ++s) tot += base[s * stride];
         for (int s = 0; s < nseg; ++s) base[s * stride] = tot;
         return;
     }
-    float run = 0.f;
+    Acc run = Acc(0);
     for (int k = 0; k < nseg; ++k) {
         const int s = reverse ? nseg - 1 - k : k;
-        const float v = base[s * stride];
+        const Acc v = base[s * stride];
         base[s * stride] = run;
         run += v;
     }
 }
 
-
-__device__ __forceinline__ float warp_dot(const float *x, const float *y, int D, int lane) {
-    float acc = 0.f;
-    for (int d = lane; d < D; d += 32) acc = fmaf(x[d], y[d], acc);
+template <typename Acc>
+__device__ __forceinline__ Acc warp_dot(const Acc *x, const Acc *y, int D, int lane) {
+    Acc acc = Acc(0);
+    for (int d = lane; d < D; d += 32) acc = fma_acc(x[d], y[d], acc);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     return acc;
@@ -182,25 +186,27 @@ __device__ __forceinline__ float warp_dot(const float *x, const float *y, int D,
 //   kBwdDQ: X[e][d] = S,  u = v,      w = k,      t = dO/g     -> dQ = X^T t - (delta/g) z
 //   kBwdDK: X[e][d] = P,  u = dO/g,   w = q,      t = v        -> dK = X^T t - y      (rows reversed)
 //   kBwdDV: X[d][e] = P,  u = q,      w = dO/g,   t = k        -> dV = e + X^T t      (rows reversed)
-// kBwdDQ also writes g_i and delta_i = dO_i . O_i to the workspace for kAggRev, kBwdDK and kBwdDV.
+//   kFwdDelta: as kFwdO, but instead of storing O it stores, per column block, sum_e dO_ie O_ie: the
+//             backward recomputes O_i in the accumulator precision rather than reading the rounded O.
+// kBwdDQ sums those partials into delta_i and writes g_i and delta_i for kAggRev, kBwdDK and kBwdDV.
 // grid = (nseg * BH, NBLK).
 // ------------------------------------------------------------------------------------------------
-template <typename T, int D, int MODE>
+template <typename T, typename Acc, int D, int MODE>
 __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
-    using C = Cfg<D>;
+    using C = Cfg<D, Acc>;
     constexpr int RB = C::RB;
     constexpr bool REV = (MODE == kBwdDK || MODE == kBwdDV);
-    extern __shared__ float smem[];
-    float *sA = smem;             // u rows [RB][D]
-    float *sB = sA + RB * D;      // w rows
-    float *sT = sB + RB * D;      // t rows
-    float *sX = sT + RB * D;      // dQ: O rows
-    float *sY = sX + RB * D;      // dQ: q rows
-    float *sRun = sY + RB * D;    // running vector after each row: z, z, y or e
-    float *sRun2 = sRun + RB * D; // forward: running a
-    float *sRed = sRun2 + RB * D; // [RB][NP][EB]
-    float *sG = sRed + RB * kThreads;
-    float *sDt = sG + RB;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Acc *sA = reinterpret_cast<Acc *>(smem_raw);  // u rows [RB][D]
+    Acc *sB = sA + RB * D;                        // w rows
+    Acc *sT = sB + RB * D;                        // t rows
+    Acc *sX = sT + RB * D;                        // dQ: O rows
+    Acc *sY = sX + RB * D;                        // dQ: q rows
+    Acc *sRun = sY + RB * D;                      // running vector after each row: z, z, y or e
+    Acc *sRun2 = sRun + RB * D;                   // forward: running a
+    Acc *sRed = sRun2 + RB * D;                   // [RB][NP][EB]
+    Acc *sG = sRed + RB * kThreads;
+    Acc *sDt = sG + RB;
 
     const int t = threadIdx.x, col = t % C::EB, p = t / C::EB;
     const int lane = t & 31, warp = t >> 5;
@@ -213,18 +219,20 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
     const long long hoff = bh * N * D;
     const T *Qh = (const T *)a.Q + hoff, *Kh = (const T *)a.K + hoff, *Vh = (const T *)a.V + hoff;
     const T *Oh = (const T *)a.O + hoff, *dOh = (const T *)a.dO + hoff;
-    const float *st = a.states + (bh * a.nseg + s) * a.stride;
+    const Acc *st = (const Acc *)a.states + (bh * a.nseg + s) * a.stride;
+    Acc *rs_g = (Acc *)a.rs_g, *rs_delta = (Acc *)a.rs_delta, *rs_dpart = (Acc *)a.rs_dpart;
+    constexpr bool FWD = (MODE == kFwdO || MODE == kFwdDelta);
 
-    float X[C::RPT];
+    Acc X[C::RPT];
 #pragma unroll
     for (int m = 0; m < C::RPT; ++m) {
         const int r = p + C::NP * m;
-        X[m] = (MODE == kFwdO || MODE == kBwdDV) ? st[(long long)r * D + colg] : st[(long long)colg * D + r];
+        X[m] = (FWD || MODE == kBwdDV) ? st[(long long)r * D + colg] : st[(long long)colg * D + r];
     }
-    float run1 = 0.f, run2 = 0.f;
+    Acc run1 = Acc(0), run2 = Acc(0);
     if (t < D) {
         run1 = (MODE == kBwdDV) ? st[(long long)D * D + D + t] : st[(long long)D * D + t];
-        if (MODE == kFwdO) run2 = st[(long long)D * D + D + t];
+        if (FWD) run2 = st[(long long)D * D + D + t];
     }
 
     const int nbatch = (int)((r1 - r0 + RB - 1) / RB);
@@ -233,35 +241,35 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
         const int nb = (int)(REV ? (r1 - (long long)bi * RB) - b0 : min((long long)RB, r1 - b0));
         if (REV) {
             if (t < nb) {
-                const float gi = a.rs_g[bh * N + b0 + t];
+                const Acc gi = rs_g[bh * N + b0 + t];
                 sG[t] = gi;
-                sDt[t] = a.rs_delta[bh * N + b0 + t] / gi;
+                sDt[t] = rs_delta[bh * N + b0 + t] / gi;
             }
             __syncthreads();
         }
-        // phase 1: stage the batch's rows as fp32
+        // phase 1: stage the batch's rows in the accumulator type
         for (int idx = t; idx < RB * D; idx += kThreads) {
             const int r = idx / D, d = idx % D;
             const bool ok = r < nb;
             const long long o = (b0 + r) * D + d;
-            if (MODE == kFwdO) {
-                sA[idx] = ok ? load_f(Kh + o) : 0.f;
-                sB[idx] = ok ? load_f(Vh + o) : 0.f;
-                sT[idx] = ok ? load_f(Qh + o) : 0.f;
+            if (FWD) {
+                sA[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
+                if (MODE == kFwdDelta) sX[idx] = ok ? (Acc)load_f(dOh + o) : Acc(0);
             } else if (MODE == kBwdDQ) {
-                sA[idx] = ok ? load_f(Vh + o) : 0.f;
-                sB[idx] = ok ? load_f(Kh + o) : 0.f;
-                sT[idx] = ok ? load_f(dOh + o) : 0.f;
-                sX[idx] = ok ? load_f(Oh + o) : 0.f;
-                sY[idx] = ok ? load_f(Qh + o) : 0.f;
+                sA[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(dOh + o) : Acc(0);
+                sY[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
             } else if (MODE == kBwdDK) {
-                sA[idx] = ok ? load_f(dOh + o) / sG[r] : 0.f;
-                sB[idx] = ok ? load_f(Qh + o) : 0.f;
-                sT[idx] = ok ? load_f(Vh + o) : 0.f;
+                sA[idx] = ok ? (Acc)load_f(dOh + o) / sG[r] : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
             } else {
-                sA[idx] = ok ? load_f(Qh + o) : 0.f;
-                sB[idx] = ok ? load_f(dOh + o) / sG[r] : 0.f;
-                sT[idx] = ok ? load_f(Kh + o) : 0.f;
+                sA[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(dOh + o) / sG[r] : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
             }
         }
         __syncthreads();
@@ -270,41 +278,42 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
             for (int k = 0; k < nb; ++k) {
                 const int r = REV ? nb - 1 - k : k;
                 if (a.causal) {
-                    if (MODE == kFwdO) {
+                    if (FWD) {
                         run1 += sA[r * D + t];
                         run2 += sB[r * D + t];
                     } else if (MODE == kBwdDQ) {
                         run1 += sB[r * D + t];
                     } else if (MODE == kBwdDK) {
-                        run1 = fmaf(sDt[r], sB[r * D + t], run1);
+                        run1 = fma_acc(sDt[r], sB[r * D + t], run1);
                     } else {
                         run1 += sB[r * D + t];
                     }
                 }
                 sRun[r * D + t] = run1;
-                if (MODE == kFwdO) sRun2[r * D + t] = run2;
+                if (FWD) sRun2[r * D + t] = run2;
             }
         }
         __syncthreads();
         // per-row scalars of the forward-direction walks
         if (!REV) {
             for (int r = warp; r < nb; r += kThreads / 32) {
-                const float n = a.causal ? (float)(b0 + r + 1) : (float)N;
-                if (MODE == kFwdO) {
-                    const float gi = n + warp_dot(sT + r * D, sRun + r * D, D, lane);
+                const Acc n = a.causal ? (Acc)(b0 + r + 1) : (Acc)N;
+                if (FWD) {
+                    const Acc gi = n + warp_dot(sT + r * D, sRun + r * D, D, lane);
                     if (lane == 0) {
                         sG[r] = gi;
-                        if (a.g_out && blockIdx.y == 0) a.g_out[bh * N + b0 + r] = gi;
+                        if (MODE == kFwdO && a.g_out && blockIdx.y == 0) a.g_out[bh * N + b0 + r] = (float)gi;
                     }
                 } else {
-                    const float gi = n + warp_dot(sY + r * D, sRun + r * D, D, lane);
-                    const float delta = warp_dot(sT + r * D, sX + r * D, D, lane);
+                    const Acc gi = n + warp_dot(sY + r * D, sRun + r * D, D, lane);
+                    Acc delta = Acc(0);
+                    for (int q = 0; q < C::NBLK; ++q) delta += rs_dpart[(long long)q * a.BHN + bh * N + b0 + r];
                     if (lane == 0) {
                         sG[r] = gi;
                         sDt[r] = delta / gi;
                         if (blockIdx.y == 0) {
-                            a.rs_g[bh * N + b0 + r] = gi;
-                            a.rs_delta[bh * N + b0 + r] = delta;
+                            rs_g[bh * N + b0 + r] = gi;
+                            rs_delta[bh * N + b0 + r] = delta;
                         }
                     }
                 }
@@ -319,23 +328,23 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
         for (int k = 0; k < nb; ++k) {
             const int r = REV ? nb - 1 - k : k;
             if (a.causal) {
-                const float wv = sB[r * D + colg];
+                const Acc wv = sB[r * D + colg];
 #pragma unroll
-                for (int m = 0; m < C::RPT; ++m) X[m] = fmaf(sA[r * D + p + C::NP * m], wv, X[m]);
+                for (int m = 0; m < C::RPT; ++m) X[m] = fma_acc(sA[r * D + p + C::NP * m], wv, X[m]);
             }
-            float part = 0.f;
+            Acc part = Acc(0);
 #pragma unroll
-            for (int m = 0; m < C::RPT; ++m) part = fmaf(sT[r * D + p + C::NP * m], X[m], part);
+            for (int m = 0; m < C::RPT; ++m) part = fma_acc(sT[r * D + p + C::NP * m], X[m], part);
             sRed[(r * C::NP + p) * C::EB + col] = part;
         }
         __syncthreads();
         // phase 4: finish the rows r = p (mod NP)
         for (int r = p; r < nb; r += C::NP) {
-            float tot = 0.f;
+            Acc tot = Acc(0);
 #pragma unroll 4
             for (int q = 0; q < C::NP; ++q) tot += sRed[(r * C::NP + q) * C::EB + col];
-            float v;
-            if (MODE == kFwdO) {
+            Acc v;
+            if (FWD) {
                 v = (sRun2[r * D + colg] + tot) / sG[r];
             } else if (MODE == kBwdDQ) {
                 v = tot - sDt[r] * sRun[r * D + colg];
@@ -344,17 +353,31 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
             } else {
                 v = sRun[r * D + colg] + tot;
             }
-            store_f((T *)a.out + hoff + (b0 + r) * D + colg, v);
+            if (MODE == kFwdDelta) {
+                sRun[r * C::EB + col] = v * sX[r * D + colg];  // sRun (z rows) is dead in phase 4
+            } else {
+                store_f((T *)a.out + hoff + (b0 + r) * D + colg, v);
+            }
+        }
+        if (MODE == kFwdDelta) {
+            __syncthreads();
+            if (t < nb) {
+                Acc dsum = Acc(0);
+                for (int c = 0; c < C::EB; ++c) dsum += sRun[t * C::EB + c];
+                rs_dpart[(long long)blockIdx.y * a.BHN + bh * N + b0 + t] = dsum;
+            }
         }
         __syncthreads();
     }
 }
 
-template <int D>
-constexpr size_t agg_smem() { return (size_t)(2 * Cfg<D>::RB * D + 2 * Cfg<D>::RB) * sizeof(float); }
-template <int D>
+template <int D, typename Acc>
+constexpr size_t agg_smem() {
+    return (size_t)(2 * Cfg<D, Acc>::RB * D + 2 * Cfg<D, Acc>::RB) * sizeof(Acc);
+}
+template <int D, typename Acc>
 constexpr size_t rows_smem() {
-    return (size_t)(7 * Cfg<D>::RB * D + Cfg<D>::RB * kThreads + 2 * Cfg<D>::RB) * sizeof(float);
+    return (size_t)(7 * Cfg<D, Acc>::RB * D + Cfg<D, Acc>::RB * kThreads + 2 * Cfg<D, Acc>::RB) * sizeof(Acc);
 }
 
 template <typename K>
@@ -371,9 +394,11 @@ Args make_args(const Plan &p, const void *Q, const void *K, const void *V, const
     a.V = V;
     a.O = O;
     a.dO = dO;
-    a.states = (float *)(ws + p.off_states);
-    a.rs_g = (float *)(ws + p.off_rowstats);
-    a.rs_delta = a.rs_g + (size_t)p.BH * p.N;
+    a.states = ws + p.off_states;
+    a.rs_g = ws + p.off_rowstats;
+    a.rs_delta = ws + p.off_rowstats + (size_t)p.BH * p.N * p.acc_bytes;
+    a.rs_dpart = ws + p.off_rowstats + 2 * (size_t)p.BH * p.N * p.acc_bytes;
+    a.BHN = (long long)p.BH * p.N;
     a.N = p.N;
     a.stride = p.stride;
     a.nseg = p.nseg;
@@ -382,72 +407,75 @@ Args make_args(const Plan &p, const void *Q, const void *K, const void *V, const
     return a;
 }
 
-template <typename T, int D>
+template <typename T, typename Acc, int D>
 cudaError_t forward_impl(const Plan &p, Args a, void *O, float *g, cudaStream_t s) {
-    using C = Cfg<D>;
+    using C = Cfg<D, Acc>;
     const dim3 grid((unsigned)(p.nseg * p.BH), C::NBLK);
     const long long used = (long long)D * D + 2 * D;
     cudaError_t e;
-    if ((e = allow_smem(simt_aggregate<T, D, kAggFwd>, agg_smem<D>())) != cudaSuccess) return e;
-    if ((e = allow_smem(simt_rows<T, D, kFwdO>, rows_smem<D>())) != cudaSuccess) return e;
-    simt_aggregate<T, D, kAggFwd><<<grid, kThreads, agg_smem<D>(), s>>>(a);
-    simt_scan<<<dim3((unsigned)((used + kThreads - 1) / kThreads), p.BH), kThreads, 0, s>>>(
-        a.states, p.nseg, p.stride, used, p.causal, 0);
+    if ((e = allow_smem(simt_aggregate<T, Acc, D, kAggFwd>, agg_smem<D, Acc>())) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, Acc, D, kFwdO>, rows_smem<D, Acc>())) != cudaSuccess) return e;
+    simt_aggregate<T, Acc, D, kAggFwd><<<grid, kThreads, agg_smem<D, Acc>(), s>>>(a);
+    simt_scan<Acc><<<dim3((unsigned)((used + kThreads - 1) / kThreads), p.BH), kThreads, 0, s>>>(
+        (Acc *)a.states, p.nseg, p.stride, used, p.causal, 0);
     a.out = O;
     a.g_out = g;
-    simt_rows<T, D, kFwdO><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    simt_rows<T, Acc, D, kFwdO><<<grid, kThreads, rows_smem<D, Acc>(), s>>>(a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(3);
     return e;
 }
 
-template <typename T, int D>
+template <typename T, typename Acc, int D>
 cudaError_t backward_impl(const Plan &p, Args a, void *dQ, void *dK, void *dV, cudaStream_t s) {
-    using C = Cfg<D>;
+    using C = Cfg<D, Acc>;
     const dim3 grid((unsigned)(p.nseg * p.BH), C::NBLK);
     const long long used = (long long)D * D + 2 * D;
     const dim3 sgrid((unsigned)((used + kThreads - 1) / kThreads), p.BH);
+    const size_t sa = agg_smem<D, Acc>(), sr = rows_smem<D, Acc>();
     cudaError_t e;
-    if ((e = allow_smem(simt_aggregate<T, D, kAggFwd>, agg_smem<D>())) != cudaSuccess) return e;
-    if ((e = allow_smem(simt_aggregate<T, D, kAggRev>, agg_smem<D>())) != cudaSuccess) return e;
-    if ((e = allow_smem(simt_rows<T, D, kBwdDQ>, rows_smem<D>())) != cudaSuccess) return e;
-    if ((e = allow_smem(simt_rows<T, D, kBwdDK>, rows_smem<D>())) != cudaSuccess) return e;
-    if ((e = allow_smem(simt_rows<T, D, kBwdDV>, rows_smem<D>())) != cudaSuccess) return e;
-    simt_aggregate<T, D, kAggFwd><<<grid, kThreads, agg_smem<D>(), s>>>(a);
-    simt_scan<<<sgrid, kThreads, 0, s>>>(a.states, p.nseg, p.stride, used, p.causal, 0);
+    if ((e = allow_smem(simt_aggregate<T, Acc, D, kAggFwd>, sa)) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_aggregate<T, Acc, D, kAggRev>, sa)) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, Acc, D, kFwdDelta>, sr)) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, Acc, D, kBwdDQ>, sr)) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, Acc, D, kBwdDK>, sr)) != cudaSuccess) return e;
+    if ((e = allow_smem(simt_rows<T, Acc, D, kBwdDV>, sr)) != cudaSuccess) return e;
+    simt_aggregate<T, Acc, D, kAggFwd><<<grid, kThreads, sa, s>>>(a);
+    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 0);
+    simt_rows<T, Acc, D, kFwdDelta><<<grid, kThreads, sr, s>>>(a);
     a.out = dQ;
-    simt_rows<T, D, kBwdDQ><<<grid, kThreads, rows_smem<D>(), s>>>(a);
-    simt_aggregate<T, D, kAggRev><<<grid, kThreads, agg_smem<D>(), s>>>(a);
-    simt_scan<<<sgrid, kThreads, 0, s>>>(a.states, p.nseg, p.stride, used, p.causal, 1);
+    simt_rows<T, Acc, D, kBwdDQ><<<grid, kThreads, sr, s>>>(a);
+    simt_aggregate<T, Acc, D, kAggRev><<<grid, kThreads, sa, s>>>(a);
+    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 1);
     a.out = dK;
-    simt_rows<T, D, kBwdDK><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    simt_rows<T, Acc, D, kBwdDK><<<grid, kThreads, sr, s>>>(a);
     a.out = dV;
-    simt_rows<T, D, kBwdDV><<<grid, kThreads, rows_smem<D>(), s>>>(a);
+    simt_rows<T, Acc, D, kBwdDV><<<grid, kThreads, sr, s>>>(a);
     e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(7);
+    if (e == cudaSuccess) count_launches(8);
     return e;
 }
 
-template <typename T>
+template <typename T, typename Acc>
 cudaError_t forward_t(const Plan &p, Args a, void *O, float *g, cudaStream_t s) {
     switch (p.D) {
-        case 16: return forward_impl<T, 16>(p, a, O, g, s);
-        case 32: return forward_impl<T, 32>(p, a, O, g, s);
-        case 64: return forward_impl<T, 64>(p, a, O, g, s);
-        case 128: return forward_impl<T, 128>(p, a, O, g, s);
-        case 256: return forward_impl<T, 256>(p, a, O, g, s);
+        case 16: return forward_impl<T, Acc, 16>(p, a, O, g, s);
+        case 32: return forward_impl<T, Acc, 32>(p, a, O, g, s);
+        case 64: return forward_impl<T, Acc, 64>(p, a, O, g, s);
+        case 128: return forward_impl<T, Acc, 128>(p, a, O, g, s);
+        case 256: return forward_impl<T, Acc, 256>(p, a, O, g, s);
         default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T>
+template <typename T, typename Acc>
 cudaError_t backward_t(const Plan &p, Args a, void *dQ, void *dK, void *dV, cudaStream_t s) {
     switch (p.D) {
-        case 16: return backward_impl<T, 16>(p, a, dQ, dK, dV, s);
-        case 32: return backward_impl<T, 32>(p, a, dQ, dK, dV, s);
-        case 64: return backward_impl<T, 64>(p, a, dQ, dK, dV, s);
-        case 128: return backward_impl<T, 128>(p, a, dQ, dK, dV, s);
-        case 256: return backward_impl<T, 256>(p, a, dQ, dK, dV, s);
+        case 16: return backward_impl<T, Acc, 16>(p, a, dQ, dK, dV, s);
+        case 32: return backward_impl<T, Acc, 32>(p, a, dQ, dK, dV, s);
+        case 64: return backward_impl<T, Acc, 64>(p, a, dQ, dK, dV, s);
+        case 128: return backward_impl<T, Acc, 128>(p, a, dQ, dK, dV, s);
+        case 256: return backward_impl<T, Acc, 256>(p, a, dQ, dK, dV, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -457,13 +485,14 @@ cudaError_t backward_t(const Plan &p, Args a, void *dQ, void *dK, void *dV, cuda
 cudaError_t simt_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
                          unsigned char *ws, cudaStream_t s) {
     Args a = make_args(p, Q, K, V, nullptr, nullptr, ws);
-    return p.dtype == 1 ? forward_t<__nv_bfloat16>(p, a, O, g, s) : forward_t<float>(p, a, O, g, s);
+    return p.dtype == 1 ? forward_t<__nv_bfloat16, float>(p, a, O, g, s) : forward_t<float, double>(p, a, O, g, s);
 }
 
 cudaError_t simt_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
                           const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s) {
     Args a = make_args(p, Q, K, V, O, dO, ws);
-    return p.dtype == 1 ? backward_t<__nv_bfloat16>(p, a, dQ, dK, dV, s) : backward_t<float>(p, a, dQ, dK, dV, s);
+    return p.dtype == 1 ? backward_t<__nv_bfloat16, float>(p, a, dQ, dK, dV, s)
+                        : backward_t<float, double>(p, a, dQ, dK, dV, s);
 }
 
 }  // namespace la

@@ -92,7 +92,10 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
  *   dQ, dK, dV      out: [B,H,N,D] of `dtype`, the gradients of L = sum dO . O
  *   causal          in : must match the forward call
  *   workspace       in/out: workspace_bytes >= la_workspace_bytes(..., backward = 1)
- * The normaliser is recomputed, not read.  Pointers must be 16-byte aligned.
+ * O must be a valid buffer but is not read: the backward recomputes the normaliser g_i and the row
+ * terms delta_i = dO_i . O_i from Q, K and V in its accumulator precision, which is both exact to that
+ * precision (the stored O is rounded to `dtype`) and one tensor read fewer.  Pointers must be 16-byte
+ * aligned.
  */
 int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
                 void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,

@@ -1,0 +1,101 @@
+// la_tc_common.cuh -- work decomposition and small helpers shared by the tensor-core (tcgen05) kernels.
+//
+// Work split.  A head's N rows are cut into chunks of kC = 128 rows (the M of one tcgen05 MMA).  All
+// (head, chunk) pairs are laid end to end, head-major, and the resulting list of T chunks is cut into
+// G contiguous slices, one per CTA: CTA b owns chunks [lo(b), lo(b+1)) with lo(b) = floor(b T / G).
+// With 64 heads and 152 SMs this keeps every SM busy (each slice is ~13.5 chunks and may straddle a head
+// boundary) where one CTA per head would leave most SMs idle.  The part of a slice that lies in one head
+// is a "piece".  A piece's D x D state sum is stored in workspace slot (head + b): the slots of one CTA's
+// pieces are consecutive and never collide with another CTA's, and a head's slots are found from the
+// CTAs that cover it.  Later kernels add the slots of a head's earlier (or later) pieces to obtain the
+// state carried into a piece, so no CTA ever waits for another inside a kernel.
+#pragma once
+
+#include <stdint.h>
+
+#include "la_sm100.cuh"
+
+namespace la {
+namespace tc {
+
+constexpr int kC = 128;               // rows per chunk
+constexpr int kMaxCtas = 256;         // upper bound on G used to size the workspace
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single barrier wait
+
+struct Slices {
+    long long T;  // total chunks = BH * nchunk
+    int G;        // CTAs
+    int nchunk;   // chunks per head
+};
+
+__host__ __device__ __forceinline__ long long slice_lo(const Slices &s, int b) { return (long long)b * s.T / s.G; }
+
+// The CTA whose slice contains flat chunk x.
+__device__ __forceinline__ int cta_of(const Slices &s, long long x) {
+    int b = (int)((x * s.G) / s.T);
+    while (b > 0 && slice_lo(s, b) > x) --b;
+    while (b + 1 < s.G && slice_lo(s, b + 1) <= x) ++b;
+    return b;
+}
+
+// Workspace slot of CTA b's piece of head h.
+__host__ __device__ __forceinline__ long long slot_of(long long h, int b) { return h + b; }
+
+struct Piece {
+    long long h;  // head (b * H + h flattened)
+    int a, e;     // chunk range [a, e) within the head
+};
+
+// Iterates over the pieces of CTA b's slice: call first(), then next() while valid.
+struct PieceIter {
+    long long x, hi;
+    int nchunk;
+    __device__ __forceinline__ PieceIter(const Slices &s, int b)
+        : x(slice_lo(s, b)), hi(slice_lo(s, b + 1)), nchunk(s.nchunk) {}
+    __device__ __forceinline__ bool valid() const { return x < hi; }
+    __device__ __forceinline__ Piece get() const {
+        Piece p;
+        p.h = x / nchunk;
+        p.a = (int)(x - p.h * nchunk);
+        const long long hend = (p.h + 1) * nchunk;
+        p.e = (int)((hi < hend ? hi : hend) - p.h * nchunk);
+        return p;
+    }
+    __device__ __forceinline__ void next() {
+        const Piece p = get();
+        x = p.h * nchunk + p.e;
+    }
+};
+
+// Records the first device-side error in the workspace status word (first error wins).
+__device__ __forceinline__ void report(uint32_t *status, uint32_t code, uint32_t where) {
+    if (atomicCAS(status, 0u, code) == 0u) status[1] = where;
+}
+
+// Barrier wait bounded in time and aborted early when another role of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t *status, uint32_t where) {
+    if (sm100::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = sm100::globaltimer_ns();
+    while (true) {
+        if (sm100::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (sm100::globaltimer_ns() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            report(status, 5u, where);
+            return false;
+        }
+    }
+}
+
+// Byte offset of the 16-byte group holding element column `col8 * 8` of row `row` in a tile written by
+// TMA with the 128-byte swizzle (rows of 128 bytes = 64 bf16; group index XOR row % 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col8) {
+    return (uint32_t)row * 128u + (uint32_t)(((col8 ^ row) & 7) << 4);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+}  // namespace tc
+}  // namespace la

@@ -2,9 +2,11 @@
 
 Tolerances (fixed for this method; the forward and backward are one rounding of an fp32-accumulated
 result for bf16 I/O):
-  * fp32 I/O: elementwise |x - r| / max(|r|, 1e-3 max|r|) <= 1e-5 per tensor;
-  * bf16 I/O: max|x - r| / max|r| <= 2e-2 per tensor (O, dQ, dK, dV);
+  * fp32 I/O: elementwise |x - r| / max(|r|, 1e-3 max|r|, 1e-6) <= 1e-5 per tensor;
+  * bf16 I/O: max|x - r| / max(max|r|, 1e-3) <= 2e-2 per tensor (O, dQ, dK, dV);
   * normaliser (fp32 output in both cases): elementwise relative 1e-5 (fp32 I/O) or 1e-3 (bf16 I/O).
+The absolute floors only matter where a reference tensor is exactly zero (dQ at N = 1 is 0 by the
+definition); every tensor here is O(1) in scale (Q, K ~ N(0, 1/D), V, dO ~ N(0, 1)).
 """
 from __future__ import annotations
 
@@ -49,13 +51,13 @@ def run_library(x: dict, dtype: str, causal: bool, backward: bool = True):
 
 def err_rel_elem(x: np.ndarray, r: np.ndarray) -> float:
     floor = 1e-3 * float(np.max(np.abs(r))) if r.size else 0.0
-    den = np.maximum(np.abs(r), max(floor, 1e-300))
+    den = np.maximum(np.abs(r), max(floor, 1e-6))
     return float(np.max(np.abs(x - r) / den)) if r.size else 0.0
 
 
 def err_norm_maxabs(x: np.ndarray, r: np.ndarray) -> float:
     m = float(np.max(np.abs(r))) if r.size else 0.0
-    return float(np.max(np.abs(x - r)) / max(m, 1e-300)) if r.size else 0.0
+    return float(np.max(np.abs(x - r)) / max(m, 1e-3)) if r.size else 0.0
 
 
 def tensor_error(x, r, dtype: str) -> float:

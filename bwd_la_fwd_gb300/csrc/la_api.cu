@@ -6,6 +6,7 @@
 
 #include "../../include/la.h"
 #include "la_internal.h"
+#include "la_tc_host.h"
 
 namespace la {
 
@@ -40,9 +41,10 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     p->nseg = (int)(((long long)N + seg - 1) / seg);
     if (BH * p->nseg >= (1LL << 31)) return false;
     p->stride = (long long)round_up((size_t)D * D + 2 * (size_t)D, 64);
-    p->use_tc = false;
     p->acc_bytes = dtype == LA_F32 ? 8 : 4;
-    const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
+    p->use_tc = tc_supported(*p);
+    size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
+    if (p->use_tc && tc_slot_bytes(*p) > states) states = tc_slot_bytes(*p);
     const size_t flags = (size_t)BH * p->nseg * sizeof(uint32_t);
     p->off_states = 256;
     p->off_flags = round_up(p->off_states + states, 256);
@@ -131,7 +133,8 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
     Range outs[2] = {range_of(O, tb), range_of(normaliser, normaliser ? (size_t)p.BH * N * 4 : 0)};
     if ((rc = check_aliasing(outs, normaliser ? 2 : 1, ins, 4))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = la::simt_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s);
+    cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s)
+                             : la::simt_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

@@ -1,0 +1,38 @@
+// la_tc_host.h -- parameters of the tensor-core kernels and the host entry points that launch them.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "la_internal.h"
+#include "la_tc_common.cuh"
+
+namespace la {
+namespace tc {
+
+// Kernel parameters (passed as a __grid_constant__ struct; the tensor maps stay in parameter space).
+struct TcParams {
+    CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D maps over [BH][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
+    Slices sl;
+    long long N;
+    float *slots;           // per-piece state sums, slot stride `slot_stride` floats
+    float *slots_rev;       // backward: per-piece reverse-direction sums
+    long long slot_stride;
+    uint32_t *status;       // workspace status word
+    void *O;                // forward output (bf16)
+    float *g;               // forward normaliser (may be null)
+    void *dQ, *dK, *dV;     // backward outputs (bf16)
+    float *rs_g, *rs_dt;    // backward row statistics: g_i and delta_i / g_i
+};
+
+}  // namespace tc
+
+// bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.
+bool tc_supported(const Plan &p);
+// Workspace bytes the tensor-core path needs for its state slots (one direction).
+size_t tc_slot_bytes(const Plan &p);
+cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
+                       unsigned char *ws, cudaStream_t s);
+
+}  // namespace la

@@ -46,6 +46,14 @@ def test_many_heads_short_sequences(oracle_lib, D):
     _check(oracle_lib, 3, 5, 130, D, "bf16", 1, seed=21)
 
 
+@pytest.mark.parametrize("causal", [1, 0])
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+def test_multi_chunk_slices(oracle_lib, monkeypatch, ctas, causal):
+    """Few CTAs, so that each one walks several chunks and pieces of several heads (tensor-core path)."""
+    monkeypatch.setenv("LA_TC_MAX_CTAS", str(ctas))
+    _check(oracle_lib, 1, 3, 549, 128, "bf16", causal, seed=31 + ctas)
+
+
 def test_repeatable_and_workspace_reusable():
     """Two calls on one workspace give bit-identical results (no state leaks between calls)."""
     import torch

@@ -1,0 +1,63 @@
+// la_noalloc.cu -- la_forward_noalloc: the forward pass for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain the workspace la_forward needs: a plugin that a host framework hands
+// only input and output pointers (the framework owns every allocation), latency-critical code that must
+// not call cudaMalloc because it can block and synchronise the whole device, or a program whose device
+// memory budget is fixed when it loads.  For them this entry point runs the same forward kernels with a
+// workspace that lives in a fixed device array compiled into the library, so it allocates nothing.
+//
+// The first call on each device looks the array's device address up (cudaGetSymbolAddress); make that
+// first call before any stream capture begins.  Every call on a device shares the one array, so calls
+// whose work overlaps on the GPU (different streams, or different host threads) race with each other.
+//
+// The array below has static storage: every device on which this part of the library is loaded keeps
+// LA_NOALLOC_SCRATCH_BYTES reserved until the process exits.  In host code its name is only a host-side
+// stand-in for the symbol, not a device address, so the device address is looked up once per device with
+// cudaGetSymbolAddress and passed to the kernels as an ordinary pointer.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/la.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+void *g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device (looked up on first use per device).
+int scratch_for_current_device(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" int la_forward_noalloc(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser,
+                                  int B, int H, int N, int D, int dtype, void *stream) {
+    const size_t need = la_workspace_bytes(B, H, N, D, causal, dtype, 0);
+    if (need == 0) {
+        // invalid or unsupported shape: let la_forward report which, before anything is enqueued
+        return la_forward(Q, K, V, causal, O, normaliser, B, H, N, D, dtype, nullptr, 0, stream);
+    }
+    if (need > (size_t)LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_WORKSPACE;  // beyond the fixed scratch size
+    void *ws = nullptr;
+    int rc = scratch_for_current_device(&ws);
+    if (rc != LA_OK) return rc;
+    // The scratch keeps whatever the previous call left in it.  Everything the forward reads is written
+    // earlier in the same call except the status header, which must start at zero: clear it on the stream.
+    if (cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
+    return la_forward(Q, K, V, causal, O, normaliser, B, H, N, D, dtype, ws, LA_NOALLOC_SCRATCH_BYTES, stream);
+}

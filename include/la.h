@@ -102,6 +102,23 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
                 size_t workspace_bytes, void *stream);
 
 /*
+ * Forward pass without a caller-supplied workspace, for callers that cannot allocate device memory (a
+ * plugin that its host framework gives only input and output buffers, code that must not call cudaMalloc
+ * because it can block and synchronise the device, a fixed memory budget).  The paper has no counterpart:
+ * this is a packaging variant of la_forward.  Arguments and results are those of la_forward; the scratch
+ * is a fixed device array of LA_NOALLOC_SCRATCH_BYTES inside the library, held on every device that loads
+ * it until the process exits.  Nothing is allocated.
+ *   - Returns LA_ERR_WORKSPACE, before enqueuing anything, when la_workspace_bytes(B, H, N, D, causal,
+ *     dtype, 0) exceeds LA_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's device address; make it before any stream capture.
+ *   - Each call clears the array's status word on `stream`; device-side status is not reported back.
+ *   - All calls on a device share the array: calls whose work overlaps on the GPU race.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int la_forward_noalloc(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B,
+                       int H, int N, int D, int dtype, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the sticky device status recorded in `workspace`
  * by earlier calls (LA_OK, LA_ERR_TIMEOUT or LA_ERR_BOUNDS), or LA_ERR_CUDA if the stream failed.
  */

@@ -43,8 +43,19 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     p->stride = (long long)round_up((size_t)D * D + 2 * (size_t)D, 64);
     p->acc_bytes = dtype == LA_F32 ? 8 : 4;
     p->use_tc = tc_supported(*p);
-    size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
-    if (p->use_tc && tc_slot_bytes(*p) > states) states = tc_slot_bytes(*p);
+    if (p->use_tc) {
+        // forward-direction slots (forward and backward), reverse-direction slots and per-row g, dt
+        // (backward only)
+        const size_t slots = tc_slot_bytes(*p);
+        p->off_states = 256;
+        p->off_states2 = round_up(p->off_states + slots, 256);
+        p->off_flags = round_up(p->off_states2 + slots, 256);
+        p->off_rowstats = p->off_flags;
+        p->bytes_fwd = p->off_states2;
+        p->bytes_bwd = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
+        return true;
+    }
+    const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
     const size_t flags = (size_t)BH * p->nseg * sizeof(uint32_t);
     p->off_states = 256;
     p->off_flags = round_up(p->off_states + states, 256);
@@ -157,7 +168,8 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
     const Range outs[] = {range_of(dQ, tb), range_of(dK, tb), range_of(dV, tb)};
     if ((rc = check_aliasing(outs, 3, ins, 6))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, (unsigned char *)workspace, s);
+    cudaError_t e = p.use_tc ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, (unsigned char *)workspace, s)
+                             : la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, (unsigned char *)workspace, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

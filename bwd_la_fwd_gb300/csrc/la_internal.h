@@ -30,6 +30,7 @@ struct Plan {
     long long stride;   // elements per segment state (S or P: D*D, then two D-vectors), padded
     int acc_bytes;      // accumulator element size: 4 (bf16 storage) or 8 (fp32 storage)
     size_t off_states;  // byte offsets of the workspace regions
+    size_t off_states2; // tensor-core backward: reverse-direction slots
     size_t off_flags;
     size_t off_rowstats;
     size_t bytes_fwd;   // workspace bytes for the forward / for the backward

@@ -28,11 +28,20 @@ struct TcParams {
 
 }  // namespace tc
 
+// Host helpers shared by the forward and backward launchers (la_tc_fwd.cu).
+namespace tc_host {
+bool make_map(CUtensorMap *m, const void *ptr, const Plan &p);
+bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
+cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
+}  // namespace tc_host
+
 // bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.
 bool tc_supported(const Plan &p);
 // Workspace bytes the tensor-core path needs for its state slots (one direction).
 size_t tc_slot_bytes(const Plan &p);
 cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
                        unsigned char *ws, cudaStream_t s);
+cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
+                        void *dK, void *dV, unsigned char *ws, cudaStream_t s);
 
 }  // namespace la

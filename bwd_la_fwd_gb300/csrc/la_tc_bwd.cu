@@ -85,6 +85,26 @@ __device__ __forceinline__ float2 weighted_colsum(const unsigned char *tile2, in
     return make_float2(s0, s1);
 }
 
+// Writes 16 fp32 values (x[c] + add_scale * add[c]) as bf16 into row `row`, columns 16 c16 .. +15, of a
+// two-box 128B-swizzled tile (the layout the output TMA map expects).
+__device__ __forceinline__ void stage16_bf16(unsigned char *tile2, int row, int c16, const uint32_t (&v)[16],
+                                             const float *add, float add_scale) {
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]) + add_scale * add[j];
+    unsigned char *tile = tile2 + (c16 / 4) * kBox;
+    const int col8 = (c16 % 4) * 2;
+#pragma unroll
+    for (int g2 = 0; g2 < 2; ++g2) {
+        uint4 w;
+        w.x = pack_bf16(f[8 * g2 + 0], f[8 * g2 + 1]);
+        w.y = pack_bf16(f[8 * g2 + 2], f[8 * g2 + 3]);
+        w.z = pack_bf16(f[8 * g2 + 4], f[8 * g2 + 5]);
+        w.w = pack_bf16(f[8 * g2 + 6], f[8 * g2 + 7]);
+        *(uint4 *)(tile + sw128_off(row, col8 + g2)) = w;
+    }
+}
+
 // Stores 16 fp32 values (x[c] * scale + add[c]) as bf16 at dst (16-byte aligned).
 __device__ __forceinline__ void store16_bf16(__nv_bfloat16 *dst, const uint32_t (&v)[16], const float *add,
                                              float add_scale, float scale) {
@@ -142,7 +162,7 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 128);
+            mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dQ tile has left the Q tile
         }
         const uint32_t counts[12] = {1, 128, 128, 1, 128, 1, 128, 1, 1, 1, 128, 128};
         for (int k = 0; k < 12; ++k) mbar_init(&bar[k], counts[k]);
@@ -288,15 +308,12 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            const long long h0 = pc.h * P.sl.nchunk;
-            const int b_first = cta_of(P.sl, h0);
-            const int b_to = CAUSAL ? (int)blockIdx.x : cta_of(P.sl, h0 + P.sl.nchunk - 1) + 1;
+            // carried forward state of the piece, combined into its own slot by tc_scan_slots
             if (CAUSAL && it > 0) {
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x30A)) break;
                 tc_fence_after();
             }
-            load_carry(P.slots, P.slot_stride, pc.h, CAUSAL && pc.a == 0 ? b_to : b_first, b_to, i, R2 + lo, Sb, zc,
-                       ac, CAUSAL);
+            load_carry1(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, R2 + lo, Sb, zc, ac, CAUSAL);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync();
@@ -409,19 +426,30 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
                     ye.x += cs.x;
                     ye.y += cs.y;
                 }
-                mbar_arrive(&empty[s]);
-                // dQ_i = X_i - dt_i z
+                // dQ_i = X_i - dt_i z, staged in the Q tile (every MMA and column sum that reads Q is done
+                // once X is complete and all threads are past this barrier) and stored by TMA
                 ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);
                 if (!ok) break;
                 tc_fence_after();
+                epi_sync();
 #pragma unroll 1
                 for (int c16 = 0; c16 < D / 16; ++c16) {
                     uint32_t v[16];
                     tmem_ld16(R1 + lo + c16 * 16, v);
-                    tmem_ld_wait();
-                    if (row_ok) store16_bf16(dQg + ((size_t)pc.h * P.N + row0 + i) * D + c16 * 16, v, zc + c16 * 16, -dt, 1.f);
+                    tmem_wait_ld(v);
+                    stage16_bf16(qt, i, c16, v, zc + c16 * 16, -dt);
                 }
+                (void)row_ok;
+                (void)dQg;
+                fence_proxy_async_smem();
                 tc_fence_before();
+                epi_sync();
+                if (threadIdx.x == 64) {
+                    for (int nb = 0; nb < NB; ++nb) tma_store_3d(&P.tmdQ, qt + nb * kBox, nb * 64, (int)row0, (int)pc.h);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&empty[s]);
+                }
                 if (!CAUSAL) mbar_arrive(barXf);
                 if (CAUSAL) {
                     ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x30F);
@@ -462,6 +490,7 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
             mbar_arrive(barPPf);
         }
     }
+    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -510,7 +539,7 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 128);
+            mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dK, dV tiles have left shared memory
         }
         const uint32_t counts[9] = {1, 128, 128, 1, 128, 1, 128, 1, 128};
         for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
@@ -648,16 +677,13 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            const long long h0 = pc.h * P.sl.nchunk;
-            const int b_last = cta_of(P.sl, h0 + P.sl.nchunk - 1);
-            // carried sums: causal = later pieces of the head, non-causal = all of them
-            const int b_from = CAUSAL ? (int)blockIdx.x + 1 : cta_of(P.sl, h0);
-            const int b_to = CAUSAL && pc.e == P.sl.nchunk ? b_from : b_last + 1;
+            // carried reverse sums (causal: the later pieces of the head; non-causal: the whole head),
+            // combined into this piece's own slot by tc_scan_slots
             if (CAUSAL && it > 0) {
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x409)) break;
                 tc_fence_after();
             }
-            load_carry(P.slots_rev, P.slot_stride, pc.h, b_from, b_to, j, R3 + lo, Pb, yc, ec, CAUSAL);
+            load_carry1(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, R3 + lo, Pb, yc, ec, CAUSAL);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync();
@@ -688,30 +714,52 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
                 ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
                 if (!ok) break;
                 tc_fence_after();
+                // dK staged in the V tile (its last reader, dK += V Pb^T, is complete) and stored by TMA
 #pragma unroll 1
                 for (int c16 = 0; c16 < D / 16; ++c16) {
                     uint32_t v[16];
                     tmem_ld16(R2 + lo + c16 * 16, v);
-                    tmem_ld_wait();
-                    if (row_ok) store16_bf16(dKg + grow * D + c16 * 16, v, yc + c16 * 16, -1.f, 1.f);
+                    tmem_wait_ld(v);
+                    stage16_bf16(st + OFF_V, j, c16, v, yc + c16 * 16, -1.f);
                 }
+                fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(barKf);
+                epi_sync();
+                if (threadIdx.x == 64) {
+                    for (int nb = 0; nb < NB; ++nb)
+                        tma_store_3d(&P.tmdK, st + OFF_V + nb * kBox, nb * 64, (int)row0, (int)pc.h);
+                    bulk_commit();
+                }
                 // dV_j = [dV accumulator]_j + e
                 ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x40C);
                 if (!ok) break;
                 tc_fence_after();
+                // dV staged in the K tile (its last reader, dV += K Pb, is complete) and stored by TMA
 #pragma unroll 1
                 for (int c16 = 0; c16 < D / 16; ++c16) {
                     uint32_t v[16];
                     tmem_ld16(R2 + lo + c16 * 16, v);
-                    tmem_ld_wait();
-                    if (row_ok) store16_bf16(dVg + grow * D + c16 * 16, v, ec + c16 * 16, 1.f, 1.f);
+                    tmem_wait_ld(v);
+                    stage16_bf16(st + OFF_K, j, c16, v, ec + c16 * 16, 1.f);
                 }
+                (void)row_ok;
+                (void)dKg;
+                (void)dVg;
+                fence_proxy_async_smem();
                 tc_fence_before();
+                epi_sync();
+                if (threadIdx.x == 64) {
+                    for (int nb = 0; nb < NB; ++nb)
+                        tma_store_3d(&P.tmdV, st + OFF_K + nb * kBox, nb * 64, (int)row0, (int)pc.h);
+                    bulk_commit();
+                }
                 if (!CAUSAL) {
                     mbar_arrive(barVf);
-                    mbar_arrive(&empty[s]);
+                    if (threadIdx.x == 64) {
+                        bulk_wait_read0();
+                        mbar_arrive(&empty[s]);
+                    }
                     continue;
                 }
                 // dO row -> dOt row in place; then y and e gain this chunk's rows
@@ -737,7 +785,11 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
                 const float2 cs = weighted_colsum(t < 64 ? qt : ot, col, t < 64 ? sDt : nullptr);
                 float *base = t < 64 ? yc : ec;
                 const float2 yn = make_float2(base[col] + cs.x, base[col + 1] + cs.y);
-                mbar_arrive(&empty[s]);
+                epi_sync();  // every read of the stage by this warp group is done
+                if (threadIdx.x == 64) {
+                    bulk_wait_read0();  // dK and dV have left the V and K tiles
+                    mbar_arrive(&empty[s]);
+                }
                 ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x40D);
                 if (!ok) break;
                 tc_fence_after();
@@ -754,6 +806,7 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
             }
         }
     }
+    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -799,7 +852,8 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     memset(&P, 0, sizeof(P));
     if (!tc_host::fill_common(P, p, ws)) return cudaErrorInvalidDevice;
     if (!tc_host::make_map(&P.tmQ, Q, p) || !tc_host::make_map(&P.tmK, K, p) || !tc_host::make_map(&P.tmV, V, p) ||
-        !tc_host::make_map(&P.tmdO, dO, p))
+        !tc_host::make_map(&P.tmdO, dO, p) || !tc_host::make_map(&P.tmdQ, dQ, p) ||
+        !tc_host::make_map(&P.tmdK, dK, p) || !tc_host::make_map(&P.tmdV, dV, p))
         return cudaErrorInvalidValue;
     P.slots_rev = (float *)(ws + p.off_states2);
     P.rs_g = (float *)(ws + p.off_rowstats);
@@ -808,16 +862,20 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dK = dK;
     P.dV = dV;
     cudaError_t e = tc_host::launch_agg(P, s);
+    if (e == cudaSuccess) e = tc_host::launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
     if (e != cudaSuccess) return e;
-    if (p.causal) {
+    if (p.causal)
         tc::tc_bwd_dq_kernel<true><<<P.sl.G, 192, kSmemDq, s>>>(P);
-        tc::tc_bwd_dkdv_kernel<true><<<P.sl.G, 192, kSmemDkdv, s>>>(P);
-    } else {
+    else
         tc::tc_bwd_dq_kernel<false><<<P.sl.G, 192, kSmemDqNc, s>>>(P);
+    e = tc_host::launch_scan(P.slots_rev, P, p.BH, p.causal ? 1 : 2, s);
+    if (e != cudaSuccess) return e;
+    if (p.causal)
+        tc::tc_bwd_dkdv_kernel<true><<<P.sl.G, 192, kSmemDkdv, s>>>(P);
+    else
         tc::tc_bwd_dkdv_kernel<false><<<P.sl.G, 192, kSmemDkdvNc, s>>>(P);
-    }
     e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(3);
+    if (e == cudaSuccess) count_launches(5);
     return e;
 }
 

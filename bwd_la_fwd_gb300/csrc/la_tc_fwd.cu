@@ -169,13 +169,18 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
 
 
 // ----------------------------------------------------------------------------------------------------
-// Forward output.  Per chunk (causal): T = Q K^T -> P = [j <= i](1 + T) (bf16, back into TMEM) ->
-// O = P V + Q Sb (Sb = bf16 state before the chunk) -> S += K^T V, from which the epilogue writes the
-// next Sb.  z and a (running column sums of K and V) are kept in fp32 by the epilogue warps, which also
-// form q_i . z and the normaliser.  Non-causal: O = Q Sb with the head's total state, no T / P.
+// Forward output.  Per chunk (causal): T = Q K^T -> P = [j <= i](1 + T) (bf16, in place in TMEM) ->
+// O = P V + Q Sb (Sb = bf16 state before the chunk) -> S += K^T V, z += K^T 1, a += V^T 1 (TMEM), from
+// which the epilogue writes the next Sb and the fp32 z, a it broadcasts.  The epilogue forms q_i . z and
+// the normaliser.  Non-causal: O = Q Sb with the head's totals (no T, P or state update) into two
+// alternating TMEM accumulators, so the MMA of one chunk overlaps the epilogue of the previous one.
+// Eight epilogue warps: two per TMEM lane quarter, each owning half of the columns; the row sums they
+// share (r_i and q_i . z) are exchanged through two TMEM columns.
+// TMEM: causal  T 0-127, O 128-255, S 256-383, z 384, a 400, exchange 416-419;
+//       non-causal  O 0-127 / 128-255, exchange 256-259.
 // ----------------------------------------------------------------------------------------------------
 template <bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr int NST = CAUSAL ? 2 : 4;
     constexpr uint32_t QB = NB * kBox;                  // Q (or K, V) tile of one chunk
@@ -184,14 +189,16 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
     bool aligned;
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
     unsigned char *stages = sm;
-    unsigned char *Sb = sm + NST * STAGE;               // bf16 state, MN-major [d][e], two 64-column boxes
-    float *zc = (float *)(Sb + QB);                     // running z (fp32, D)
+    unsigned char *Sb = sm + NST * STAGE;               // bf16 state, [d][e], two 64-column boxes
+    unsigned char *ones = Sb + QB;                      // 8 rows x 128 B of bf16 1.0 (the N = 16 operand)
+    float *zc = (float *)(ones + 1024);                 // running z (fp32, D)
     float *ac = zc + D;                                 // running a (fp32, D)
     uint64_t *full = (uint64_t *)(ac + D);
     uint64_t *empty = full + NST;
-    uint64_t *barT = empty + NST, *barP = barT + 1, *barSb = barP + 1, *barO = barSb + 1, *barS = barO + 1;
-    uint64_t *barOf = barS + 1;  // non-causal: the epilogue has drained the O accumulator
-    uint32_t *tslot = (uint32_t *)(barOf + 1);
+    uint64_t *barT = empty + NST, *barP = barT + 1, *barSb = barP + 1, *barS = barSb + 1;
+    uint64_t *barO = barS + 1;    // [2]
+    uint64_t *barOf = barO + 2;   // [2] non-causal: accumulator drained
+    uint32_t *tslot = (uint32_t *)(barOf + 2);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
@@ -199,17 +206,21 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + 128);  // MMA commit + every epilogue thread (they read Q, K, V too)
+            mbar_init(&empty[s], 2);  // MMA commit + the epilogue, once its O tile has left the Q tile
         }
         mbar_init(barT, 1);
-        mbar_init(barP, 128);
-        mbar_init(barSb, 128);
-        mbar_init(barO, 1);
+        mbar_init(barP, kEpiThreads);
+        mbar_init(barSb, kEpiThreads);
         mbar_init(barS, 1);
-        mbar_init(barOf, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&barO[b], 1);
+            mbar_init(&barOf[b], kEpiThreads);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
+    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -218,7 +229,8 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tT = tmem, tO = tmem + 128, tS = tmem + 256;
+    const uint32_t tT = tmem, tS = tmem + 256, tZ = tmem + 384, tA = tmem + 400;
+    const uint32_t tX = tmem + (CAUSAL ? 416 : 256);
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer
@@ -256,19 +268,24 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
         const uint32_t idMM = idesc_bf16(128, 128, true, true);
-        const uint32_t sb = smem_u32(Sb);
+        const uint32_t idZ = idesc_bf16(128, 16, true, false);
+        const uint32_t sb = smem_u32(Sb), on = smem_u32(ones);
         int it = 0, pno = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
             if (!CAUSAL && !wait_or_abort(barSb, pno & 1, abort_flag, P.status, 0x202)) break;
-            for (int c = pc.a; c < pc.e; ++c, ++it) {
+            for (int c = pc.a; c < pc.e && ok; ++c, ++it) {
                 const int s = it % NST;
                 const uint32_t ph = it & 1;
-                if (!wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x203)) {
-                    ok = false;
-                    break;
+                const int ob = CAUSAL ? 0 : (it & 1);  // accumulator buffer
+                const uint32_t tO = tmem + (CAUSAL ? 128 : 128 * ob);
+                if (!CAUSAL && it >= 2) {
+                    ok = wait_or_abort(&barOf[ob], ((it >> 1) - 1) & 1, abort_flag, P.status, 0x20A);
+                    if (!ok) break;
                 }
+                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x203);
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t qb = smem_u32(stages + s * STAGE), kb = qb + QB, vb = qb + 2 * QB;
                 if (CAUSAL) {
@@ -277,39 +294,32 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
                         mma_ss(tT, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                                sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
                     mma_commit(barT);
-                    if (!wait_or_abort(barP, ph, abort_flag, P.status, 0x204)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x204);
+                    if (!ok) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k = 0; k < kC / 16; ++k)  // O = P V, K steps over j (P in TMEM, 8 columns each)
                         mma_ts(tO, tT + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, k > 0);
-                    if (!wait_or_abort(barSb, ph, abort_flag, P.status, 0x205)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                } else if (it > 0) {
-                    // O is overwritten below: wait until the epilogue has read the previous chunk's O
-                    // (otherwise barO could complete twice before its waiter sees the first phase)
-                    if (!wait_or_abort(barOf, (it - 1) & 1, abort_flag, P.status, 0x20A)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x205);
+                    if (!ok) break;
                     tc_fence_after();
                 }
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)  // O += Q Sb, K steps over d
                     mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                            sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
-                mma_commit(barO);
+                mma_commit(&barO[ob]);
                 if (CAUSAL) {
                     if (c + 1 < pc.e) {
 #pragma unroll
-                        for (int k = 0; k < kC / 16; ++k)  // S += K^T V, K steps over j
-                            mma_ss(tS, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
-                                   idMM, 1u);
+                        for (int k = 0; k < kC / 16; ++k) {  // S += K^T V, z += K^T 1, a += V^T 1
+                            const uint64_t kt = sdesc_sw128(kb + 2048 * k, kBox, 1024);
+                            const uint64_t vt = sdesc_sw128(vb + 2048 * k, kBox, 1024);
+                            const uint64_t o1 = sdesc_sw128(on + 32 * (k & 3), 16, 0);
+                            mma_ss(tS, kt, vt, idMM, 1u);
+                            mma_ss(tZ, kt, o1, idZ, 1u);
+                            mma_ss(tA, vt, o1, idZ, 1u);
+                        }
                     }
                     mma_commit(barS);
                 }
@@ -317,177 +327,139 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
             }
         }
     } else if (warp >= 2) {
-        // ---- epilogue warps: thread <-> chunk row i (TMEM lane) and state row d (same index)
-        const int lb = 32 * (warp & 3);
-        const int i = lb + lane;
-        const uint32_t lane_off = (uint32_t)lb << 16;
+        // ---- epilogue: thread <-> chunk row i (TMEM lane) and column half hf
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int i = 32 * q4 + lane;
+        const uint32_t lo = (uint32_t)(32 * q4) << 16;
         __nv_bfloat16 *Og = (__nv_bfloat16 *)P.O;
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            const long long h0 = pc.h * P.sl.nchunk;  // flat chunk index of the head's first chunk
-            // carried state: causal = earlier pieces of the head, non-causal = all pieces of the head
-            const int b_first = cta_of(P.sl, h0);
-            const int b_to = CAUSAL ? (int)blockIdx.x : cta_of(P.sl, h0 + P.sl.nchunk - 1) + 1;
-            if (CAUSAL && it > 0) {  // the previous piece's last S update must be done before TMEM S is reset
+            // carried state (causal: the earlier pieces of the head; non-causal: the whole head), already
+            // combined into this piece's own slot by tc_scan_slots
+            if (CAUSAL && it > 0) {  // the previous piece's last MMAs must be done before TMEM S is reset
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x206)) break;
                 tc_fence_after();
             }
-            load_carry(P.slots, P.slot_stride, pc.h, CAUSAL && pc.a == 0 ? b_to : b_first, b_to, i, tS + lane_off, Sb, zc, ac, CAUSAL);
+            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, tS + lo, tZ + lo, tA + lo,
+                            Sb, zc, ac, CAUSAL);
             fence_proxy_async_smem();
             tc_fence_before();
-            epi_sync();
+            epi_sync256();
             mbar_arrive(barSb);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 const int s = it % NST;
                 const uint32_t ph = it & 1;
+                const int ob = CAUSAL ? 0 : (it & 1);
+                const uint32_t tO = tmem + (CAUSAL ? 128 : 128 * ob);
+                const uint32_t ph_o = CAUSAL ? ph : ((it >> 1) & 1);
                 unsigned char *st = stages + s * STAGE;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
-                float r = 0.f;
+                float part = 0.f;
                 if (CAUSAL) {
-                    // P = [j <= i](1 + T), bf16, written over T's first 64 columns; r_i = sum_j P_ij (fp32)
-                    if (!wait_or_abort(barT, ph, abort_flag, P.status, 0x207)) {
-                        ok = false;
-                        break;
-                    }
+                    // P = [j <= i](1 + T) for this half's columns j; r_i partial sum in fp32
+                    ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x207);
+                    if (!ok) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int q = 0; q < kC / 32; ++q) {
-                        uint32_t t0[16], t1[16], pk[16];
-                        tmem_ld16(tT + lane_off + 32 * q, t0);
-                        tmem_ld16(tT + lane_off + 32 * q + 16, t1);
-                        tmem_ld_wait();
+                    uint32_t t0[32], t1[32], pk[32];
+                    tmem_ld32(tT + lo + 64 * hf, t0);
+                    tmem_ld32(tT + lo + 64 * hf + 32, t1);
+                    tmem_wait_ld(t0);
+                    tmem_wait_ld(t1);
 #pragma unroll
-                        for (int j2 = 0; j2 < 16; ++j2) {
-                            const int j = 32 * q + 2 * j2;
-                            const uint32_t lo = j2 < 8 ? t0[2 * j2] : t1[2 * j2 - 16];
-                            const uint32_t hi = j2 < 8 ? t0[2 * j2 + 1] : t1[2 * j2 - 15];
-                            const float p0 = j <= i ? 1.f + __uint_as_float(lo) : 0.f;
-                            const float p1 = j + 1 <= i ? 1.f + __uint_as_float(hi) : 0.f;
-                            pk[j2] = pack_bf16(p0, p1);
-                            r += p0 + p1;  // the normaliser sums the fp32 weights; only the MMA operand is bf16
-                        }
-                        tmem_st16(tT + lane_off + 16 * q, pk);
+                    for (int m = 0; m < 32; ++m) {
+                        const int j = 64 * hf + 2 * m;
+                        const uint32_t a0 = m < 16 ? t0[2 * m] : t1[2 * m - 32];
+                        const uint32_t a1 = m < 16 ? t0[2 * m + 1] : t1[2 * m - 31];
+                        const float p0 = j <= i ? 1.f + __uint_as_float(a0) : 0.f;
+                        const float p1 = j + 1 <= i ? 1.f + __uint_as_float(a1) : 0.f;
+                        pk[m] = pack_bf16(p0, p1);
+                        part += p0 + p1;
                     }
+                    tc_fence_before();
+                    epi_sync256();  // both halves have read T before P overwrites it
+                    tc_fence_after();
+                    tmem_st32(tT + lo + 32 * hf, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barP);
                 }
-                // q_i . z (z before this chunk), from the Q tile in shared memory
-                float qz = 0.f;
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        const uint4 v = *(const uint4 *)(st + nb * kBox + sw128_off(i, g8));
-                        const float *zz = zc + nb * 64 + g8 * 8;
-                        qz += bf16lo(v.x) * zz[0] + bf16hi(v.x) * zz[1] + bf16lo(v.y) * zz[2] + bf16hi(v.y) * zz[3] +
-                              bf16lo(v.z) * zz[4] + bf16hi(v.z) * zz[5] + bf16lo(v.w) * zz[6] + bf16hi(v.w) * zz[7];
-                    }
-                }
-                float anew0 = 0.f, anew1 = 0.f;
-                const int t = threadIdx.x - 64;  // 0..127
+                part += dot_half(st, i, hf, zc);  // q_i . z over this half's d
+                // exchange columns alternate by chunk parity: the barrier below then orders every read of
+                // one chunk's pair before the other half's write of the same pair two chunks later
+                const uint32_t tXc = tX + lo + 2 * (it & 1);
+                tmem_st1(tXc + hf, __float_as_uint(part));
+                float vn = 0.f;          // z (half 0) or a (half 1) after this chunk, for row d = i
                 if (CAUSAL) {
-                    epi_sync();  // every thread has read z before it is advanced
-                    // column sums of this chunk's K (threads 0-63) or V (64-127), two columns each
-                    const int col = 2 * (t & 63);
-                    const unsigned char *tile = st + (t < 64 ? QB : 2 * QB) + (col / 64) * kBox;
-                    const int cc = col % 64;
-                    float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-                    for (int j = 0; j < kC; ++j) {
-                        const uint32_t v = *(const uint32_t *)(tile + sw128_off(j, cc / 8) + (cc % 8) * 2);
-                        s0 += bf16lo(v);
-                        s1 += bf16hi(v);
-                    }
-                    if (t < 64) {
-                        zc[col] += s0;
-                        zc[col + 1] += s1;
-                    } else {
-                        anew0 = ac[col] + s0;
-                        anew1 = ac[col + 1] + s1;
-                    }
-                }
-                mbar_arrive(&empty[s]);  // this thread is done reading the stage
-                if (CAUSAL) {
-                    // next chunk's Sb from the updated state (not after the piece's last chunk)
-                    if (!wait_or_abort(barS, ph, abort_flag, P.status, 0x208)) {
-                        ok = false;
-                        break;
-                    }
+                    ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x208);
+                    if (!ok) break;
                     tc_fence_after();
                     if (c + 1 < pc.e) {
-#pragma unroll 1
-                        for (int c16 = 0; c16 < D / 16; ++c16) {
-                            uint32_t v[16];
-                            tmem_ld16(tS + lane_off + c16 * 16, v);
-                            tmem_ld_wait();
-                            unsigned char *tile = Sb + (c16 / 4) * kBox;
-                            const int col8 = (c16 % 4) * 2;
-#pragma unroll
-                            for (int g2 = 0; g2 < 2; ++g2) {
-                                uint4 w;
-                                w.x = pack_bf16(__uint_as_float(v[8 * g2 + 0]), __uint_as_float(v[8 * g2 + 1]));
-                                w.y = pack_bf16(__uint_as_float(v[8 * g2 + 2]), __uint_as_float(v[8 * g2 + 3]));
-                                w.z = pack_bf16(__uint_as_float(v[8 * g2 + 4]), __uint_as_float(v[8 * g2 + 5]));
-                                w.w = pack_bf16(__uint_as_float(v[8 * g2 + 6]), __uint_as_float(v[8 * g2 + 7]));
-                                *(uint4 *)(tile + sw128_off(i, col8 + g2)) = w;
-                            }
-                        }
+                        tmem_half_to_tile(tS + lo, Sb, i, hf);
+                        uint32_t za, zb;
+                        tmem_ld2((hf == 0 ? tZ : tA) + lo, za, zb);
+                        tmem_wait_ld(za, zb);
+                        vn = __uint_as_float(za);
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(barSb);
                     }
                 }
-                // output rows: O_i = (a + [P V + Q Sb]_i) / g_i
-                if (!wait_or_abort(barO, ph, abort_flag, P.status, 0x209)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float n_prev = CAUSAL ? (float)row0 : (float)P.N;
-                const float gi = n_prev + qz + r;
-                const float inv = 1.f / gi;
-                const bool row_ok = i < nvalid;
-                __nv_bfloat16 *orow = Og + ((size_t)pc.h * P.N + row0 + i) * D;
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    uint32_t v[16];
-                    tmem_ld16(tO + lane_off + c16 * 16, v);
-                    tmem_ld_wait();
-                    uint4 w0, w1;
-                    const float *aa = ac + c16 * 16;
-                    w0.x = pack_bf16((__uint_as_float(v[0]) + aa[0]) * inv, (__uint_as_float(v[1]) + aa[1]) * inv);
-                    w0.y = pack_bf16((__uint_as_float(v[2]) + aa[2]) * inv, (__uint_as_float(v[3]) + aa[3]) * inv);
-                    w0.z = pack_bf16((__uint_as_float(v[4]) + aa[4]) * inv, (__uint_as_float(v[5]) + aa[5]) * inv);
-                    w0.w = pack_bf16((__uint_as_float(v[6]) + aa[6]) * inv, (__uint_as_float(v[7]) + aa[7]) * inv);
-                    w1.x = pack_bf16((__uint_as_float(v[8]) + aa[8]) * inv, (__uint_as_float(v[9]) + aa[9]) * inv);
-                    w1.y = pack_bf16((__uint_as_float(v[10]) + aa[10]) * inv, (__uint_as_float(v[11]) + aa[11]) * inv);
-                    w1.z = pack_bf16((__uint_as_float(v[12]) + aa[12]) * inv, (__uint_as_float(v[13]) + aa[13]) * inv);
-                    w1.w = pack_bf16((__uint_as_float(v[14]) + aa[14]) * inv, (__uint_as_float(v[15]) + aa[15]) * inv);
-                    if (row_ok) {
-                        uint4 *dst = (uint4 *)(orow + c16 * 16);
-                        dst[0] = w0;
-                        dst[1] = w1;
-                    }
-                }
-                if (row_ok && P.g) P.g[(size_t)pc.h * P.N + row0 + i] = gi;
+                // g_i from both halves' partial sums
+                tmem_st_wait();
                 tc_fence_before();
-                if (!CAUSAL) mbar_arrive(barOf);
+                epi_sync256();
+                tc_fence_after();
+                uint32_t x0, x1;
+                tmem_ld2(tXc, x0, x1);
+                tmem_wait_ld(x0, x1);
+                const float gi = (CAUSAL ? (float)row0 : (float)P.N) + __uint_as_float(x0) + __uint_as_float(x1);
+                const float inv = 1.f / gi;
+                // output: O_i = (a + [P V + Q Sb]_i) / g_i, this half's 64 columns
+                ok = wait_or_abort(&barO[ob], ph_o, abort_flag, P.status, 0x209);
+                if (!ok) break;
+                tc_fence_after();
+                const bool row_ok = i < nvalid;
+                // the O tile is staged in this stage's Q tile (Q is dead once O is complete; each thread
+                // overwrites only the row and box it read for q . z) and leaves by TMA
+                unsigned char *otile = st + hf * kBox;
+#pragma unroll 1
+                for (int half32 = 0; half32 < 2; ++half32) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + lo + 64 * hf + 32 * half32, v);
+                    tmem_wait_ld(v);
+                    const float *aa = ac + 64 * hf + 32 * half32;
+                    uint4 w[4];
+                    uint32_t *wv = (uint32_t *)w;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        wv[m] = pack_bf16((__uint_as_float(v[2 * m]) + aa[2 * m]) * inv,
+                                          (__uint_as_float(v[2 * m + 1]) + aa[2 * m + 1]) * inv);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) *(uint4 *)(otile + sw128_off(i, 4 * half32 + q)) = w[q];
+                }
+                if (row_ok && hf == 0 && P.g) P.g[(size_t)pc.h * P.N + row0 + i] = gi;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                epi_sync256();  // the whole O tile is in shared memory
+                if (threadIdx.x == 64) {
+                    for (int nb = 0; nb < NB; ++nb) tma_store_3d(&P.tmO, st + nb * kBox, nb * 64, (int)row0, (int)pc.h);
+                    bulk_commit();
+                    bulk_wait_read0();       // the tile has been read out of shared memory
+                    mbar_arrive(&empty[s]);  // the stage may be refilled
+                }
+                if (!CAUSAL) mbar_arrive(&barOf[ob]);
                 if (CAUSAL) {
-                    epi_sync();  // everyone has read a before it is advanced
-                    if (t >= 64) {
-                        const int col = 2 * (t & 63);
-                        ac[col] = anew0;
-                        ac[col + 1] = anew1;
-                    }
-                    epi_sync();
+                    epi_sync256();  // everyone has read z and a of this chunk
+                    if (c + 1 < pc.e) (hf == 0 ? zc : ac)[i] = vn;
+                    epi_sync256();
                 }
             }
         }
     }
+    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -497,6 +469,48 @@ __global__ void __launch_bounds__(192, 1) tc_fwd_kernel(const __grid_constant__ 
 
 template __global__ void tc_fwd_kernel<true>(const __grid_constant__ TcParams P);
 template __global__ void tc_fwd_kernel<false>(const __grid_constant__ TcParams P);
+
+// ----------------------------------------------------------------------------------------------------
+// In-place scan of the per-piece state sums of each head, so that every piece then reads exactly one
+// slot (its own): mode 0 = exclusive prefix over the head's pieces (causal forward direction),
+// 1 = exclusive suffix (causal reverse direction), 2 = the head's total in every slot (non-causal).
+// grid = (ceil(used4 / 256), BH); thread x owns float4 x of the state.  A head's slots are read in groups
+// of eight with every load of a group issued before any store.
+// ----------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_scan_slots(float *slots, long long stride, Slices sl, int mode,
+                                                      int used4) {
+    const int x = blockIdx.x * 256 + threadIdx.x;
+    if (x >= used4) return;
+    const long long h = blockIdx.y;
+    const long long h0 = h * sl.nchunk;
+    const int b0 = cta_of(sl, h0), b1 = cta_of(sl, h0 + sl.nchunk - 1);
+    const int n = b1 - b0 + 1;
+    float4 *base = (float4 *)slots + x;
+    const long long s4 = stride / 4;
+    auto at = [&](int k) -> float4 * {  // k-th slot of the head in scan order
+        const int b = mode == 1 ? b1 - k : b0 + k;
+        return base + slot_of(h, b) * s4;
+    };
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g0 = 0; g0 < n; g0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (g0 + k < n) v[k] = *at(g0 + k);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (g0 + k < n) {
+                if (mode != 2) *at(g0 + k) = run;
+                run.x += v[k].x;
+                run.y += v[k].y;
+                run.z += v[k].z;
+                run.w += v[k].w;
+            }
+        }
+    }
+    if (mode == 2)
+        for (int k = 0; k < n; ++k) *at(k) = run;
+}
 
 }  // namespace tc
 
@@ -543,8 +557,8 @@ bool make_map(CUtensorMap *m, const void *ptr, const Plan &p) {
 }
 
 constexpr size_t kSmemAgg = 3 * 2 * 2 * (size_t)tc::kBox + 2048 + 256;
-constexpr size_t kSmemFwdCausal = 2 * 3 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
-constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
+constexpr size_t kSmemFwdCausal = 2 * 3 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 1024 + 256;
+constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 1024 + 256;
 static_assert(kSmemFwdCausal <= 232448, "forward kernel exceeds the shared-memory limit");
 
 bool set_smem_attrs() {
@@ -580,6 +594,12 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     return true;
 }
 
+cudaError_t launch_scan(float *slots, const tc::TcParams &P, int BH, int mode, cudaStream_t s) {
+    const int used4 = (128 * 128 + 2 * 128) / 4;
+    tc::tc_scan_slots<<<dim3((used4 + 255) / 256, BH), 256, 0, s>>>(slots, P.slot_stride, P.sl, mode, used4);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
     if (!set_smem_attrs()) return cudaErrorInvalidValue;
     tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
@@ -600,16 +620,19 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
     if (!fill_common(P, p, ws)) return cudaErrorInvalidDevice;
-    if (!make_map(&P.tmQ, Q, p) || !make_map(&P.tmK, K, p) || !make_map(&P.tmV, V, p)) return cudaErrorInvalidValue;
+    if (!make_map(&P.tmQ, Q, p) || !make_map(&P.tmK, K, p) || !make_map(&P.tmV, V, p) || !make_map(&P.tmO, O, p))
+        return cudaErrorInvalidValue;
     P.O = O;
     P.g = g;
     tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
+    cudaError_t e0 = launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
+    if (e0 != cudaSuccess) return e0;
     if (p.causal)
-        tc::tc_fwd_kernel<true><<<P.sl.G, 192, kSmemFwdCausal, s>>>(P);
+        tc::tc_fwd_kernel<true><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s>>>(P);
     else
-        tc::tc_fwd_kernel<false><<<P.sl.G, 192, kSmemFwdNonCausal, s>>>(P);
+        tc::tc_fwd_kernel<false><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s>>>(P);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(2);
+    if (e == cudaSuccess) count_launches(3);
     return e;
 }
 

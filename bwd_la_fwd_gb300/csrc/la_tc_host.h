@@ -14,6 +14,7 @@ namespace tc {
 // Kernel parameters (passed as a __grid_constant__ struct; the tensor maps stay in parameter space).
 struct TcParams {
     CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D maps over [BH][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmO, tmdQ, tmdK, tmdV;  // the outputs, same form (tiles are staged in shared memory)
     Slices sl;
     long long N;
     float *slots;           // per-piece state sums, slot stride `slot_stride` floats
@@ -33,6 +34,8 @@ namespace tc_host {
 bool make_map(CUtensorMap *m, const void *ptr, const Plan &p);
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
+// mode 0: exclusive prefix per head, 1: exclusive suffix, 2: head total in every slot
+cudaError_t launch_scan(float *slots, const tc::TcParams &P, int BH, int mode, cudaStream_t s);
 }  // namespace tc_host
 
 // bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.

@@ -20,56 +20,128 @@ __device__ __forceinline__ unsigned char *smem_base(unsigned char *raw, uint32_t
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Loads the state carried into a piece (sum of slots b_from..b_to-1 of head h) for TMEM lane / row d:
-// row d of the D x D sum into TMEM (if to_tmem) and, rounded to bf16, into row d of the operand tile Sb
-// (two 64-column boxes, 128-byte swizzle); the two vector sums into zc[d] and ac[d].
-__device__ __forceinline__ void load_carry(const float *slots, long long slot_stride, long long h, int b_from, int b_to, int d,
-                                           uint32_t tS, unsigned char *Sb, float *zc, float *ac, bool to_tmem) {
+constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane quarter
+__device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// The whole carried state `slot` ([S row-major | z | a], fp32) for row d (four-warp epilogues): row d of S
+// into TMEM (if to_tmem) and, as bf16, into row d of the operand tile Sb; z[d] to zc, a[d] to ac.
+// The loads of each 64-column half are issued together.
+__device__ __forceinline__ void load_carry1(const float *slot, int d, uint32_t tS, unsigned char *Sb, float *zc,
+                                            float *ac, bool to_tmem) {
     constexpr int D = 128;
+    const float zv = slot[(size_t)D * D + d], av = slot[(size_t)D * D + D + d];
 #pragma unroll 1
-    for (int c16 = 0; c16 < D / 16; ++c16) {
-        float acc[16];
+    for (int hf = 0; hf < 2; ++hf) {
+        const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
+        float4 v4[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-        for (int b = b_from; b < b_to; ++b) {
-            const float4 *src = (const float4 *)(slots + slot_of(h, b) * slot_stride + (size_t)d * D + c16 * 16);
+        for (int q = 0; q < 16; ++q) v4[q] = src[q];
+        const float *acc = (const float *)v4;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = src[q];
-                acc[4 * q] += v.x;
-                acc[4 * q + 1] += v.y;
-                acc[4 * q + 2] += v.z;
-                acc[4 * q + 3] += v.w;
+        for (int half32 = 0; half32 < 2; ++half32) {
+            const float *a32 = acc + 32 * half32;
+            if (to_tmem) {
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a32[j]);
+                tmem_st32(tS + 64 * hf + 32 * half32, r);
+            }
+            unsigned char *tile = Sb + hf * kBox;
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) {
+                uint4 w;
+                w.x = pack_bf16(a32[8 * g4 + 0], a32[8 * g4 + 1]);
+                w.y = pack_bf16(a32[8 * g4 + 2], a32[8 * g4 + 3]);
+                w.z = pack_bf16(a32[8 * g4 + 4], a32[8 * g4 + 5]);
+                w.w = pack_bf16(a32[8 * g4 + 6], a32[8 * g4 + 7]);
+                *(uint4 *)(tile + sw128_off(d, 4 * half32 + g4)) = w;
             }
         }
-        if (to_tmem) {
-            uint32_t r[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(acc[j]);
-            tmem_st16(tS + c16 * 16, r);
-        }
-        // bf16 copy: row d of an MN-major operand, columns e = c16*16 .. +15 (two 16-byte groups)
-        unsigned char *tile = Sb + (c16 / 4) * kBox;
-        const int col8 = (c16 % 4) * 2;
-#pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-            uint4 v;
-            v.x = pack_bf16(acc[8 * g2 + 0], acc[8 * g2 + 1]);
-            v.y = pack_bf16(acc[8 * g2 + 2], acc[8 * g2 + 3]);
-            v.z = pack_bf16(acc[8 * g2 + 4], acc[8 * g2 + 5]);
-            v.w = pack_bf16(acc[8 * g2 + 6], acc[8 * g2 + 7]);
-            *(uint4 *)(tile + sw128_off(d, col8 + g2)) = v;
-        }
     }
-    float z = 0.f, a = 0.f;
-    for (int b = b_from; b < b_to; ++b) {
-        const float *sl = slots + slot_of(h, b) * slot_stride;
-        z += sl[(size_t)D * D + d];
-        a += sl[(size_t)D * D + D + d];
-    }
-    zc[d] = z;
-    ac[d] = a;
+    zc[d] = zv;
+    ac[d] = av;
     if (to_tmem) tmem_st_wait();
+}
+
+// Half `hf` of the carried state `slot` ([S row-major | z | a], fp32) for row d: columns [64 hf, 64 hf + 64)
+// of S into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes z[d]
+// to zc (and TMEM column tZ), half 1 writes a[d] to ac (and TMEM column tA).  All loads are issued
+// before any is used.
+__device__ __forceinline__ void load_carry_half(const float *slot, int d, int hf, uint32_t tS, uint32_t tZ,
+                                                uint32_t tA, unsigned char *Sb, float *zc, float *ac, bool to_tmem) {
+    constexpr int D = 128;
+    const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
+    float4 v4[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v4[q] = src[q];
+    const float vsum = slot[(size_t)D * D + hf * D + d];
+    const float *acc = (const float *)v4;
+#pragma unroll
+    for (int half32 = 0; half32 < 2; ++half32) {
+        const float *a32 = acc + 32 * half32;
+        if (to_tmem) {
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a32[j]);
+            tmem_st32(tS + 64 * hf + 32 * half32, r);
+        }
+        unsigned char *tile = Sb + hf * kBox;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            uint4 w;
+            w.x = pack_bf16(a32[8 * g4 + 0], a32[8 * g4 + 1]);
+            w.y = pack_bf16(a32[8 * g4 + 2], a32[8 * g4 + 3]);
+            w.z = pack_bf16(a32[8 * g4 + 4], a32[8 * g4 + 5]);
+            w.w = pack_bf16(a32[8 * g4 + 6], a32[8 * g4 + 7]);
+            *(uint4 *)(tile + sw128_off(d, 4 * half32 + g4)) = w;
+        }
+    }
+    (hf == 0 ? zc : ac)[d] = vsum;
+    if (to_tmem) {
+        tmem_st1(hf == 0 ? tZ : tA, __float_as_uint(vsum));
+        tmem_st_wait();
+    }
+}
+
+// Row d's 64 columns [64 hf, 64 hf + 64) of an fp32 TMEM block, rounded into box hf of a bf16 operand tile.
+__device__ __forceinline__ void tmem_half_to_tile(uint32_t taddr, unsigned char *tile2, int d, int hf) {
+#pragma unroll 1
+    for (int half32 = 0; half32 < 2; ++half32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 64 * hf + 32 * half32, v);
+        tmem_wait_ld(v);
+        unsigned char *tile = tile2 + hf * kBox;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[8 * g4 + 0]), __uint_as_float(v[8 * g4 + 1]));
+            w.y = pack_bf16(__uint_as_float(v[8 * g4 + 2]), __uint_as_float(v[8 * g4 + 3]));
+            w.z = pack_bf16(__uint_as_float(v[8 * g4 + 4]), __uint_as_float(v[8 * g4 + 5]));
+            w.w = pack_bf16(__uint_as_float(v[8 * g4 + 6]), __uint_as_float(v[8 * g4 + 7]));
+            *(uint4 *)(tile + sw128_off(d, 4 * half32 + g4)) = w;
+        }
+    }
+}
+
+// q_row . z over the 64 entries of box hf, from a bf16 Q tile (two 64-column boxes) and fp32 z.
+__device__ __forceinline__ float dot_half(const unsigned char *qtile2, int row, int hf, const float *z) {
+    const unsigned char *tile = qtile2 + hf * kBox;
+    const float *zz0 = z + 64 * hf;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        const uint4 v = *(const uint4 *)(tile + sw128_off(row, g8));
+        const float *zz = zz0 + 8 * g8;
+        acc0 = fmaf(bf16lo(v.x), zz[0], acc0);
+        acc1 = fmaf(bf16hi(v.x), zz[1], acc1);
+        acc0 = fmaf(bf16lo(v.y), zz[2], acc0);
+        acc1 = fmaf(bf16hi(v.y), zz[3], acc1);
+        acc0 = fmaf(bf16lo(v.z), zz[4], acc0);
+        acc1 = fmaf(bf16hi(v.z), zz[5], acc1);
+        acc0 = fmaf(bf16lo(v.w), zz[6], acc0);
+        acc1 = fmaf(bf16hi(v.w), zz[7], acc1);
+    }
+    return acc0 + acc1;
 }
 
 }  // namespace tc

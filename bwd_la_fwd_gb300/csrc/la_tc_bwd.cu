@@ -9,9 +9,11 @@
 // where S_c, z_c (earlier rows) are the forward state and P_c = sum q_i dOt_i^T, y_c = sum dt_i q_i,
 // e_c = sum dOt_i run over the later rows.  Non-causal: every sum runs over the whole head.
 //
-// Three launches: the per-piece K^T V sums (shared with the forward), then the dQ walk in chunk order,
-// which recomputes O_i (hence g_i and delta_i; the stored O is not read) and also writes each piece's
-// reverse sums (P, y, e) and the per-row g_i, dt_i, then the dK / dV walk in reverse chunk order.
+// Launches: the per-piece K^T V sums and their scan (shared with the forward), the dQ walk in chunk
+// order (it recomputes O_i, hence g_i and delta_i; the stored O is not read; it also writes each piece's
+// reverse sums P, y, e and the per-row g_i, dt_i), the scan of the reverse sums, and the dK / dV walk in
+// reverse chunk order.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
+// per TMEM lane quarter, each owning 64 of the 128 columns).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
@@ -27,56 +29,34 @@ namespace tc {
 
 using namespace sm100;
 
-// P (or U) in bf16 written over the first 64 columns of a 128-column fp32 TMEM block, in place.
-// f(j, x) maps the fp32 value of column j to the bf16 operand value.
+// Reads this half's 64 columns (lane = the thread's row) of a 128-column fp32 TMEM block and maps them
+// through f(column, value) to 32 packed bf16 pairs.  The caller writes them back (tmem_st32 at column
+// 32 hf) after a barrier, because the two halves' reads and writes overlap.
 template <typename F>
-__device__ __forceinline__ void tmem_to_bf16_inplace(uint32_t taddr, F f) {
-#pragma unroll 1
-    for (int q = 0; q < kC / 32; ++q) {
-        uint32_t t0[16], t1[16], pk[16];
-        tmem_ld16(taddr + 32 * q, t0);
-        tmem_ld16(taddr + 32 * q + 16, t1);
-        tmem_ld_wait();
+__device__ __forceinline__ void tmem_half_to_bf16(uint32_t taddr, int hf, F f, uint32_t (&pk)[32]) {
+    uint32_t t0[32], t1[32];
+    tmem_ld32(taddr + 64 * hf, t0);
+    tmem_ld32(taddr + 64 * hf + 32, t1);
+    tmem_wait_ld(t0);
+    tmem_wait_ld(t1);
 #pragma unroll
-        for (int j2 = 0; j2 < 16; ++j2) {
-            const int j = 32 * q + 2 * j2;
-            const uint32_t lo = j2 < 8 ? t0[2 * j2] : t1[2 * j2 - 16];
-            const uint32_t hi = j2 < 8 ? t0[2 * j2 + 1] : t1[2 * j2 - 15];
-            pk[j2] = pack_bf16(f(j, __uint_as_float(lo)), f(j + 1, __uint_as_float(hi)));
-        }
-        tmem_st16(taddr + 16 * q, pk);
-    }
-    tmem_st_wait();
-}
-
-// Row `row` of the state tile (fp32 TMEM block, 128 columns) rounded into the bf16 operand tile.
-__device__ __forceinline__ void tmem_row_to_tile(uint32_t taddr, unsigned char *tile2, int row) {
-#pragma unroll 1
-    for (int c16 = 0; c16 < 8; ++c16) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c16 * 16, v);
-        tmem_ld_wait();
-        unsigned char *tile = tile2 + (c16 / 4) * kBox;
-        const int col8 = (c16 % 4) * 2;
-#pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[8 * g2 + 0]), __uint_as_float(v[8 * g2 + 1]));
-            w.y = pack_bf16(__uint_as_float(v[8 * g2 + 2]), __uint_as_float(v[8 * g2 + 3]));
-            w.z = pack_bf16(__uint_as_float(v[8 * g2 + 4]), __uint_as_float(v[8 * g2 + 5]));
-            w.w = pack_bf16(__uint_as_float(v[8 * g2 + 6]), __uint_as_float(v[8 * g2 + 7]));
-            *(uint4 *)(tile + sw128_off(row, col8 + g2)) = w;
-        }
+    for (int m = 0; m < 32; ++m) {
+        const int c = 64 * hf + 2 * m;
+        const uint32_t a0 = m < 16 ? t0[2 * m] : t1[2 * m - 32];
+        const uint32_t a1 = m < 16 ? t0[2 * m + 1] : t1[2 * m - 31];
+        pk[m] = pack_bf16(f(c, __uint_as_float(a0)), f(c + 1, __uint_as_float(a1)));
     }
 }
 
-// Sum over the chunk's rows r of w[r] * X[r][col..col+1] for a bf16 tile X (two 64-column boxes).
-__device__ __forceinline__ float2 weighted_colsum(const unsigned char *tile2, int col, const float *w) {
+// Sum over rows [64 rh, 64 rh + 64) of w[r] * X[r][2 cp .. 2 cp + 1] for a bf16 tile X (two 64-column
+// boxes, 128-byte swizzle); w == nullptr means weights of one.
+__device__ __forceinline__ float2 colsum_half(const unsigned char *tile2, int cp, int rh, const float *w) {
+    const int col = 2 * cp;
     const unsigned char *tile = tile2 + (col / 64) * kBox;
     const int cc = col % 64;
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll 8
-    for (int r = 0; r < kC; ++r) {
+    for (int r = 64 * rh; r < 64 * rh + 64; ++r) {
         const uint32_t v = *(const uint32_t *)(tile + sw128_off(r, cc / 8) + (cc % 8) * 2);
         const float wr = w ? w[r] : 1.f;
         s0 = fmaf(wr, bf16lo(v), s0);
@@ -85,57 +65,53 @@ __device__ __forceinline__ float2 weighted_colsum(const unsigned char *tile2, in
     return make_float2(s0, s1);
 }
 
-// Writes 16 fp32 values (x[c] + add_scale * add[c]) as bf16 into row `row`, columns 16 c16 .. +15, of a
-// two-box 128B-swizzled tile (the layout the output TMA map expects).
-__device__ __forceinline__ void stage16_bf16(unsigned char *tile2, int row, int c16, const uint32_t (&v)[16],
-                                             const float *add, float add_scale) {
-    float f[16];
+// Reads this half's 64 columns of an fp32 TMEM block, adds add_scale * add[c] (c = column), rounds to
+// bf16 and writes them into row `row`, box hf of a two-box 128B-swizzled tile (the layout of the output
+// TMA maps).
+__device__ __forceinline__ void tmem_half_to_out(uint32_t taddr, int hf, const float *add, float add_scale,
+                                                 unsigned char *tile2, int row) {
+    unsigned char *tile = tile2 + hf * kBox;
+#pragma unroll 1
+    for (int half32 = 0; half32 < 2; ++half32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 64 * hf + 32 * half32, v);
+        tmem_wait_ld(v);
+        const float *aa = add + 64 * hf + 32 * half32;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]) + add_scale * add[j];
-    unsigned char *tile = tile2 + (c16 / 4) * kBox;
-    const int col8 = (c16 % 4) * 2;
+        for (int g4 = 0; g4 < 4; ++g4) {
+            uint4 w;
+            uint32_t *wv = (uint32_t *)&w;
 #pragma unroll
-    for (int g2 = 0; g2 < 2; ++g2) {
-        uint4 w;
-        w.x = pack_bf16(f[8 * g2 + 0], f[8 * g2 + 1]);
-        w.y = pack_bf16(f[8 * g2 + 2], f[8 * g2 + 3]);
-        w.z = pack_bf16(f[8 * g2 + 4], f[8 * g2 + 5]);
-        w.w = pack_bf16(f[8 * g2 + 6], f[8 * g2 + 7]);
-        *(uint4 *)(tile + sw128_off(row, col8 + g2)) = w;
+            for (int q = 0; q < 4; ++q) {
+                const int m = 8 * g4 + 2 * q;
+                wv[q] = pack_bf16(__uint_as_float(v[m]) + add_scale * aa[m],
+                                  __uint_as_float(v[m + 1]) + add_scale * aa[m + 1]);
+            }
+            *(uint4 *)(tile + sw128_off(row, 4 * half32 + g4)) = w;
+        }
     }
 }
 
-// Stores 16 fp32 values (x[c] * scale + add[c]) as bf16 at dst (16-byte aligned).
-__device__ __forceinline__ void store16_bf16(__nv_bfloat16 *dst, const uint32_t (&v)[16], const float *add,
-                                             float add_scale, float scale) {
-    uint4 w0, w1;
-    float f[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) f[j] = (__uint_as_float(v[j]) + add_scale * add[j]) * scale;
-    w0.x = pack_bf16(f[0], f[1]);
-    w0.y = pack_bf16(f[2], f[3]);
-    w0.z = pack_bf16(f[4], f[5]);
-    w0.w = pack_bf16(f[6], f[7]);
-    w1.x = pack_bf16(f[8], f[9]);
-    w1.y = pack_bf16(f[10], f[11]);
-    w1.z = pack_bf16(f[12], f[13]);
-    w1.w = pack_bf16(f[14], f[15]);
-    uint4 *d = (uint4 *)dst;
-    d[0] = w0;
-    d[1] = w1;
+// Issues the TMA stores of a two-box output tile from shared memory and commits them.  One thread.
+__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, int h) {
+    tma_store_3d(map, tile2, 0, row0, h);
+    tma_store_3d(map, tile2 + kBox, 64, row0, h);
+    bulk_commit();
 }
 
 // ----------------------------------------------------------------------------------------------------
 // dQ walk (chunk order).  Per chunk, causal:
 //   T = Q K^T -> P (bf16, TMEM) ; O = P V + Q Sb ; S += K^T V            (the forward, recomputed)
-//   epilogue: O_i, g_i, delta_i ; dO tile <- dOt = dO / g (in place) ; g_i, dt_i to the workspace
+//   epilogue: g_i, O_i, delta_i ; dO tile <- dOt = dO / g (in place) ; g_i, dt_i to the workspace
 //   W = dOt V^T -> U = [j <= i](W - dt_i) (bf16, TMEM) ; X = dOt Sb^T + U K ; Ppiece += Q^T dOt
-//   epilogue: dQ_i = X_i - dt_i z ; y += sum dt_i q_i, e += sum dOt_i (fp32, CUDA cores)
+//   epilogue: dQ_i = X_i - dt_i z (staged in the Q tile, stored by TMA) ; column sums for z, a, y, e
 // Non-causal: O = Q Sb and X = dOt Sb^T with the head's totals; stages hold only Q and dO.
 // TMEM: R0 T/P then W/U, R1 O then X, R2 S, R3 the piece's reverse sum P.
+// Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128; for the
+// column sums it owns column pair cp = u % 64 of tensor u / 128 over row half (u / 64) % 2.
 // ----------------------------------------------------------------------------------------------------
 template <bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr int NST = CAUSAL ? 1 : 2;
     constexpr uint32_t TB = NB * kBox;
@@ -145,10 +121,13 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
     unsigned char *stages = sm;
     unsigned char *Sb = sm + NST * STAGE;
-    float *zc = (float *)(Sb + TB);
-    float *ac = zc + D;
-    float *sDt = ac + D;
-    uint64_t *full = (uint64_t *)(sDt + kC);
+    float *zc = (float *)(Sb + TB);  // z before the chunk (fp32, D)
+    float *ac = zc + D;              // a before the chunk
+    float *sDt = ac + D;             // dt_i of the chunk's rows
+    float *xg = sDt + kC;            // [2][128] row partials of g (per column half)
+    float *xd = xg + 2 * kC;         // [2][128] row partials of delta
+    float *cs = xd + 2 * kC;         // [2 tensors][2 row halves][128 columns] column-sum partials
+    uint64_t *full = (uint64_t *)(cs + 4 * D);
     uint64_t *empty = full + NST;
     uint64_t *bar = empty + NST;
     uint64_t *barT = bar, *barP = bar + 1, *barSb = bar + 2, *barO = bar + 3, *barDt = bar + 4, *barW = bar + 5,
@@ -164,7 +143,8 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dQ tile has left the Q tile
         }
-        const uint32_t counts[12] = {1, 128, 128, 1, 128, 1, 128, 1, 1, 1, 128, 128};
+        const uint32_t E = kEpiThreads;
+        const uint32_t counts[12] = {1, E, E, 1, E, 1, E, 1, 1, 1, E, E};
         for (int k = 0; k < 12; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -297,13 +277,12 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
             }
         }
     } else if (warp >= 2) {
-        // ---- epilogue warps: thread <-> chunk row i (TMEM lane) and state row d (same index)
-        const int lb = 32 * (warp & 3);
-        const int i = lb + lane;
-        const int t = threadIdx.x - 64;
-        const int col = 2 * (t & 63);
-        const uint32_t lo = (uint32_t)lb << 16;
-        __nv_bfloat16 *dQg = (__nv_bfloat16 *)P.dQ;
+        // ---- epilogue
+        const int u = threadIdx.x - 64;
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int i = 32 * q4 + lane;
+        const int which = u >> 7, cp = u & 63, rh = (u >> 6) & 1;  // column-sum role
+        const uint32_t lo = (uint32_t)(32 * q4) << 16;
         int it = 0, pno = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
@@ -313,12 +292,13 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x30A)) break;
                 tc_fence_after();
             }
-            load_carry1(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, R2 + lo, Sb, zc, ac, CAUSAL);
+            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, R2 + lo, 0u, 0u, Sb, zc,
+                            ac, CAUSAL, /*vec_to_tmem=*/false);
             fence_proxy_async_smem();
             tc_fence_before();
-            epi_sync();
+            epi_sync256();
             mbar_arrive(barSb);
-            float2 ye = make_float2(0.f, 0.f);  // y (t < 64) or e (t >= 64) of this piece, two columns
+            float2 ye = make_float2(0.f, 0.f);  // this thread's part of y (which 0) or e (which 1)
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 const int s = it % NST;
                 const uint32_t ph = it & 1;
@@ -326,146 +306,138 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
                 unsigned char *qt = st, *ot = st + TB, *kt = st + 2 * TB, *vt = st + 3 * TB;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
-                const bool row_ok = i < nvalid;
-                float r = 0.f;
-                if (CAUSAL) {
+                float part = 0.f;
+                if (CAUSAL) {  // P = [j <= i](1 + T); partial r_i over this half's columns (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int q = 0; q < kC / 32; ++q) {  // P = [j <= i](1 + T), r_i = sum_j P_ij (fp32)
-                        uint32_t t0[16], t1[16], pk[16];
-                        tmem_ld16(R0 + lo + 32 * q, t0);
-                        tmem_ld16(R0 + lo + 32 * q + 16, t1);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j2 = 0; j2 < 16; ++j2) {
-                            const int j = 32 * q + 2 * j2;
-                            const uint32_t a0 = j2 < 8 ? t0[2 * j2] : t1[2 * j2 - 16];
-                            const uint32_t a1 = j2 < 8 ? t0[2 * j2 + 1] : t1[2 * j2 - 15];
-                            const float p0 = j <= i ? 1.f + __uint_as_float(a0) : 0.f;
-                            const float p1 = j + 1 <= i ? 1.f + __uint_as_float(a1) : 0.f;
-                            pk[j2] = pack_bf16(p0, p1);
-                            r += p0 + p1;
-                        }
-                        tmem_st16(R0 + lo + 16 * q, pk);
-                    }
+                    uint32_t pk[32];
+                    tmem_half_to_bf16(R0 + lo, hf, [&](int j, float x) {
+                        const float p = j <= i ? 1.f + x : 0.f;
+                        part += p;
+                        return p;
+                    }, pk);
+                    tc_fence_before();
+                    epi_sync256();
+                    tc_fence_after();
+                    tmem_st32(R0 + lo + 32 * hf, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barP);
                 }
-                // q_i . z with z before the chunk
-                float qz = 0.f;
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        const uint4 v = *(const uint4 *)(qt + nb * kBox + sw128_off(i, g8));
-                        const float *zz = zc + nb * 64 + g8 * 8;
-                        qz += bf16lo(v.x) * zz[0] + bf16hi(v.x) * zz[1] + bf16lo(v.y) * zz[2] + bf16hi(v.y) * zz[3] +
-                              bf16lo(v.z) * zz[4] + bf16hi(v.z) * zz[5] + bf16lo(v.w) * zz[6] + bf16hi(v.w) * zz[7];
-                    }
+                part += dot_half(qt, i, hf, zc);  // q_i . z, z before the chunk
+                xg[hf * kC + i] = part;
+                float2 zn = make_float2(0.f, 0.f);
+                if (CAUSAL) {  // column sums of K (which 0) and V (which 1) over this thread's row half
+                    const float2 v = colsum_half(which == 0 ? kt : vt, cp, rh, nullptr);
+                    cs[(which * 2 + rh) * D + 2 * cp] = v.x;
+                    cs[(which * 2 + rh) * D + 2 * cp + 1] = v.y;
                 }
-                float2 zn = make_float2(0.f, 0.f);  // z (t < 64) or a (t >= 64) after this chunk
-                if (CAUSAL) {
-                    const float2 cs = weighted_colsum(t < 64 ? kt : vt, col, nullptr);
-                    const float *base = t < 64 ? zc : ac;
-                    zn = make_float2(base[col] + cs.x, base[col + 1] + cs.y);
+                epi_sync256();
+                const float gi = (CAUSAL ? (float)row0 : (float)P.N) + xg[i] + xg[kC + i];
+                const float ig = 1.f / gi;
+                if (CAUSAL && rh == 0) {
+                    const float *base = which == 0 ? zc : ac;
+                    const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
+                    zn = make_float2(base[2 * cp] + c0[2 * cp] + c1[2 * cp], base[2 * cp + 1] + c0[2 * cp + 1] + c1[2 * cp + 1]);
                 }
-                // O_i, g_i, delta_i; dO row -> dOt row in place
+                // O_i over this half's columns, delta partial, and dO -> dOt in place
                 ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x30C);
                 if (!ok) break;
                 tc_fence_after();
-                const float gi = (CAUSAL ? (float)row0 : (float)P.N) + qz + r;
-                const float ig = 1.f / gi;
-                float delta = 0.f;
+                float dpart = 0.f;
+                {
+                    unsigned char *tile = ot + hf * kBox;
 #pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    uint32_t v[16];
-                    tmem_ld16(R1 + lo + c16 * 16, v);
-                    tmem_ld_wait();
-                    unsigned char *tile = ot + (c16 / 4) * kBox;
-                    const int col8 = (c16 % 4) * 2;
+                    for (int half32 = 0; half32 < 2; ++half32) {
+                        uint32_t v[32];
+                        tmem_ld32(R1 + lo + 64 * hf + 32 * half32, v);
+                        tmem_wait_ld(v);
+                        const float *aa = ac + 64 * hf + 32 * half32;
 #pragma unroll
-                    for (int g2 = 0; g2 < 2; ++g2) {
-                        uint4 *p4 = (uint4 *)(tile + sw128_off(i, col8 + g2));
-                        uint4 w = *p4;
-                        uint32_t *wv = (uint32_t *)&w;
+                        for (int g4 = 0; g4 < 4; ++g4) {
+                            uint4 *p4 = (uint4 *)(tile + sw128_off(i, 4 * half32 + g4));
+                            uint4 w = *p4;
+                            uint32_t *wv = (uint32_t *)&w;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = c16 * 16 + g2 * 8 + 2 * q;
-                            const float o0 = (__uint_as_float(v[g2 * 8 + 2 * q]) + ac[e]) * ig;
-                            const float o1 = (__uint_as_float(v[g2 * 8 + 2 * q + 1]) + ac[e + 1]) * ig;
-                            const float d0 = bf16lo(wv[q]), d1 = bf16hi(wv[q]);
-                            delta = fmaf(d0, o0, fmaf(d1, o1, delta));
-                            wv[q] = pack_bf16(d0 * ig, d1 * ig);
+                            for (int q = 0; q < 4; ++q) {
+                                const int m = 8 * g4 + 2 * q;
+                                const float o0 = (__uint_as_float(v[m]) + aa[m]) * ig;
+                                const float o1 = (__uint_as_float(v[m + 1]) + aa[m + 1]) * ig;
+                                const float d0 = bf16lo(wv[q]), d1 = bf16hi(wv[q]);
+                                dpart = fmaf(d0, o0, fmaf(d1, o1, dpart));
+                                wv[q] = pack_bf16(d0 * ig, d1 * ig);
+                            }
+                            *p4 = w;
                         }
-                        *p4 = w;
                     }
                 }
-                const float dt = delta * ig;
-                sDt[i] = dt;
-                if (row_ok) {
-                    P.rs_g[(size_t)pc.h * P.N + row0 + i] = gi;
-                    P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
-                }
+                xd[hf * kC + i] = dpart;
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(barDt);
+                epi_sync256();
+                const float dt = (xd[i] + xd[kC + i]) * ig;
+                if (hf == 0) {
+                    sDt[i] = dt;
+                    if (i < nvalid) {
+                        P.rs_g[(size_t)pc.h * P.N + row0 + i] = gi;
+                        P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
+                    }
+                }
                 if (CAUSAL) {  // U = [j <= i](W - dt), bf16, in place of W
                     ok = wait_or_abort(barW, ph, abort_flag, P.status, 0x30D);
                     if (!ok) break;
                     tc_fence_after();
-                    tmem_to_bf16_inplace(R0 + lo, [&](int j, float w) { return j <= i ? w - dt : 0.f; });
+                    uint32_t pk[32];
+                    tmem_half_to_bf16(R0 + lo, hf, [&](int j, float w) { return j <= i ? w - dt : 0.f; }, pk);
+                    tc_fence_before();
+                    epi_sync256();
+                    tc_fence_after();
+                    tmem_st32(R0 + lo + 32 * hf, pk);
+                    tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barU);
+                } else {
+                    epi_sync256();  // sDt is complete
                 }
-                epi_sync();  // every row's dt and dOt are in shared memory
-                {
-                    const float2 cs = weighted_colsum(t < 64 ? qt : ot, col, t < 64 ? sDt : nullptr);
-                    ye.x += cs.x;
-                    ye.y += cs.y;
+                {  // y += sum_i dt_i q_i (which 0), e += sum_i dOt_i (which 1), over this thread's row half
+                    const float2 v = colsum_half(which == 0 ? qt : ot, cp, rh, which == 0 ? sDt : nullptr);
+                    ye.x += v.x;
+                    ye.y += v.y;
                 }
-                // dQ_i = X_i - dt_i z, staged in the Q tile (every MMA and column sum that reads Q is done
-                // once X is complete and all threads are past this barrier) and stored by TMA
+                // dQ_i = X_i - dt_i z: staged in the Q tile, whose readers (MMAs, q . z, the y sums) are done
                 ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);
                 if (!ok) break;
                 tc_fence_after();
-                epi_sync();
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    uint32_t v[16];
-                    tmem_ld16(R1 + lo + c16 * 16, v);
-                    tmem_wait_ld(v);
-                    stage16_bf16(qt, i, c16, v, zc + c16 * 16, -dt);
-                }
-                (void)row_ok;
-                (void)dQg;
+                epi_sync256();
+                tmem_half_to_out(R1 + lo, hf, zc, -dt, qt, i);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                epi_sync();
-                if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < NB; ++nb) tma_store_3d(&P.tmdQ, qt + nb * kBox, nb * 64, (int)row0, (int)pc.h);
-                    bulk_commit();
+                if (!CAUSAL) mbar_arrive(barXf);
+                epi_sync256();
+                if (u == 0) {
+                    store_tile(&P.tmdQ, qt, (int)row0, (int)pc.h);
                     bulk_wait_read0();
                     mbar_arrive(&empty[s]);
                 }
-                if (!CAUSAL) mbar_arrive(barXf);
                 if (CAUSAL) {
                     ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x30F);
                     if (!ok) break;
                     tc_fence_after();
                     if (c + 1 < pc.e) {
-                        tmem_row_to_tile(R2 + lo, Sb, i);
+                        tmem_half_to_tile(R2 + lo, Sb, i, hf);
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(barSb);
                     }
-                    epi_sync();  // everyone is done with z and a of this chunk
-                    float *base = t < 64 ? zc : ac;
-                    base[col] = zn.x;
-                    base[col + 1] = zn.y;
-                    epi_sync();
+                    // z (which 0) and a (which 1) after this chunk
+                    if (rh == 0) {
+                        float *base = which == 0 ? zc : ac;
+                        base[2 * cp] = zn.x;
+                        base[2 * cp + 1] = zn.y;
+                    }
+                    epi_sync256();
                 }
             }
             if (!ok) break;
@@ -474,20 +446,28 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dq_kernel(const __grid_constant
             tc_fence_after();
             float *slot = P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride;
 #pragma unroll 1
-            for (int c16 = 0; c16 < D / 16; ++c16) {
-                uint32_t v[16];
-                tmem_ld16(R3 + lo + c16 * 16, v);
-                tmem_ld_wait();
-                float4 *dst = (float4 *)(slot + (size_t)i * D + c16 * 16);
+            for (int half32 = 0; half32 < 2; ++half32) {
+                uint32_t v[32];
+                tmem_ld32(R3 + lo + 64 * hf + 32 * half32, v);
+                tmem_wait_ld(v);
+                float4 *dst = (float4 *)(slot + (size_t)i * D + 64 * hf + 32 * half32);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                for (int q = 0; q < 8; ++q)
                     dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             }
-            slot[(size_t)D * D + (t < 64 ? 0 : D) + col] = ye.x;
-            slot[(size_t)D * D + (t < 64 ? 0 : D) + col + 1] = ye.y;
+            // y, e: add the two row halves
+            cs[(which * 2 + rh) * D + 2 * cp] = ye.x;
+            cs[(which * 2 + rh) * D + 2 * cp + 1] = ye.y;
             tc_fence_before();
+            epi_sync256();
+            if (rh == 0) {
+                const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
+                slot[(size_t)D * D + which * D + 2 * cp] = c0[2 * cp] + c1[2 * cp];
+                slot[(size_t)D * D + which * D + 2 * cp + 1] = c0[2 * cp + 1] + c1[2 * cp + 1];
+            }
             mbar_arrive(barPPf);
+            epi_sync256();  // cs is reused by the next piece
         }
     }
     if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
@@ -507,11 +487,11 @@ template __global__ void tc_bwd_dq_kernel<false>(const __grid_constant__ TcParam
 //   dK = U^T Q + V Pb^T  (then - y)        dV = P^T dO + K Pb  (then + e)
 //   dO tile <- dOt in place ; P += Q^T dOt (for the earlier chunks) ; y, e += this chunk's rows
 // Pb is the bf16 copy of P (the sum over later rows).  Non-causal: dK = V Pb^T - y, dV = K Pb + e with
-// the head's totals; stages hold only K and V.
+// the head's totals; stages hold only K and V.  dK leaves through the V tile and dV through the K tile.
 // TMEM: R0 T^T/P^T, R1 W^T/U^T, R2 dK then dV, R3 P.
 // ----------------------------------------------------------------------------------------------------
 template <bool CAUSAL>
-__global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr int NST = CAUSAL ? 1 : 3;
     constexpr uint32_t TB = NB * kBox;
@@ -524,9 +504,10 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
     unsigned char *Pb = sm + NST * STAGE;
     float *yc = (float *)(Pb + TB);
     float *ec = yc + D;
-    float *sIg = ec + D;
-    float *sDt = sIg + kC;
-    uint64_t *full = (uint64_t *)(sDt + kC);
+    float *sIg = ec + D;                  // causal only: 1/g_i and dt_i of the chunk's rows
+    float *sDt = sIg + (CAUSAL ? kC : 0);
+    float *cs = sDt + (CAUSAL ? kC : 0);  // causal only: [2][2][128] column-sum partials
+    uint64_t *full = (uint64_t *)(cs + (CAUSAL ? 4 * D : 0));
     uint64_t *empty = full + NST;
     uint64_t *bar = empty + NST;
     uint64_t *barT = bar, *barP = bar + 1, *barPb = bar + 2, *barK = bar + 3, *barKf = bar + 4, *barV = bar + 5,
@@ -541,7 +522,8 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dK, dV tiles have left shared memory
         }
-        const uint32_t counts[9] = {1, 128, 128, 1, 128, 1, 128, 1, 128};
+        const uint32_t E = kEpiThreads;
+        const uint32_t counts[9] = {1, E, E, 1, E, 1, E, 1, E};
         for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -666,27 +648,27 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
             }
         }
     } else if (warp >= 2) {
-        // ---- epilogue warps: thread <-> key row j (TMEM lane) and state row d (same index)
-        const int lb = 32 * (warp & 3);
-        const int j = lb + lane;
-        const int t = threadIdx.x - 64;
-        const int col = 2 * (t & 63);
-        const uint32_t lo = (uint32_t)lb << 16;
-        __nv_bfloat16 *dKg = (__nv_bfloat16 *)P.dK, *dVg = (__nv_bfloat16 *)P.dV;
+        // ---- epilogue: thread <-> key row j (TMEM lane) and column half hf
+        const int u = threadIdx.x - 64;
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int j = 32 * q4 + lane;
+        const int which = u >> 7, cp = u & 63, rh = (u >> 6) & 1;
+        const uint32_t lo = (uint32_t)(32 * q4) << 16;
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried reverse sums (causal: the later pieces of the head; non-causal: the whole head),
-            // combined into this piece's own slot by tc_scan_slots
+            // carried reverse sums (causal: later pieces of the head; non-causal: the whole head), combined
+            // into this piece's own slot by tc_scan_slots
             if (CAUSAL && it > 0) {
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x409)) break;
                 tc_fence_after();
             }
-            load_carry1(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, R3 + lo, Pb, yc, ec, CAUSAL);
+            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, R3 + lo, 0u, 0u, Pb, yc,
+                            ec, CAUSAL, /*vec_to_tmem=*/false);
             fence_proxy_async_smem();
             tc_fence_before();
-            epi_sync();
+            epi_sync256();
             mbar_arrive(barPb);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 const int s = it % NST;
@@ -695,98 +677,88 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
                 unsigned char *qt = st, *ot = st + TB;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
-                const bool row_ok = j < nvalid;
-                const size_t grow = (size_t)pc.h * P.N + row0 + j;
                 if (CAUSAL) {
-                    sIg[j] = row_ok ? 1.f / P.rs_g[grow] : 0.f;
-                    sDt[j] = row_ok ? P.rs_dt[grow] : 0.f;
-                    epi_sync();
+                    if (hf == 0) {
+                        const bool ok_row = j < nvalid;
+                        const size_t grow = (size_t)pc.h * P.N + row0 + j;
+                        sIg[j] = ok_row ? 1.f / P.rs_g[grow] : 0.f;
+                        sDt[j] = ok_row ? P.rs_dt[grow] : 0.f;
+                    }
+                    epi_sync256();
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x40A);
                     if (!ok) break;
                     tc_fence_after();
                     // columns are query rows i of the chunk: keep i >= j
-                    tmem_to_bf16_inplace(R0 + lo, [&](int i, float x) { return i >= j ? (1.f + x) * sIg[i] : 0.f; });
-                    tmem_to_bf16_inplace(R1 + lo, [&](int i, float x) { return i >= j ? x * sIg[i] - sDt[i] : 0.f; });
+                    uint32_t pk0[32], pk1[32];
+                    tmem_half_to_bf16(R0 + lo, hf, [&](int i, float x) { return i >= j ? (1.f + x) * sIg[i] : 0.f; }, pk0);
+                    tmem_half_to_bf16(R1 + lo, hf, [&](int i, float x) { return i >= j ? x * sIg[i] - sDt[i] : 0.f; }, pk1);
+                    tc_fence_before();
+                    epi_sync256();
+                    tc_fence_after();
+                    tmem_st32(R0 + lo + 32 * hf, pk0);
+                    tmem_st32(R1 + lo + 32 * hf, pk1);
+                    tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barP);
                 }
-                // dK_j = [dK accumulator]_j - y
+                // dK_j = [accumulator]_j - y, staged in the V tile (its last reader, dK += V Pb^T, is done)
                 ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
                 if (!ok) break;
                 tc_fence_after();
-                // dK staged in the V tile (its last reader, dK += V Pb^T, is complete) and stored by TMA
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    uint32_t v[16];
-                    tmem_ld16(R2 + lo + c16 * 16, v);
-                    tmem_wait_ld(v);
-                    stage16_bf16(st + OFF_V, j, c16, v, yc + c16 * 16, -1.f);
-                }
+                tmem_half_to_out(R2 + lo, hf, yc, -1.f, st + OFF_V, j);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(barKf);
-                epi_sync();
-                if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < NB; ++nb)
-                        tma_store_3d(&P.tmdK, st + OFF_V + nb * kBox, nb * 64, (int)row0, (int)pc.h);
-                    bulk_commit();
-                }
-                // dV_j = [dV accumulator]_j + e
+                epi_sync256();
+                if (u == 0) store_tile(&P.tmdK, st + OFF_V, (int)row0, (int)pc.h);
+                // dV_j = [accumulator]_j + e, staged in the K tile (its last reader, dV += K Pb, is done)
                 ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x40C);
                 if (!ok) break;
                 tc_fence_after();
-                // dV staged in the K tile (its last reader, dV += K Pb, is complete) and stored by TMA
-#pragma unroll 1
-                for (int c16 = 0; c16 < D / 16; ++c16) {
-                    uint32_t v[16];
-                    tmem_ld16(R2 + lo + c16 * 16, v);
-                    tmem_wait_ld(v);
-                    stage16_bf16(st + OFF_K, j, c16, v, ec + c16 * 16, 1.f);
-                }
-                (void)row_ok;
-                (void)dKg;
-                (void)dVg;
+                tmem_half_to_out(R2 + lo, hf, ec, 1.f, st + OFF_K, j);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                epi_sync();
-                if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < NB; ++nb)
-                        tma_store_3d(&P.tmdV, st + OFF_K + nb * kBox, nb * 64, (int)row0, (int)pc.h);
-                    bulk_commit();
-                }
+                if (!CAUSAL) mbar_arrive(barVf);
+                epi_sync256();
+                if (u == 0) store_tile(&P.tmdV, st + OFF_K, (int)row0, (int)pc.h);
                 if (!CAUSAL) {
-                    mbar_arrive(barVf);
-                    if (threadIdx.x == 64) {
+                    if (u == 0) {
                         bulk_wait_read0();
                         mbar_arrive(&empty[s]);
                     }
                     continue;
                 }
-                // dO row -> dOt row in place; then y and e gain this chunk's rows
+                // dO row -> dOt row in place, for P += Q^T dOt and the e sums
                 {
                     const float igj = sIg[j];
+                    unsigned char *tile = ot + hf * kBox;
 #pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        uint4 *p4 = (uint4 *)(tile + sw128_off(j, g8));
+                        uint4 w = *p4;
+                        uint32_t *wv = (uint32_t *)&w;
 #pragma unroll
-                        for (int g8 = 0; g8 < 8; ++g8) {
-                            uint4 *p4 = (uint4 *)(ot + nb * kBox + sw128_off(j, g8));
-                            uint4 w = *p4;
-                            uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * igj, bf16hi(wv[q]) * igj);
-                            *p4 = w;
-                        }
+                        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * igj, bf16hi(wv[q]) * igj);
+                        *p4 = w;
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(barDt);
-                epi_sync();  // every row of dOt is in shared memory
-                const float2 cs = weighted_colsum(t < 64 ? qt : ot, col, t < 64 ? sDt : nullptr);
-                float *base = t < 64 ? yc : ec;
-                const float2 yn = make_float2(base[col] + cs.x, base[col + 1] + cs.y);
-                epi_sync();  // every read of the stage by this warp group is done
-                if (threadIdx.x == 64) {
+                epi_sync256();  // every row of dOt is in shared memory
+                {  // this chunk's rows: y += sum dt_i q_i (which 0), e += sum dOt_i (which 1)
+                    const float2 v = colsum_half(which == 0 ? qt : ot, cp, rh, which == 0 ? sDt : nullptr);
+                    cs[(which * 2 + rh) * D + 2 * cp] = v.x;
+                    cs[(which * 2 + rh) * D + 2 * cp + 1] = v.y;
+                }
+                epi_sync256();
+                float2 yn = make_float2(0.f, 0.f);
+                if (rh == 0) {
+                    const float *base = which == 0 ? yc : ec;
+                    const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
+                    yn = make_float2(base[2 * cp] + c0[2 * cp] + c1[2 * cp], base[2 * cp + 1] + c0[2 * cp + 1] + c1[2 * cp + 1]);
+                }
+                if (u == 0) {
                     bulk_wait_read0();  // dK and dV have left the V and K tiles
                     mbar_arrive(&empty[s]);
                 }
@@ -794,15 +766,17 @@ __global__ void __launch_bounds__(192, 1) tc_bwd_dkdv_kernel(const __grid_consta
                 if (!ok) break;
                 tc_fence_after();
                 if (c > pc.a) {
-                    tmem_row_to_tile(R3 + lo, Pb, j);
+                    tmem_half_to_tile(R3 + lo, Pb, j, hf);
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(barPb);
                 }
-                epi_sync();  // everyone is done with y and e of this chunk
-                base[col] = yn.x;
-                base[col + 1] = yn.y;
-                epi_sync();
+                if (rh == 0) {
+                    float *base = which == 0 ? yc : ec;
+                    base[2 * cp] = yn.x;
+                    base[2 * cp + 1] = yn.y;
+                }
+                epi_sync256();
             }
         }
     }
@@ -824,21 +798,21 @@ template __global__ void tc_bwd_dkdv_kernel<false>(const __grid_constant__ TcPar
 namespace {
 
 constexpr size_t kTB = 2 * (size_t)tc::kBox;
-constexpr size_t kSmemDq = 4 * kTB + kTB + 3 * 512 + 512;          // causal: 1 stage of Q, dO, K, V
-constexpr size_t kSmemDqNc = 2 * 2 * kTB + kTB + 3 * 512 + 512;    // 2 stages of Q, dO
-constexpr size_t kSmemDkdv = 4 * kTB + kTB + 4 * 512 + 512;        // 1 stage of Q, dO, K, V
-constexpr size_t kSmemDkdvNc = 3 * 2 * kTB + kTB + 4 * 512 + 512;  // 3 stages of K, V
-static_assert(kSmemDkdvNc <= 232448, "dK/dV kernel exceeds the shared-memory limit");
+constexpr size_t kEpiSmemDq = 2 * 128 * 4 + 128 * 4 + 4 * 128 * 4 + 4 * 128 * 4;  // z, a, dt, 2 x-arrays, cs
+constexpr size_t kSmemDq = 4 * kTB + kTB + kEpiSmemDq + 512;         // causal: 1 stage of Q, dO, K, V
+constexpr size_t kSmemDqNc = 2 * 2 * kTB + kTB + kEpiSmemDq + 512;   // 2 stages of Q, dO
+constexpr size_t kSmemDkdv = 4 * kTB + kTB + 4 * 128 * 4 + 4 * 128 * 4 + 512;  // y, e, 1/g, dt, cs
+constexpr size_t kSmemDkdvNc = 3 * 2 * kTB + kTB + 2 * 128 * 4 + 512;         // 3 stages of K, V
+static_assert(kSmemDkdvNc <= 232448 && kSmemDq <= 232448, "backward kernel exceeds the shared-memory limit");
 
 bool set_bwd_attrs() {
     static int done = 0;
     if (done) return done > 0;
-    const int A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    bool ok = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<true>, (cudaFuncAttribute)A, (int)kSmemDq) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<false>, (cudaFuncAttribute)A, (int)kSmemDqNc) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<true>, (cudaFuncAttribute)A, (int)kSmemDkdv) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<false>, (cudaFuncAttribute)A, (int)kSmemDkdvNc) ==
-                  cudaSuccess;
+    const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    bool ok = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<true>, A, (int)kSmemDq) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<false>, A, (int)kSmemDqNc) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<true>, A, (int)kSmemDkdv) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<false>, A, (int)kSmemDkdvNc) == cudaSuccess;
     done = ok ? 1 : -1;
     return ok;
 }
@@ -861,19 +835,20 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dQ = dQ;
     P.dK = dK;
     P.dV = dV;
+    const unsigned nthr = 64 + tc::kEpiThreads;
     cudaError_t e = tc_host::launch_agg(P, s);
     if (e == cudaSuccess) e = tc_host::launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
     if (e != cudaSuccess) return e;
     if (p.causal)
-        tc::tc_bwd_dq_kernel<true><<<P.sl.G, 192, kSmemDq, s>>>(P);
+        tc::tc_bwd_dq_kernel<true><<<P.sl.G, nthr, kSmemDq, s>>>(P);
     else
-        tc::tc_bwd_dq_kernel<false><<<P.sl.G, 192, kSmemDqNc, s>>>(P);
+        tc::tc_bwd_dq_kernel<false><<<P.sl.G, nthr, kSmemDqNc, s>>>(P);
     e = tc_host::launch_scan(P.slots_rev, P, p.BH, p.causal ? 1 : 2, s);
     if (e != cudaSuccess) return e;
     if (p.causal)
-        tc::tc_bwd_dkdv_kernel<true><<<P.sl.G, 192, kSmemDkdv, s>>>(P);
+        tc::tc_bwd_dkdv_kernel<true><<<P.sl.G, nthr, kSmemDkdv, s>>>(P);
     else
-        tc::tc_bwd_dkdv_kernel<false><<<P.sl.G, 192, kSmemDkdvNc, s>>>(P);
+        tc::tc_bwd_dkdv_kernel<false><<<P.sl.G, nthr, kSmemDkdvNc, s>>>(P);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(5);
     return e;

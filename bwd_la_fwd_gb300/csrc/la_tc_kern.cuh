@@ -65,10 +65,11 @@ __device__ __forceinline__ void load_carry1(const float *slot, int d, uint32_t t
 
 // Half `hf` of the carried state `slot` ([S row-major | z | a], fp32) for row d: columns [64 hf, 64 hf + 64)
 // of S into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes z[d]
-// to zc (and TMEM column tZ), half 1 writes a[d] to ac (and TMEM column tA).  All loads are issued
+// to zc (and TMEM column tZ if to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and TMEM column tA).  All loads are issued
 // before any is used.
 __device__ __forceinline__ void load_carry_half(const float *slot, int d, int hf, uint32_t tS, uint32_t tZ,
-                                                uint32_t tA, unsigned char *Sb, float *zc, float *ac, bool to_tmem) {
+                                                uint32_t tA, unsigned char *Sb, float *zc, float *ac, bool to_tmem,
+                                                bool vec_to_tmem = true) {
     constexpr int D = 128;
     const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
     float4 v4[16];
@@ -97,10 +98,8 @@ __device__ __forceinline__ void load_carry_half(const float *slot, int d, int hf
         }
     }
     (hf == 0 ? zc : ac)[d] = vsum;
-    if (to_tmem) {
-        tmem_st1(hf == 0 ? tZ : tA, __float_as_uint(vsum));
-        tmem_st_wait();
-    }
+    if (to_tmem && vec_to_tmem) tmem_st1(hf == 0 ? tZ : tA, __float_as_uint(vsum));
+    if (to_tmem) tmem_st_wait();
 }
 
 // Row d's 64 columns [64 hf, 64 hf + 64) of an fp32 TMEM block, rounded into box hf of a bf16 operand tile.

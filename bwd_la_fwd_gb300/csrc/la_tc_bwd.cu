@@ -100,13 +100,14 @@ __device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigne
 }
 
 // ----------------------------------------------------------------------------------------------------
-// dQ walk (chunk order).  Per chunk, causal:
-//   T = Q K^T -> P (bf16, TMEM) ; O = P V + Q Sb ; S += K^T V            (the forward, recomputed)
-//   epilogue: g_i, O_i, delta_i ; dO tile <- dOt = dO / g (in place) ; g_i, dt_i to the workspace
-//   W = dOt V^T -> U = [j <= i](W - dt_i) (bf16, TMEM) ; X = dOt Sb^T + U K ; Ppiece += Q^T dOt
-//   epilogue: dQ_i = X_i - dt_i z (staged in the Q tile, stored by TMA) ; column sums for z, a, y, e
-// Non-causal: O = Q Sb and X = dOt Sb^T with the head's totals; stages hold only Q and dO.
-// TMEM: R0 T/P then W/U, R1 O then X, R2 S, R3 the piece's reverse sum P.
+// dQ walk (chunk order).  The forward output is not recomputed: with W' = dO V^T and Y = dO Sb^T (Sb =
+// bf16 state before the chunk),
+//   delta_i g_i = dO_i . a + sum_j P_ij W'_ij + q_i . Y_i,      P_ij = [j <= i](1 + q_i . k_j)
+//   dQ_i = (Y_i + [U' K]_i) / g_i - dt_i z,                     U'_ij = [j <= i](W'_ij - delta_i)
+// Per chunk, causal: T = Q K^T and W' (R0, R1); S += K^T V (R2); the epilogue forms P, r_i and
+// sum_j P_ij W'_ij from T and W' in registers; Y into R0; the epilogue forms g_i, delta_i, dt_i and U'
+// (bf16, in place of W'); X = Y + U' K in R0; dO -> dO / g in place; Ppiece += Q^T (dO / g) (R3).
+// Non-causal: only Y (R0, the head's totals) and Ppiece; stages hold only Q and dO.
 // Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128; for the
 // column sums it owns column pair cp = u % 64 of tensor u / 128 over row half (u / 64) % 2.
 // ----------------------------------------------------------------------------------------------------
@@ -125,15 +126,14 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     float *ac = zc + D;              // a before the chunk
     float *sDt = ac + D;             // dt_i of the chunk's rows
     float *xg = sDt + kC;            // [2][128] row partials of g (per column half)
-    float *xd = xg + 2 * kC;         // [2][128] row partials of delta
+    float *xd = xg + 2 * kC;         // [2][128] row partials of delta g
     float *cs = xd + 2 * kC;         // [2 tensors][2 row halves][128 columns] column-sum partials
     uint64_t *full = (uint64_t *)(cs + 4 * D);
     uint64_t *empty = full + NST;
     uint64_t *bar = empty + NST;
-    uint64_t *barT = bar, *barP = bar + 1, *barSb = bar + 2, *barO = bar + 3, *barDt = bar + 4, *barW = bar + 5,
-             *barU = bar + 6, *barX = bar + 7, *barS = bar + 8, *barPP = bar + 9, *barPPf = bar + 10,
-             *barXf = bar + 11;
-    uint32_t *tslot = (uint32_t *)(bar + 12);
+    uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barDt = bar + 4, *barU = bar + 5,
+             *barX = bar + 6, *barS = bar + 7, *barPP = bar + 8, *barPPf = bar + 9, *barXf = bar + 10;
+    uint32_t *tslot = (uint32_t *)(bar + 11);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
@@ -141,11 +141,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dQ tile has left the Q tile
+            mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dQ tile has left shared memory
         }
         const uint32_t E = kEpiThreads;
-        const uint32_t counts[12] = {1, E, E, 1, E, 1, E, 1, 1, 1, E, E};
-        for (int k = 0; k < 12; ++k) mbar_init(&bar[k], counts[k]);
+        const uint32_t counts[11] = {1, E, E, 1, E, E, 1, 1, 1, E, E};
+        for (int k = 0; k < 11; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -213,16 +213,14 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 const uint32_t qb = smem_u32(stages + s * STAGE), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
                 if (CAUSAL) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)  // T = Q K^T
-                        mma_ss(R0, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                               sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
+                    for (int k = 0; k < 8; ++k) {  // T = Q K^T ; W' = dO V^T
+                        const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
+                        mma_ss(R0, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idKK, k > 0);
+                        mma_ss(R1, sdesc_sw128(ob + o, 16, 1024), sdesc_sw128(vb + o, 16, 1024), idKK, k > 0);
+                    }
                     mma_commit(barT);
-                    ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x305);
+                    ok = wait_or_abort(barTr, ph, abort_flag, P.status, 0x305);  // T has been read out of R0
                     if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)  // O = P V
-                        mma_ts(R1, R0 + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, k > 0);
                     ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x306);
                     if (!ok) break;
                     tc_fence_after();
@@ -232,46 +230,33 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     tc_fence_after();
                 }
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // O += Q Sb
-                    mma_ss(R1, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
-                mma_commit(barO);
-                if (CAUSAL && c + 1 < pc.e) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)  // S += K^T V
-                        mma_ss(R2, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
-                               idMM, 1u);
-                }
-                ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x308);  // dOt is in place of dO
-                if (!ok) break;
-                tc_fence_after();
+                for (int k = 0; k < 8; ++k)  // Y = dO Sb^T
+                    mma_ss(R0, sdesc_sw128(ob + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                           sdesc_sw128(sb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
+                mma_commit(barY);
                 if (CAUSAL) {
+                    if (c + 1 < pc.e) {  // S += K^T V, once the epilogue has copied S into Sb (barSb above)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)  // W = dOt V^T
-                        mma_ss(R0, sdesc_sw128(ob + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                               sdesc_sw128(vb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
-                    mma_commit(barW);
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // Ppiece += Q^T dOt
-                    mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024), idMM,
-                           (c > pc.a || k > 0) ? 1u : 0u);
-                if (CAUSAL) {
-                    ok = wait_or_abort(barU, ph, abort_flag, P.status, 0x309);
+                        for (int k = 0; k < 8; ++k)
+                            mma_ss(R2, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
+                                   idMM, 1u);
+                    }
+                    ok = wait_or_abort(barU, ph, abort_flag, P.status, 0x308);
                     if (!ok) break;
                     tc_fence_after();
-                }
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // X = dOt Sb^T
-                    mma_ss(R1, sdesc_sw128(ob + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(sb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
-                if (CAUSAL) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)  // X += U K
-                        mma_ts(R1, R0 + 8 * k, sdesc_sw128(kb + 2048 * k, kBox, 1024), idKM, 1u);
+                    for (int k = 0; k < 8; ++k)  // X = Y + U' K
+                        mma_ts(R0, R1 + 8 * k, sdesc_sw128(kb + 2048 * k, kBox, 1024), idKM, 1u);
                 }
+                ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x309);  // dO / g is in place of dO
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // Ppiece += Q^T (dO / g)
+                    mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024), idMM,
+                           (c > pc.a || k > 0) ? 1u : 0u);
                 mma_commit(barX);
-                if (CAUSAL) mma_commit(barS);
+                mma_commit(barS);
                 mma_commit(&empty[s]);
                 if (c + 1 == pc.e) mma_commit(barPP);
             }
@@ -306,27 +291,32 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 unsigned char *qt = st, *ot = st + TB, *kt = st + 2 * TB, *vt = st + 3 * TB;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
-                float part = 0.f;
-                if (CAUSAL) {  // P = [j <= i](1 + T); partial r_i over this half's columns (fp32)
+                float gpart = 0.f, dpart = 0.f;  // partial g_i and partial delta_i g_i over this half
+                if (CAUSAL) {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
                     if (!ok) break;
                     tc_fence_after();
-                    uint32_t pk[32];
-                    tmem_half_to_bf16(R0 + lo, hf, [&](int j, float x) {
-                        const float p = j <= i ? 1.f + x : 0.f;
-                        part += p;
-                        return p;
-                    }, pk);
+                    uint32_t t0[32], w0[32];
+#pragma unroll 1
+                    for (int half32 = 0; half32 < 2; ++half32) {
+                        tmem_ld32(R0 + lo + 64 * hf + 32 * half32, t0);
+                        tmem_ld32(R1 + lo + 64 * hf + 32 * half32, w0);
+                        tmem_wait_ld(t0);
+                        tmem_wait_ld(w0);
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) {
+                            const int j = 64 * hf + 32 * half32 + m;
+                            const float pij = j <= i ? 1.f + __uint_as_float(t0[m]) : 0.f;
+                            gpart += pij;
+                            dpart = fmaf(pij, __uint_as_float(w0[m]), dpart);
+                        }
+                    }
                     tc_fence_before();
-                    epi_sync256();
-                    tc_fence_after();
-                    tmem_st32(R0 + lo + 32 * hf, pk);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(barP);
+                    mbar_arrive(barTr);
                 }
-                part += dot_half(qt, i, hf, zc);  // q_i . z, z before the chunk
-                xg[hf * kC + i] = part;
+                gpart += dot_half(qt, i, hf, zc);  // q_i . z, z before the chunk
+                dpart += dot_half(ot, i, hf, ac);  // dO_i . a, a before the chunk
+                xg[hf * kC + i] = gpart;
                 float2 zn = make_float2(0.f, 0.f);
                 if (CAUSAL) {  // column sums of K (which 0) and V (which 1) over this thread's row half
                     const float2 v = colsum_half(which == 0 ? kt : vt, cp, rh, nullptr);
@@ -341,43 +331,39 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
                     zn = make_float2(base[2 * cp] + c0[2 * cp] + c1[2 * cp], base[2 * cp + 1] + c0[2 * cp + 1] + c1[2 * cp + 1]);
                 }
-                // O_i over this half's columns, delta partial, and dO -> dOt in place
-                ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x30C);
+                // q_i . Y_i over this half's d (Y = dO Sb^T)
+                ok = wait_or_abort(barY, ph, abort_flag, P.status, 0x30C);
                 if (!ok) break;
                 tc_fence_after();
-                float dpart = 0.f;
+                uint32_t y0[32], y1[32];
+                tmem_ld32(R0 + lo + 64 * hf, y0);
+                tmem_ld32(R0 + lo + 64 * hf + 32, y1);
+                tmem_wait_ld(y0);
+                tmem_wait_ld(y1);
                 {
-                    unsigned char *tile = ot + hf * kBox;
-#pragma unroll 1
-                    for (int half32 = 0; half32 < 2; ++half32) {
-                        uint32_t v[32];
-                        tmem_ld32(R1 + lo + 64 * hf + 32 * half32, v);
-                        tmem_wait_ld(v);
-                        const float *aa = ac + 64 * hf + 32 * half32;
+                    const unsigned char *tile = qt + hf * kBox;
+                    float acc = 0.f;
 #pragma unroll
-                        for (int g4 = 0; g4 < 4; ++g4) {
-                            uint4 *p4 = (uint4 *)(tile + sw128_off(i, 4 * half32 + g4));
-                            uint4 w = *p4;
-                            uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int m = 8 * g4 + 2 * q;
-                                const float o0 = (__uint_as_float(v[m]) + aa[m]) * ig;
-                                const float o1 = (__uint_as_float(v[m + 1]) + aa[m + 1]) * ig;
-                                const float d0 = bf16lo(wv[q]), d1 = bf16hi(wv[q]);
-                                dpart = fmaf(d0, o0, fmaf(d1, o1, dpart));
-                                wv[q] = pack_bf16(d0 * ig, d1 * ig);
-                            }
-                            *p4 = w;
-                        }
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        const uint4 v = *(const uint4 *)(tile + sw128_off(i, g8));
+                        const uint32_t *yy = g8 < 4 ? y0 + 8 * g8 : y1 + 8 * (g8 - 4);
+                        acc = fmaf(bf16lo(v.x), __uint_as_float(yy[0]), acc);
+                        acc = fmaf(bf16hi(v.x), __uint_as_float(yy[1]), acc);
+                        acc = fmaf(bf16lo(v.y), __uint_as_float(yy[2]), acc);
+                        acc = fmaf(bf16hi(v.y), __uint_as_float(yy[3]), acc);
+                        acc = fmaf(bf16lo(v.z), __uint_as_float(yy[4]), acc);
+                        acc = fmaf(bf16hi(v.z), __uint_as_float(yy[5]), acc);
+                        acc = fmaf(bf16lo(v.w), __uint_as_float(yy[6]), acc);
+                        acc = fmaf(bf16hi(v.w), __uint_as_float(yy[7]), acc);
                     }
+                    dpart += acc;
                 }
                 xd[hf * kC + i] = dpart;
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(barDt);
                 epi_sync256();
-                const float dt = (xd[i] + xd[kC + i]) * ig;
+                tc_fence_after();
+                const float delta = (xd[i] + xd[kC + i]) * ig;
+                const float dt = delta * ig;
                 if (hf == 0) {
                     sDt[i] = dt;
                     if (i < nvalid) {
@@ -385,39 +371,73 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                         P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
                     }
                 }
-                if (CAUSAL) {  // U = [j <= i](W - dt), bf16, in place of W
-                    ok = wait_or_abort(barW, ph, abort_flag, P.status, 0x30D);
-                    if (!ok) break;
-                    tc_fence_after();
+                if (CAUSAL) {  // U' = [j <= i](W' - delta), bf16, in place of W'
                     uint32_t pk[32];
-                    tmem_half_to_bf16(R0 + lo, hf, [&](int j, float w) { return j <= i ? w - dt : 0.f; }, pk);
+                    tmem_half_to_bf16(R1 + lo, hf, [&](int j, float w) { return j <= i ? w - delta : 0.f; }, pk);
                     tc_fence_before();
-                    epi_sync256();
+                    epi_sync256();  // both halves have read W' before U' overwrites it
                     tc_fence_after();
-                    tmem_st32(R0 + lo + 32 * hf, pk);
+                    tmem_st32(R1 + lo + 32 * hf, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barU);
-                } else {
-                    epi_sync256();  // sDt is complete
                 }
-                {  // y += sum_i dt_i q_i (which 0), e += sum_i dOt_i (which 1), over this thread's row half
+                {  // dO -> dO / g in place (W' and Y, its unscaled readers, are done)
+                    unsigned char *tile = ot + hf * kBox;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        uint4 *p4 = (uint4 *)(tile + sw128_off(i, g8));
+                        uint4 w = *p4;
+                        uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * ig, bf16hi(wv[q]) * ig);
+                        *p4 = w;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(barDt);
+                epi_sync256();  // every row of dO / g and every dt_i is in shared memory
+                {  // y += sum_i dt_i q_i (which 0), e += sum_i dO_i / g_i (which 1), over this thread's row half
                     const float2 v = colsum_half(which == 0 ? qt : ot, cp, rh, which == 0 ? sDt : nullptr);
                     ye.x += v.x;
                     ye.y += v.y;
                 }
-                // dQ_i = X_i - dt_i z: staged in the Q tile, whose readers (MMAs, q . z, the y sums) are done
+                // dQ_i = X_i / g_i - dt_i z (X = Y + U' K; non-causal X = Y), staged in a tile whose readers
+                // are done (causal: V; non-causal: Q, once Ppiece is complete)
                 ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);
                 if (!ok) break;
                 tc_fence_after();
-                epi_sync256();
-                tmem_half_to_out(R1 + lo, hf, zc, -dt, qt, i);
+                unsigned char *dqt = CAUSAL ? vt : qt;
+                if (!CAUSAL) epi_sync256();  // every read of the Q tile (y sums) is done
+                {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(R0 + lo + 64 * hf, v0);
+                    tmem_ld32(R0 + lo + 64 * hf + 32, v1);
+                    tmem_wait_ld(v0);
+                    tmem_wait_ld(v1);
+                    unsigned char *tile = dqt + hf * kBox;
+                    const float *zz = zc + 64 * hf;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        const uint32_t *xx = g8 < 4 ? v0 + 8 * g8 : v1 + 8 * (g8 - 4);
+                        uint4 w;
+                        uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int m = 8 * g8 + 2 * q;
+                            wv[q] = pack_bf16(__uint_as_float(xx[2 * q]) * ig - dt * zz[m],
+                                              __uint_as_float(xx[2 * q + 1]) * ig - dt * zz[m + 1]);
+                        }
+                        *(uint4 *)(tile + sw128_off(i, g8)) = w;
+                    }
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (!CAUSAL) mbar_arrive(barXf);
                 epi_sync256();
                 if (u == 0) {
-                    store_tile(&P.tmdQ, qt, (int)row0, (int)pc.h);
+                    store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
                     bulk_wait_read0();
                     mbar_arrive(&empty[s]);
                 }

@@ -10,9 +10,9 @@
 // e_c = sum dOt_i run over the later rows.  Non-causal: every sum runs over the whole head.
 //
 // Launches: the per-piece K^T V sums and their scan (shared with the forward), the dQ walk in chunk
-// order (it recomputes O_i, hence g_i and delta_i; the stored O is not read; it also writes each piece's
-// reverse sums P, y, e and the per-row g_i, dt_i), the scan of the reverse sums, and the dK / dV walk in
-// reverse chunk order.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
+// order (it forms g_i and delta_i from the chunk's own products and the carried state, so the stored O
+// is not read; it also writes each piece's reverse sums P, y, e and, causal, the per-row g_i, dt_i), the
+// scan of the reverse sums, and the dK / dV walk in reverse chunk order.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
 // per TMEM lane quarter, each owning 64 of the 128 columns).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -30,8 +30,8 @@ namespace tc {
 using namespace sm100;
 
 // Reads this half's 64 columns (lane = the thread's row) of a 128-column fp32 TMEM block and maps them
-// through f(column, value) to 32 packed bf16 pairs.  The caller writes them back (tmem_st32 at column
-// 32 hf) after a barrier, because the two halves' reads and writes overlap.
+// through f(column, value) to 32 packed bf16 pairs.  Callers write them back into TMEM columns this
+// thread has itself read, so that no other thread's pending reads are overwritten.
 template <typename F>
 __device__ __forceinline__ void tmem_half_to_bf16(uint32_t taddr, int hf, F f, uint32_t (&pk)[32]) {
     uint32_t t0[32], t1[32];
@@ -92,6 +92,160 @@ __device__ __forceinline__ void tmem_half_to_out(uint32_t taddr, int hf, const f
     }
 }
 
+// q_row . y over box hf of a bf16 tile, with y the 64 fp32 values (bit patterns) of this half.
+__device__ __forceinline__ float dot_half_regs(const unsigned char *tile2, int row, int hf, const uint32_t (&y0)[32],
+                                               const uint32_t (&y1)[32]) {
+    const unsigned char *tile = tile2 + hf * kBox;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        const uint4 v = *(const uint4 *)(tile + sw128_off(row, g8));
+        const uint32_t *yy = g8 < 4 ? y0 + 8 * g8 : y1 + 8 * (g8 - 4);
+        acc0 = fmaf(bf16lo(v.x), __uint_as_float(yy[0]), acc0);
+        acc1 = fmaf(bf16hi(v.x), __uint_as_float(yy[1]), acc1);
+        acc0 = fmaf(bf16lo(v.y), __uint_as_float(yy[2]), acc0);
+        acc1 = fmaf(bf16hi(v.y), __uint_as_float(yy[3]), acc1);
+        acc0 = fmaf(bf16lo(v.z), __uint_as_float(yy[4]), acc0);
+        acc1 = fmaf(bf16hi(v.z), __uint_as_float(yy[5]), acc1);
+        acc0 = fmaf(bf16lo(v.w), __uint_as_float(yy[6]), acc0);
+        acc1 = fmaf(bf16hi(v.w), __uint_as_float(yy[7]), acc1);
+    }
+    return acc0 + acc1;
+}
+
+// Row `row` of dQ over columns [64 hf, 64 hf + 64): x * ig - dt * z, rounded to bf16 into box hf of the
+// staging tile (x: the 64 fp32 values of this half, as bit patterns).
+__device__ __forceinline__ void regs_half_to_dq(const uint32_t (&x0)[32], const uint32_t (&x1)[32], int hf, float ig,
+                                                float dt, const float *z, unsigned char *tile2, int row) {
+    unsigned char *tile = tile2 + hf * kBox;
+    const float *zz = z + 64 * hf;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        const uint32_t *xx = g8 < 4 ? x0 + 8 * g8 : x1 + 8 * (g8 - 4);
+        uint4 w;
+        uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int m = 8 * g8 + 2 * q;
+            wv[q] = pack_bf16(__uint_as_float(xx[2 * q]) * ig - dt * zz[m],
+                              __uint_as_float(xx[2 * q + 1]) * ig - dt * zz[m + 1]);
+        }
+        *(uint4 *)(tile + sw128_off(row, g8)) = w;
+    }
+}
+
+// The same from this half's 64 columns of an fp32 TMEM block (lane = row).
+__device__ __forceinline__ void tmem_half_to_dq(uint32_t taddr, int hf, float ig, float dt, const float *z,
+                                                unsigned char *tile2, int row) {
+    uint32_t x0[32], x1[32];
+    tmem_ld32(taddr + 64 * hf, x0);
+    tmem_ld32(taddr + 64 * hf + 32, x1);
+    tmem_wait_ld(x0);
+    tmem_wait_ld(x1);
+    regs_half_to_dq(x0, x1, hf, ig, dt, z, tile2, row);
+}
+
+// Multiplies row `row` of box hf of a bf16 tile by s in place.
+__device__ __forceinline__ void scale_row_half(unsigned char *tile2, int row, int hf, float s) {
+    unsigned char *tile = tile2 + hf * kBox;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        uint4 *p4 = (uint4 *)(tile + sw128_off(row, g8));
+        uint4 w = *p4;
+        uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * s, bf16hi(wv[q]) * s);
+        *p4 = w;
+    }
+}
+
+// End of a dQ-walk piece: its reverse sums into its workspace slot.  Ppiece = sum_i q_i (dO_i / g_i)^T
+// from TMEM (row i, this half's 64 columns); half 1 also writes component i of y and of e.
+__device__ __forceinline__ void piece_rev_sums(const TcParams &P, const Piece &pc, uint32_t taddr, int i, int hf,
+                                               float y, float e) {
+    constexpr int D = 128;
+    float *slot = P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride;
+#pragma unroll 1
+    for (int half32 = 0; half32 < 2; ++half32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + 64 * hf + 32 * half32, v);
+        tmem_wait_ld(v);
+        float4 *dst = (float4 *)(slot + (size_t)i * D + 64 * hf + 32 * half32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+    }
+    if (hf == 1) {
+        slot[(size_t)D * D + i] = y;
+        slot[(size_t)D * D + D + i] = e;
+    }
+}
+
+// q_row . z and q_row . y over box hf of a bf16 tile in one pass over the row: z fp32 (shared memory), y the
+// 64 fp32 values of this half (bit patterns).
+__device__ __forceinline__ float2 dot2_half(const unsigned char *tile2, int row, int hf, const float *z,
+                                            const uint32_t (&y0)[32], const uint32_t (&y1)[32]) {
+    const unsigned char *tile = tile2 + hf * kBox;
+    const float *zz0 = z + 64 * hf;
+    float az = 0.f, bz = 0.f, ay = 0.f, by = 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        const uint4 v = *(const uint4 *)(tile + sw128_off(row, g8));
+        const float *zz = zz0 + 8 * g8;
+        const uint32_t *yy = g8 < 4 ? y0 + 8 * g8 : y1 + 8 * (g8 - 4);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = bf16lo(w[q]), hi = bf16hi(w[q]);
+            az = fmaf(lo, zz[2 * q], az);
+            bz = fmaf(hi, zz[2 * q + 1], bz);
+            ay = fmaf(lo, __uint_as_float(yy[2 * q]), ay);
+            by = fmaf(hi, __uint_as_float(yy[2 * q + 1]), by);
+        }
+    }
+    return make_float2(az + bz, ay + by);
+}
+
+// dt_i (row i of the chunk) into an N = 16 MMA operand: two 8-row boxes of 128-byte rows in the 128-byte
+// swizzle (rows i < 64 in the first box), row 0 = bf16(dt_i), row 1 = bf16(dt_i - row 0), rows 2-7 zero.
+// An MMA of Q^T against it puts sum_i dt_i q_i, in two parts, into output columns 0 and 1.
+__device__ __forceinline__ void dt_tile_put(unsigned char *dtt, int i, float dt) {
+    unsigned char *bx = dtt + (i >> 6) * 1024;
+    const int e = i & 63;
+    const __nv_bfloat16 h = __float2bfloat16_rn(dt);
+    const __nv_bfloat16 l = __float2bfloat16_rn(dt - __bfloat162float(h));
+    *(__nv_bfloat16 *)(bx + ((e >> 3) << 4) + (e & 7) * 2) = h;              // row 0: 16-byte group e / 8
+    *(__nv_bfloat16 *)(bx + 128 + (((e >> 3) ^ 1) << 4) + (e & 7) * 2) = l;  // row 1: group index XOR 1
+}
+
+// The chunk walked after chunk c of piece pc when each piece is walked in reverse: c - 1 in the piece,
+// else the last chunk of the slice's next piece.  False when c is the slice's last.
+__device__ __forceinline__ bool next_rev_chunk(const PieceIter &pi, const Piece &pc, int c, long long *h, int *cn) {
+    if (c > pc.a) {
+        *h = pc.h;
+        *cn = c - 1;
+        return true;
+    }
+    PieceIter pn = pi;
+    pn.next();
+    if (!pn.valid()) return false;
+    const Piece q = pn.get();
+    *h = q.h;
+    *cn = q.e - 1;
+    return true;
+}
+
+// g and dt of row j of chunk c of head h, from the dQ walk's row statistics (0 past the end of the head).
+// Loads only: the values are used one chunk later.
+__device__ __forceinline__ void load_row_stats(const TcParams &P, long long h, int c, int j, float *g, float *dt) {
+    const long long r = (long long)c * kC + j;
+    const bool in = r < P.N;
+    const size_t x = (size_t)h * P.N + (in ? r : 0);
+    *g = in ? P.rs_g[x] : 0.f;
+    *dt = in ? P.rs_dt[x] : 0.f;
+}
+
 // Issues the TMA stores of a two-box output tile from shared memory and commits them.  One thread.
 __device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, int h) {
     tma_store_3d(map, tile2, 0, row0, h);
@@ -100,55 +254,57 @@ __device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigne
 }
 
 // ----------------------------------------------------------------------------------------------------
-// dQ walk (chunk order).  The forward output is not recomputed: with W' = dO V^T and Y = dO Sb^T (Sb =
-// bf16 state before the chunk),
+// dQ walk (chunk order), causal.  The forward output is not recomputed: with W' = dO V^T and Y = dO Sb^T
+// (Sb = bf16 state before the chunk),
 //   delta_i g_i = dO_i . a + sum_j P_ij W'_ij + q_i . Y_i,      P_ij = [j <= i](1 + q_i . k_j)
 //   dQ_i = (Y_i + [U' K]_i) / g_i - dt_i z,                     U'_ij = [j <= i](W'_ij - delta_i)
-// Per chunk, causal: T = Q K^T and W' (R0, R1); S += K^T V (R2); the epilogue forms P, r_i and
-// sum_j P_ij W'_ij from T and W' in registers; Y into R0; the epilogue forms g_i, delta_i, dt_i and U'
-// (bf16, in place of W'); X = Y + U' K in R0; dO -> dO / g in place; Ppiece += Q^T (dO / g) (R3).
-// Non-causal: only Y (R0, the head's totals) and Ppiece; stages hold only Q and dO.
-// Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128; for the
-// column sums it owns column pair cp = u % 64 of tensor u / 128 over row half (u / 64) % 2.
+// Per chunk: T = Q K^T and W' (R0, R1); the epilogue forms P, r_i and sum_j P_ij W'_ij from T and W' in
+// registers; Y into R0; S += K^T V (R2); the epilogue forms g_i, delta_i, dt_i and U' (bf16, in place of
+// W'); X = Y + U' K in R0; dO -> dO / g in place; Ppiece += Q^T (dO / g) (R3).  The column sums the
+// state and the reverse sums need (z += sum k_j, a += sum v_j, y += sum dt_i q_i, e += sum dO_i / g_i)
+// are N = 16 MMAs against a tile of ones or of dt_i, into the columns of R1 that U' leaves free; the
+// epilogue drains them with the dQ row.  One TMA stage (Q, dO, K, V); the next chunk's tiles are
+// prefetched into L2 meanwhile, and dQ leaves through its own staging tile.
+// Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128.
 // ----------------------------------------------------------------------------------------------------
-template <bool CAUSAL>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
-    constexpr int NST = CAUSAL ? 1 : 2;
     constexpr uint32_t TB = NB * kBox;
-    constexpr uint32_t STAGE = CAUSAL ? 4 * TB : 2 * TB;  // Q, dO (, K, V)
+    constexpr uint32_t STAGE = 4 * TB;  // Q, dO, K, V
+    constexpr uint32_t E = kEpiThreads;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     bool aligned;
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
-    unsigned char *stages = sm;
-    unsigned char *Sb = sm + NST * STAGE;
-    float *zc = (float *)(Sb + TB);  // z before the chunk (fp32, D)
-    float *ac = zc + D;              // a before the chunk
-    float *sDt = ac + D;             // dt_i of the chunk's rows
-    float *xg = sDt + kC;            // [2][128] row partials of g (per column half)
-    float *xd = xg + 2 * kC;         // [2][128] row partials of delta g
-    float *cs = xd + 2 * kC;         // [2 tensors][2 row halves][128 columns] column-sum partials
-    uint64_t *full = (uint64_t *)(cs + 4 * D);
-    uint64_t *empty = full + NST;
-    uint64_t *bar = empty + NST;
-    uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barDt = bar + 4, *barU = bar + 5,
-             *barX = bar + 6, *barS = bar + 7, *barPP = bar + 8, *barPPf = bar + 9, *barXf = bar + 10;
-    uint32_t *tslot = (uint32_t *)(bar + 11);
+    unsigned char *stage = sm;
+    unsigned char *Sb = sm + STAGE;
+    unsigned char *dqt = Sb + TB;        // dQ staging tile
+    unsigned char *ones = dqt + TB;      // 8 rows x 128 B of bf16 1.0 (N = 16 operand, rows repeated)
+    unsigned char *dtt = ones + 1024;    // dt_i of the chunk's rows, as an N = 16 operand (dt_tile_put)
+    float *zc = (float *)(dtt + 2048);   // z before the chunk (fp32, D)
+    float *ac = zc + D;                  // a before the chunk
+    float *xg = ac + D;                  // [2][128] row partials of g (per column half)
+    float *xd = xg + 2 * kC;             // [2][128] row partials of delta g
+    uint64_t *full = (uint64_t *)(xd + 2 * kC);
+    uint64_t *empty = full + 1;
+    uint64_t *bar = empty + 1;
+    uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barU = bar + 4, *barDt = bar + 5,
+             *barX = bar + 6, *barR = bar + 7, *barPPf = bar + 8;
+    uint32_t *tslot = (uint32_t *)(bar + 9);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dQ tile has left shared memory
-        }
-        const uint32_t E = kEpiThreads;
-        const uint32_t counts[11] = {1, E, E, 1, E, E, 1, 1, 1, E, E};
-        for (int k = 0; k < 11; ++k) mbar_init(&bar[k], counts[k]);
+        mbar_init(full, 1);
+        mbar_init(empty, 1);  // the chunk's last MMA commit: every epilogue read of the stage precedes barDt
+        const uint32_t counts[9] = {1, E, E, 1, E, E, 1, E, E};
+        for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
+    for (int k = threadIdx.x; k < 512; k += blockDim.x) ((uint32_t *)dtt)[k] = 0u;
+    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -158,107 +314,112 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
+    // column sums of the chunk (N = 16 each; column 0 of each holds the sum, column 1 of cY the dt remainder),
+    // in the R1 columns that U' (R1 + [0, 32) and R1 + [64, 96)) leaves free
+    const uint32_t cZ = R1 + 32, cA = R1 + 48, cY = R1 + 96, cE = R1 + 112;
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
-        if (CAUSAL) {
-            prefetch_tmap(&P.tmK);
-            prefetch_tmap(&P.tmV);
-        }
+        prefetch_tmap(&P.tmK);
+        prefetch_tmap(&P.tmV);
+        const long long hi = slice_lo(P.sl, blockIdx.x + 1);
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                const int s = it % NST;
-                if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x301)) {
+                if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x301)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], STAGE);
-                unsigned char *st = stages + s * STAGE;
+                mbar_arrive_expect_tx(full, STAGE);
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, (int)pc.h);
-                    if (CAUSAL) {
-                        tma_load_3d(st + 2 * TB + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
-                        tma_load_3d(st + 3 * TB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, (int)pc.h);
+                }
+                const long long nx = pc.h * P.sl.nchunk + c + 1;  // the slice's next chunk, into L2
+                if (nx < hi) {
+                    const int nh = (int)(nx / P.sl.nchunk), nrow = (int)(nx % P.sl.nchunk) * kC;
+                    for (int nb = 0; nb < NB; ++nb) {
+                        tma_prefetch_3d(&P.tmQ, nb * 64, nrow, nh);
+                        tma_prefetch_3d(&P.tmdO, nb * 64, nrow, nh);
+                        tma_prefetch_3d(&P.tmK, nb * 64, nrow, nh);
+                        tma_prefetch_3d(&P.tmV, nb * 64, nrow, nh);
                     }
                 }
             }
         }
-        if (!ok) {
-            for (int k = it > NST ? it - NST : 0; k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1, 50000000ull);
-        }
+        if (!ok && it > 0) mbar_wait(full, (it - 1) & 1, 50000000ull);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
         const uint32_t idMM = idesc_bf16(128, 128, true, true);
-        const uint32_t sb = smem_u32(Sb);
+        const uint32_t idZ = idesc_bf16(128, 16, true, false);
+        const uint32_t sb = smem_u32(Sb), on = smem_u32(ones), dtb = smem_u32(dtt);
+        const uint32_t qb = smem_u32(stage), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
         int it = 0, pno = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            if (!CAUSAL && !wait_or_abort(barSb, pno & 1, abort_flag, P.status, 0x302)) break;
-            if (pno > 0 && !wait_or_abort(barPPf, (pno - 1) & 1, abort_flag, P.status, 0x303)) break;
             for (int c = pc.a; c < pc.e && ok; ++c, ++it) {
-                const int s = it % NST;
                 const uint32_t ph = it & 1;
-                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x304);
+                ok = wait_or_abort(full, ph, abort_flag, P.status, 0x304);
+                if (ok && it > 0) ok = wait_or_abort(barR, ph ^ 1, abort_flag, P.status, 0x307);  // R0, R1 drained
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t qb = smem_u32(stages + s * STAGE), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
-                if (CAUSAL) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {  // T = Q K^T ; W' = dO V^T
-                        const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
-                        mma_ss(R0, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idKK, k > 0);
-                        mma_ss(R1, sdesc_sw128(ob + o, 16, 1024), sdesc_sw128(vb + o, 16, 1024), idKK, k > 0);
-                    }
-                    mma_commit(barT);
-                    ok = wait_or_abort(barTr, ph, abort_flag, P.status, 0x305);  // T has been read out of R0
-                    if (!ok) break;
-                    ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x306);
-                    if (!ok) break;
-                    tc_fence_after();
-                } else if (it > 0) {
-                    ok = wait_or_abort(barXf, (it - 1) & 1, abort_flag, P.status, 0x307);
-                    if (!ok) break;
-                    tc_fence_after();
+                for (int k = 0; k < 8; ++k) {  // T = Q K^T ; W' = dO V^T
+                    const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
+                    mma_ss(R0, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idKK, k > 0);
+                    mma_ss(R1, sdesc_sw128(ob + o, 16, 1024), sdesc_sw128(vb + o, 16, 1024), idKK, k > 0);
                 }
+                mma_commit(barT);
+                ok = wait_or_abort(barTr, ph, abort_flag, P.status, 0x305);  // T has been read out of R0
+                if (!ok) break;
+                ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x306);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k)  // Y = dO Sb^T
                     mma_ss(R0, sdesc_sw128(ob + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                            sdesc_sw128(sb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
                 mma_commit(barY);
-                if (CAUSAL) {
-                    if (c + 1 < pc.e) {  // S += K^T V, once the epilogue has copied S into Sb (barSb above)
+                if (c + 1 < pc.e) {  // S += K^T V, once the epilogue has copied S into Sb (barSb above)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            mma_ss(R2, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
-                                   idMM, 1u);
-                    }
-                    ok = wait_or_abort(barU, ph, abort_flag, P.status, 0x308);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)  // X = Y + U' K
-                        mma_ts(R0, R1 + 8 * k, sdesc_sw128(kb + 2048 * k, kBox, 1024), idKM, 1u);
+                    for (int k = 0; k < 8; ++k)
+                        mma_ss(R2, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
+                               idMM, 1u);
                 }
-                ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x309);  // dO / g is in place of dO
+                ok = wait_or_abort(barU, ph, abort_flag, P.status, 0x308);  // U' written, W' no longer needed
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k)  // Ppiece += Q^T (dO / g)
-                    mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024), idMM,
-                           (c > pc.a || k > 0) ? 1u : 0u);
+                for (int k = 0; k < 8; ++k) {  // X = Y + U' K ; z_c = K^T 1 ; a_c = V^T 1
+                    const uint64_t o1 = sdesc_sw128(on + 32 * (k & 3), 16, 0);
+                    mma_ts(R0, R1 + 64 * (k >> 2) + 8 * (k & 3), sdesc_sw128(kb + 2048 * k, kBox, 1024), idKM, 1u);
+                    mma_ss(cZ, sdesc_sw128(kb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
+                    mma_ss(cA, sdesc_sw128(vb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
+                }
+                ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x309);  // dO / g in place, dt_i in dtt
+                if (!ok) break;
+                if (c == pc.a && pno > 0) ok = wait_or_abort(barPPf, (pno - 1) & 1, abort_flag, P.status, 0x303);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // Ppiece += Q^T (dO / g) ; y_c = Q^T dt ; e_c = (dO / g)^T 1
+                    const uint64_t qa = sdesc_sw128(qb + 2048 * k, kBox, 1024);
+                    const uint64_t oa = sdesc_sw128(ob + 2048 * k, kBox, 1024);
+                    mma_ss(R3, qa, oa, idMM, (c > pc.a || k > 0) ? 1u : 0u);
+                    mma_ss(cY, qa, sdesc_sw128(dtb + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idZ, k > 0);
+                    mma_ss(cE, oa, sdesc_sw128(on + 32 * (k & 3), 16, 0), idZ, k > 0);
+                }
                 mma_commit(barX);
-                mma_commit(barS);
-                mma_commit(&empty[s]);
-                if (c + 1 == pc.e) mma_commit(barPP);
+                mma_commit(empty);
             }
         }
     } else if (warp >= 2) {
@@ -266,33 +427,27 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         const int u = threadIdx.x - 64;
         const int q4 = warp & 3, hf = (warp - 2) >> 2;
         const int i = 32 * q4 + lane;
-        const int which = u >> 7, cp = u & 63, rh = (u >> 6) & 1;  // column-sum role
         const uint32_t lo = (uint32_t)(32 * q4) << 16;
-        int it = 0, pno = 0;
+        unsigned char *qt = stage, *ot = stage + TB;
+        int it = 0;
         bool ok = true;
-        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried forward state of the piece, combined into its own slot by tc_scan_slots
-            if (CAUSAL && it > 0) {
-                if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x30A)) break;
-                tc_fence_after();
-            }
+            // carried forward state of the piece, combined into its own slot by tc_scan_slots (the previous
+            // piece's MMAs on R2 are complete: its last barX has been waited for)
             load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, R2 + lo, 0u, 0u, Sb, zc,
-                            ac, CAUSAL, /*vec_to_tmem=*/false);
+                            ac, true, /*vec_to_tmem=*/false);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
             mbar_arrive(barSb);
-            float2 ye = make_float2(0.f, 0.f);  // this thread's part of y (which 0) or e (which 1)
+            float yacc = 0.f, eacc = 0.f;  // half 1: y_i and e_i of the piece (row i = component d)
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                const int s = it % NST;
                 const uint32_t ph = it & 1;
-                unsigned char *st = stages + s * STAGE;
-                unsigned char *qt = st, *ot = st + TB, *kt = st + 2 * TB, *vt = st + 3 * TB;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
                 float gpart = 0.f, dpart = 0.f;  // partial g_i and partial delta_i g_i over this half
-                if (CAUSAL) {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
+                {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
                     if (!ok) break;
                     tc_fence_after();
@@ -314,180 +469,81 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     tc_fence_before();
                     mbar_arrive(barTr);
                 }
-                gpart += dot_half(qt, i, hf, zc);  // q_i . z, z before the chunk
                 dpart += dot_half(ot, i, hf, ac);  // dO_i . a, a before the chunk
-                xg[hf * kC + i] = gpart;
-                float2 zn = make_float2(0.f, 0.f);
-                if (CAUSAL) {  // column sums of K (which 0) and V (which 1) over this thread's row half
-                    const float2 v = colsum_half(which == 0 ? kt : vt, cp, rh, nullptr);
-                    cs[(which * 2 + rh) * D + 2 * cp] = v.x;
-                    cs[(which * 2 + rh) * D + 2 * cp + 1] = v.y;
-                }
-                epi_sync256();
-                const float gi = (CAUSAL ? (float)row0 : (float)P.N) + xg[i] + xg[kC + i];
-                const float ig = 1.f / gi;
-                if (CAUSAL && rh == 0) {
-                    const float *base = which == 0 ? zc : ac;
-                    const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
-                    zn = make_float2(base[2 * cp] + c0[2 * cp] + c1[2 * cp], base[2 * cp + 1] + c0[2 * cp + 1] + c1[2 * cp + 1]);
-                }
-                // q_i . Y_i over this half's d (Y = dO Sb^T)
+                // q_i . z and q_i . Y_i over this half's d (Y = dO Sb^T), one pass over the Q row
                 ok = wait_or_abort(barY, ph, abort_flag, P.status, 0x30C);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t y0[32], y1[32];
-                tmem_ld32(R0 + lo + 64 * hf, y0);
-                tmem_ld32(R0 + lo + 64 * hf + 32, y1);
-                tmem_wait_ld(y0);
-                tmem_wait_ld(y1);
                 {
-                    const unsigned char *tile = qt + hf * kBox;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        const uint4 v = *(const uint4 *)(tile + sw128_off(i, g8));
-                        const uint32_t *yy = g8 < 4 ? y0 + 8 * g8 : y1 + 8 * (g8 - 4);
-                        acc = fmaf(bf16lo(v.x), __uint_as_float(yy[0]), acc);
-                        acc = fmaf(bf16hi(v.x), __uint_as_float(yy[1]), acc);
-                        acc = fmaf(bf16lo(v.y), __uint_as_float(yy[2]), acc);
-                        acc = fmaf(bf16hi(v.y), __uint_as_float(yy[3]), acc);
-                        acc = fmaf(bf16lo(v.z), __uint_as_float(yy[4]), acc);
-                        acc = fmaf(bf16hi(v.z), __uint_as_float(yy[5]), acc);
-                        acc = fmaf(bf16lo(v.w), __uint_as_float(yy[6]), acc);
-                        acc = fmaf(bf16hi(v.w), __uint_as_float(yy[7]), acc);
-                    }
-                    dpart += acc;
+                    uint32_t y0[32], y1[32];
+                    tmem_ld32(R0 + lo + 64 * hf, y0);
+                    tmem_ld32(R0 + lo + 64 * hf + 32, y1);
+                    tmem_wait_ld(y0);
+                    tmem_wait_ld(y1);
+                    const float2 qq = dot2_half(qt, i, hf, zc, y0, y1);
+                    gpart += qq.x;
+                    dpart += qq.y;
                 }
+                xg[hf * kC + i] = gpart;
                 xd[hf * kC + i] = dpart;
+                if (u == 0) bulk_wait_read0();  // the previous chunk's dQ has left the staging tile
                 tc_fence_before();
                 epi_sync256();
                 tc_fence_after();
+                const float gi = (float)row0 + xg[i] + xg[kC + i];
+                const float ig = 1.f / gi;
                 const float delta = (xd[i] + xd[kC + i]) * ig;
                 const float dt = delta * ig;
-                if (hf == 0) {
-                    sDt[i] = dt;
-                    if (i < nvalid) {
-                        P.rs_g[(size_t)pc.h * P.N + row0 + i] = gi;
-                        P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
-                    }
+                if (hf == 0 && i < nvalid) {
+                    P.rs_g[(size_t)pc.h * P.N + row0 + i] = gi;
+                    P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
                 }
-                if (CAUSAL) {  // U' = [j <= i](W' - delta), bf16, in place of W'
+                {  // U' = [j <= i](W' - delta), bf16, over the R1 columns this half has read: R1 + 64 hf + [0, 32)
                     uint32_t pk[32];
                     tmem_half_to_bf16(R1 + lo, hf, [&](int j, float w) { return j <= i ? w - delta : 0.f; }, pk);
-                    tc_fence_before();
-                    epi_sync256();  // both halves have read W' before U' overwrites it
-                    tc_fence_after();
-                    tmem_st32(R1 + lo + 32 * hf, pk);
+                    tmem_st32(R1 + lo + 64 * hf, pk);
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barU);
                 }
-                {  // dO -> dO / g in place (W' and Y, its unscaled readers, are done)
-                    unsigned char *tile = ot + hf * kBox;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        uint4 *p4 = (uint4 *)(tile + sw128_off(i, g8));
-                        uint4 w = *p4;
-                        uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * ig, bf16hi(wv[q]) * ig);
-                        *p4 = w;
-                    }
-                }
+                scale_row_half(ot, i, hf, ig);  // dO -> dO / g in place (W' and Y, its unscaled readers, are done)
+                if (hf == 0) dt_tile_put(dtt, i, dt);
                 fence_proxy_async_smem();
-                tc_fence_before();
                 mbar_arrive(barDt);
-                epi_sync256();  // every row of dO / g and every dt_i is in shared memory
-                {  // y += sum_i dt_i q_i (which 0), e += sum_i dO_i / g_i (which 1), over this thread's row half
-                    const float2 v = colsum_half(which == 0 ? qt : ot, cp, rh, which == 0 ? sDt : nullptr);
-                    ye.x += v.x;
-                    ye.y += v.y;
-                }
-                // dQ_i = X_i / g_i - dt_i z (X = Y + U' K; non-causal X = Y), staged in a tile whose readers
-                // are done (causal: V; non-causal: Q, once Ppiece is complete)
+                // dQ_i = X_i / g_i - dt_i z (X = Y + U' K), and the chunk's column sums
                 ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);
                 if (!ok) break;
                 tc_fence_after();
-                unsigned char *dqt = CAUSAL ? vt : qt;
-                if (!CAUSAL) epi_sync256();  // every read of the Q tile (y sums) is done
-                {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(R0 + lo + 64 * hf, v0);
-                    tmem_ld32(R0 + lo + 64 * hf + 32, v1);
-                    tmem_wait_ld(v0);
-                    tmem_wait_ld(v1);
-                    unsigned char *tile = dqt + hf * kBox;
-                    const float *zz = zc + 64 * hf;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        const uint32_t *xx = g8 < 4 ? v0 + 8 * g8 : v1 + 8 * (g8 - 4);
-                        uint4 w;
-                        uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int m = 8 * g8 + 2 * q;
-                            wv[q] = pack_bf16(__uint_as_float(xx[2 * q]) * ig - dt * zz[m],
-                                              __uint_as_float(xx[2 * q + 1]) * ig - dt * zz[m + 1]);
-                        }
-                        *(uint4 *)(tile + sw128_off(i, g8)) = w;
-                    }
-                }
-                fence_proxy_async_smem();
+                tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
+                uint32_t s0, s1, s2, s3;
+                tmem_ld2(hf == 0 ? cZ + lo : cY + lo, s0, s1);  // half 0: z_c, -; half 1: y_c (two parts)
+                tmem_ld2(hf == 0 ? cA + lo : cE + lo, s2, s3);  // half 0: a_c, -; half 1: e_c, -
+                tmem_wait_ld(s0, s1);
+                tmem_wait_ld(s2, s3);
                 tc_fence_before();
-                if (!CAUSAL) mbar_arrive(barXf);
+                mbar_arrive(barR);
+                fence_proxy_async_smem();
+                epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
+                if (u == 0) store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
+                if (c + 1 < pc.e) {
+                    tmem_half_to_tile(R2 + lo, Sb, i, hf);
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(barSb);
+                }
+                if (hf == 0) {  // z and a after this chunk
+                    zc[i] += __uint_as_float(s0);
+                    ac[i] += __uint_as_float(s2);
+                } else {
+                    yacc += __uint_as_float(s0) + __uint_as_float(s1);
+                    eacc += __uint_as_float(s2);
+                }
                 epi_sync256();
-                if (u == 0) {
-                    store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
-                    bulk_wait_read0();
-                    mbar_arrive(&empty[s]);
-                }
-                if (CAUSAL) {
-                    ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x30F);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (c + 1 < pc.e) {
-                        tmem_half_to_tile(R2 + lo, Sb, i, hf);
-                        fence_proxy_async_smem();
-                        tc_fence_before();
-                        mbar_arrive(barSb);
-                    }
-                    // z (which 0) and a (which 1) after this chunk
-                    if (rh == 0) {
-                        float *base = which == 0 ? zc : ac;
-                        base[2 * cp] = zn.x;
-                        base[2 * cp + 1] = zn.y;
-                    }
-                    epi_sync256();
-                }
             }
             if (!ok) break;
-            // the piece's reverse sums -> workspace
-            if (!wait_or_abort(barPP, pno & 1, abort_flag, P.status, 0x310)) break;
-            tc_fence_after();
-            float *slot = P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride;
-#pragma unroll 1
-            for (int half32 = 0; half32 < 2; ++half32) {
-                uint32_t v[32];
-                tmem_ld32(R3 + lo + 64 * hf + 32 * half32, v);
-                tmem_wait_ld(v);
-                float4 *dst = (float4 *)(slot + (size_t)i * D + 64 * hf + 32 * half32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            }
-            // y, e: add the two row halves
-            cs[(which * 2 + rh) * D + 2 * cp] = ye.x;
-            cs[(which * 2 + rh) * D + 2 * cp + 1] = ye.y;
+            piece_rev_sums(P, pc, R3 + lo, i, hf, yacc, eacc);  // Ppiece is complete (last barX)
             tc_fence_before();
-            epi_sync256();
-            if (rh == 0) {
-                const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
-                slot[(size_t)D * D + which * D + 2 * cp] = c0[2 * cp] + c1[2 * cp];
-                slot[(size_t)D * D + which * D + 2 * cp + 1] = c0[2 * cp + 1] + c1[2 * cp + 1];
-            }
             mbar_arrive(barPPf);
-            epi_sync256();  // cs is reused by the next piece
         }
     }
     if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
@@ -498,25 +554,508 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     }
 }
 
-template __global__ void tc_bwd_dq_kernel<true>(const __grid_constant__ TcParams P);
-template __global__ void tc_bwd_dq_kernel<false>(const __grid_constant__ TcParams P);
+// ----------------------------------------------------------------------------------------------------
+// dQ walk, non-causal.  Every row sees the head's totals S, z, a (tc_scan_slots mode 2), so the chunks
+// of a piece are independent apart from the piece sums Ppiece = sum_i q_i (dO_i / g_i)^T, y and e:
+//   g_i = N + q_i . z,   delta_i g_i = dO_i . a + q_i . Y_i,   dQ_i = Y_i / g_i - dt_i z,   Y = dO Sb^T.
+// Two TMA stages of (Q, dO).  Y alternates between TMEM blocks R0 and R1, so that the MMA of the next
+// chunk runs while the epilogue works on this one; Ppiece (R3) and the column sums y, e (N = 16 MMAs
+// into R2) are issued one chunk behind, once the epilogue has rewritten dO as dO / g in place; dQ leaves
+// through its own staging tile.
+// ----------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const __grid_constant__ TcParams P) {
+    constexpr int D = 128, NB = D / 64, NST = 2;
+    constexpr uint32_t TB = NB * kBox;
+    constexpr uint32_t STAGE = 2 * TB;  // Q, dO
+    constexpr uint32_t E = kEpiThreads;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    bool aligned;
+    unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
+    unsigned char *stages = sm;
+    unsigned char *Sb = sm + NST * STAGE;
+    unsigned char *dqt = Sb + TB;      // dQ staging tile
+    unsigned char *ones = dqt + TB;    // 8 rows x 128 B of bf16 1.0
+    unsigned char *dtt = ones + 1024;  // [2 chunk parities] dt_i as an N = 16 operand (dt_tile_put)
+    float *zc = (float *)(dtt + 4096); // the head's z
+    float *ac = zc + D;                // the head's a
+    float *xg = ac + D;                // [2][128] row partials of g
+    float *xd = xg + 2 * kC;           // [2][128] row partials of delta g
+    uint64_t *full = (uint64_t *)(xd + 2 * kC);
+    uint64_t *empty = full + NST;
+    uint64_t *barY = empty + NST;  // [2]: Y of the chunk is in R0 / R1
+    uint64_t *barYf = barY + 2;    // [2]: the epilogue has read Y out of R0 / R1
+    uint64_t *barDt = barYf + 2, *barX = barDt + 1, *barSb = barDt + 2, *barPP = barDt + 3, *barPPf = barDt + 4;
+    uint32_t *tslot = (uint32_t *)(barDt + 5);
+    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    if (!aligned) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);  // the Ppiece MMA commit: every epilogue read of the stage precedes barDt
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&barY[b], 1);
+            mbar_init(&barYf[b], E);
+        }
+        mbar_init(barDt, E);
+        mbar_init(barX, 1);
+        mbar_init(barSb, E);
+        mbar_init(barPP, 1);
+        mbar_init(barPPf, E);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
+    for (int k = threadIdx.x; k < 1024; k += blockDim.x) ((uint32_t *)dtt)[k] = 0u;
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t R2 = tmem + 256, R3 = tmem + 384;
+    const uint32_t cY = R2, cE = R2 + 16;  // piece sums y (columns 0, 1: two parts) and e (column 0)
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer
+        prefetch_tmap(&P.tmQ);
+        prefetch_tmap(&P.tmdO);
+        int it = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+            const Piece pc = pi.get();
+            for (int c = pc.a; c < pc.e; ++c, ++it) {
+                const int s = it % NST;
+                if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x321)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], STAGE);
+                unsigned char *st = stages + s * STAGE;
+                for (int nb = 0; nb < NB; ++nb) {
+                    tma_load_3d(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, (int)pc.h);
+                }
+            }
+        }
+        if (!ok) {
+            for (int k = it > NST ? it - NST : 0; k < it; ++k) mbar_wait(&full[k % NST], (k / NST) & 1, 50000000ull);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t idKK = idesc_bf16(128, 128, false, false);
+        const uint32_t idMM = idesc_bf16(128, 128, true, true);
+        const uint32_t idZ = idesc_bf16(128, 16, true, false);
+        const uint32_t sb = smem_u32(Sb), on = smem_u32(ones), dtb = smem_u32(dtt);
+        // Ppiece += Q^T (dO / g), y += Q^T dt, e += (dO / g)^T 1 for flat chunk index itp
+        auto ppiece = [&](int itp, bool first) -> bool {
+            if (!wait_or_abort(barDt, itp & 1, abort_flag, P.status, 0x322)) return false;
+            tc_fence_after();
+            const uint32_t qb = smem_u32(stages + (itp % NST) * STAGE), ob = qb + TB;
+            const uint32_t db = dtb + (itp & 1) * 2048;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t acc = (!first || k > 0) ? 1u : 0u;
+                const uint64_t qa = sdesc_sw128(qb + 2048 * k, kBox, 1024);
+                const uint64_t oa = sdesc_sw128(ob + 2048 * k, kBox, 1024);
+                mma_ss(R3, qa, oa, idMM, acc);
+                mma_ss(cY, qa, sdesc_sw128(db + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idZ, acc);
+                mma_ss(cE, oa, sdesc_sw128(on + 32 * (k & 3), 16, 0), idZ, acc);
+            }
+            mma_commit(barX);
+            mma_commit(&empty[itp % NST]);
+            return true;
+        };
+        int it = 0, pno = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
+            const Piece pc = pi.get();
+            if (!wait_or_abort(barSb, pno & 1, abort_flag, P.status, 0x323)) break;
+            if (pno > 0 && !wait_or_abort(barPPf, (pno - 1) & 1, abort_flag, P.status, 0x324)) break;
+            for (int c = pc.a; c < pc.e && ok; ++c, ++it) {
+                const int s = it % NST, b = it & 1;
+                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x325);
+                if (ok && it >= 2) ok = wait_or_abort(&barYf[b], ((it >> 1) - 1) & 1, abort_flag, P.status, 0x326);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ob = smem_u32(stages + s * STAGE) + TB;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // Y = dO Sb^T
+                    mma_ss(tmem + 128 * b, sdesc_sw128(ob + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                           sdesc_sw128(sb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
+                mma_commit(&barY[b]);
+                if (c > pc.a) ok = ppiece(it - 1, c - 1 == pc.a);
+            }
+            if (!ok || !ppiece(it - 1, pc.e - 1 == pc.a)) break;
+            mma_commit(barPP);
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue
+        const int u = threadIdx.x - 64;
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int i = 32 * q4 + lane;
+        const uint32_t lo = (uint32_t)(32 * q4) << 16;
+        int it = 0, pno = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
+            const Piece pc = pi.get();
+            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, 0u, 0u, 0u, Sb, zc, ac,
+                            false, false);
+            fence_proxy_async_smem();
+            epi_sync256();
+            mbar_arrive(barSb);
+            for (int c = pc.a; c < pc.e; ++c, ++it) {
+                const int s = it % NST, b = it & 1;
+                unsigned char *qt = stages + s * STAGE, *ot = qt + TB;
+                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x327);
+                if (!ok) break;
+                const float dpart = dot_half(ot, i, hf, ac);  // dO_i . a
+                ok = wait_or_abort(&barY[b], (it >> 1) & 1, abort_flag, P.status, 0x328);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t y0[32], y1[32];
+                tmem_ld32(tmem + 128 * b + lo + 64 * hf, y0);
+                tmem_ld32(tmem + 128 * b + lo + 64 * hf + 32, y1);
+                tmem_wait_ld(y0);
+                tmem_wait_ld(y1);
+                tc_fence_before();
+                mbar_arrive(&barYf[b]);
+                const float2 qq = dot2_half(qt, i, hf, zc, y0, y1);  // q_i . z, q_i . Y_i
+                xg[hf * kC + i] = qq.x;
+                xd[hf * kC + i] = dpart + qq.y;
+                if (u == 0) bulk_wait_read0();  // the previous chunk's dQ has left the staging tile
+                epi_sync256();
+                const float gi = (float)P.N + xg[i] + xg[kC + i];
+                const float ig = 1.f / gi;
+                const float dt = (xd[i] + xd[kC + i]) * ig * ig;
+                regs_half_to_dq(y0, y1, hf, ig, dt, zc, dqt, i);
+                scale_row_half(ot, i, hf, ig);  // dO -> dO / g in place (Y, its unscaled reader, is done)
+                if (hf == 0) dt_tile_put(dtt + (it & 1) * 2048, i, dt);
+                fence_proxy_async_smem();
+                if (it > 0) {  // keeps barDt one phase ahead of the MMA issuer at most
+                    ok = wait_or_abort(barX, (it - 1) & 1, abort_flag, P.status, 0x329);
+                    if (!ok) break;
+                }
+                mbar_arrive(barDt);
+                epi_sync256();  // dQ of every row is staged
+                if (u == 0) store_tile(&P.tmdQ, dqt, c * kC, (int)pc.h);
+            }
+            if (!ok) break;
+            ok = wait_or_abort(barPP, pno & 1, abort_flag, P.status, 0x32A);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s0, s1, s2, s3;
+            tmem_ld2(cY + lo, s0, s1);
+            tmem_ld2(cE + lo, s2, s3);
+            tmem_wait_ld(s0, s1);
+            tmem_wait_ld(s2, s3);
+            piece_rev_sums(P, pc, R3 + lo, i, hf, __uint_as_float(s0) + __uint_as_float(s1), __uint_as_float(s2));
+            tc_fence_before();
+            mbar_arrive(barPPf);
+            epi_sync256();  // zc, ac and Sb are rewritten by the next piece
+        }
+    }
+    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
 
 // ----------------------------------------------------------------------------------------------------
-// dK / dV walk (reverse chunk order), with lane = key row j of the chunk.  Per chunk, causal:
-//   T^T = K Q^T, W^T = V dO^T -> P^T = [i >= j](1 + T^T) / g_i and U^T = [i >= j](W^T / g_i - dt_i)
-//   dK = U^T Q + V Pb^T  (then - y)        dV = P^T dO + K Pb  (then + e)
-//   dO tile <- dOt in place ; P += Q^T dOt (for the earlier chunks) ; y, e += this chunk's rows
-// Pb is the bf16 copy of P (the sum over later rows).  Non-causal: dK = V Pb^T - y, dV = K Pb + e with
-// the head's totals; stages hold only K and V.  dK leaves through the V tile and dV through the K tile.
-// TMEM: R0 T^T/P^T, R1 W^T/U^T, R2 dK then dV, R3 P.
+// dK / dV walk (reverse chunk order), causal, with lane = key row j of the chunk.  Per chunk:
+//   the epilogue first rewrites dO as dOt = dO / g in place (g_i and dt_i are the dQ walk's row
+//   statistics, loaded one chunk ahead); T^T = K Q^T (R0) and Wt^T = V dOt^T (R1);
+//   P^T = [i >= j](1 + T^T) and U^T = [i >= j](Wt^T - dt_i), both bf16, into R0 (per 64 rows i: P^T in
+//   the first 32 columns of the 64, U^T in the next 32);
+//   dK = U^T Q + V Pb^T (R2, then - y) and dV = P^T dOt + K Pb (R1, then + e);
+//   P += Q^T dOt (R3: the sum over later rows, for the earlier chunks), and the chunk's column sums
+//   y_c = Q^T dt, e_c = dOt^T 1 (N = 16 MMAs into R2 once dK has been drained).
+// Pb is the bf16 copy of P.  dK leaves through the V tile, dV through its own staging tile.  One TMA stage
+// (Q, dO, K, V); the next chunk's tiles are prefetched into L2 meanwhile.
 // ----------------------------------------------------------------------------------------------------
-template <bool CAUSAL>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
-    constexpr int NST = CAUSAL ? 1 : 3;
     constexpr uint32_t TB = NB * kBox;
-    constexpr uint32_t STAGE = CAUSAL ? 4 * TB : 2 * TB;  // causal: Q, dO, K, V; non-causal: K, V
-    constexpr uint32_t OFF_K = CAUSAL ? 2 * TB : 0, OFF_V = CAUSAL ? 3 * TB : TB;
+    constexpr uint32_t STAGE = 4 * TB;  // Q, dO, K, V
+    constexpr uint32_t E = kEpiThreads;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    bool aligned;
+    unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
+    unsigned char *stage = sm;
+    unsigned char *Pb = sm + STAGE;
+    unsigned char *dvt = Pb + TB;      // dV staging tile
+    unsigned char *ones = dvt + TB;    // 8 rows x 128 B of bf16 1.0
+    unsigned char *dtt = ones + 1024;  // dt_i of the chunk's rows as an N = 16 operand (dt_tile_put)
+    float *yc = (float *)(dtt + 2048); // y over the later rows (fp32, D)
+    float *ec = yc + D;                // e over the later rows
+    float *sDt = ec + D;               // dt_i of the chunk's rows
+    uint64_t *full = (uint64_t *)(sDt + kC);
+    uint64_t *empty = full + 1;
+    uint64_t *bar = empty + 1;
+    uint64_t *barO = bar, *barT = bar + 1, *barP = bar + 2, *barPb = bar + 3, *barK = bar + 4, *barV = bar + 5,
+             *barKf = bar + 6, *barC = bar + 7, *barR = bar + 8;
+    uint32_t *tslot = (uint32_t *)(bar + 9);
+    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    if (!aligned) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(full, 1);
+        mbar_init(empty, 2);  // the chunk's last MMA commit + the epilogue once dK has left the V tile
+        const uint32_t counts[9] = {E, 1, E, E, 1, 1, E, 1, E};
+        for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
+    for (int k = threadIdx.x; k < 512; k += blockDim.x) ((uint32_t *)dtt)[k] = 0u;
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
+    const uint32_t cY = R2, cE = R2 + 16;  // the chunk's y (columns 0, 1: two parts) and e (column 0)
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer (chunks of each piece in reverse order)
+        prefetch_tmap(&P.tmQ);
+        prefetch_tmap(&P.tmdO);
+        prefetch_tmap(&P.tmK);
+        prefetch_tmap(&P.tmV);
+        int it = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+            const Piece pc = pi.get();
+            for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
+                if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x401)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full, STAGE);
+                for (int nb = 0; nb < NB; ++nb) {
+                    tma_load_3d(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, (int)pc.h);
+                }
+                long long nh;
+                int nc;
+                if (next_rev_chunk(pi, pc, c, &nh, &nc)) {  // the next chunk to be walked, into L2
+                    for (int nb = 0; nb < NB; ++nb) {
+                        tma_prefetch_3d(&P.tmQ, nb * 64, nc * kC, (int)nh);
+                        tma_prefetch_3d(&P.tmdO, nb * 64, nc * kC, (int)nh);
+                        tma_prefetch_3d(&P.tmK, nb * 64, nc * kC, (int)nh);
+                        tma_prefetch_3d(&P.tmV, nb * 64, nc * kC, (int)nh);
+                    }
+                }
+            }
+        }
+        if (!ok && it > 0) mbar_wait(full, (it - 1) & 1, 50000000ull);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t idKK = idesc_bf16(128, 128, false, false);
+        const uint32_t idKM = idesc_bf16(128, 128, false, true);
+        const uint32_t idMM = idesc_bf16(128, 128, true, true);
+        const uint32_t idZ = idesc_bf16(128, 16, true, false);
+        const uint32_t pb = smem_u32(Pb), on = smem_u32(ones), dtb = smem_u32(dtt);
+        const uint32_t qb = smem_u32(stage), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
+        int it = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+            const Piece pc = pi.get();
+            for (int c = pc.e - 1; c >= pc.a && ok; --c, ++it) {
+                const uint32_t ph = it & 1;
+                ok = wait_or_abort(full, ph, abort_flag, P.status, 0x403);
+                if (ok && it > 0) ok = wait_or_abort(barR, ph ^ 1, abort_flag, P.status, 0x402);  // TMEM drained
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // T^T = K Q^T
+                    const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
+                    mma_ss(R0, sdesc_sw128(kb + o, 16, 1024), sdesc_sw128(qb + o, 16, 1024), idKK, k > 0);
+                }
+                ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x404);  // dOt is in place of dO
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // Wt^T = V dOt^T
+                    const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
+                    mma_ss(R1, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(ob + o, 16, 1024), idKK, k > 0);
+                }
+                mma_commit(barT);
+                if (c > pc.a) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)  // P += Q^T dOt
+                        mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024),
+                               idMM, 1u);
+                }
+                ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x405);
+                if (ok) ok = wait_or_abort(barPb, ph, abort_flag, P.status, 0x406);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // dK = U^T Q + V Pb^T
+                    const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
+                    mma_ts(R2, R0 + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_sw128(qb + 2048 * k, kBox, 1024), idKM, k > 0);
+                    mma_ss(R2, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(pb + o, 16, 1024), idKK, 1u);
+                }
+                mma_commit(barK);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // dV = P^T dOt + K Pb
+                    mma_ts(R1, R0 + 64 * (k >> 2) + 8 * (k & 3), sdesc_sw128(ob + 2048 * k, kBox, 1024), idKM, k > 0);
+                    mma_ss(R1, sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                           sdesc_sw128(pb + 2048 * k, kBox, 1024), idKM, 1u);
+                }
+                mma_commit(barV);
+                ok = wait_or_abort(barKf, ph, abort_flag, P.status, 0x407);  // dK has been read out of R2
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // y_c = Q^T dt ; e_c = dOt^T 1
+                    mma_ss(cY, sdesc_sw128(qb + 2048 * k, kBox, 1024),
+                           sdesc_sw128(dtb + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idZ, k > 0);
+                    mma_ss(cE, sdesc_sw128(ob + 2048 * k, kBox, 1024), sdesc_sw128(on + 32 * (k & 3), 16, 0), idZ,
+                           k > 0);
+                }
+                mma_commit(barC);
+                mma_commit(empty);
+            }
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue: thread <-> key row j (TMEM lane) and column half hf
+        const int u = threadIdx.x - 64;
+        const int q4 = warp & 3, hf = (warp - 2) >> 2;
+        const int j = 32 * q4 + lane;
+        const uint32_t lo = (uint32_t)(32 * q4) << 16;
+        unsigned char *ot = stage + TB, *vt = stage + 3 * TB;
+        float ng = 0.f, ndt = 0.f;  // g_j and dt_j of row j of the next chunk to be walked
+        {
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid()) {
+                const Piece q = p0.get();
+                load_row_stats(P, q.h, q.e - 1, j, &ng, &ndt);
+            }
+        }
+        int it = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+            const Piece pc = pi.get();
+            // carried reverse sums (the later pieces of the head), combined into this piece's own slot by
+            // tc_scan_slots; the previous piece's MMAs on R3 and Pb are complete (its last barC)
+            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, R3 + lo, 0u, 0u, Pb, yc,
+                            ec, true, /*vec_to_tmem=*/false);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            epi_sync256();
+            mbar_arrive(barPb);
+            for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
+                const uint32_t ph = it & 1;
+                const long long row0 = (long long)c * kC;
+                const float igj = row0 + j < P.N ? 1.f / ng : 0.f, dtj = ndt;
+                {
+                    long long nh;
+                    int nc;
+                    if (next_rev_chunk(pi, pc, c, &nh, &nc)) load_row_stats(P, nh, nc, j, &ng, &ndt);
+                }
+                ok = wait_or_abort(full, ph, abort_flag, P.status, 0x408);
+                if (!ok) break;
+                scale_row_half(ot, j, hf, igj);  // dO row -> dOt row in place
+                if (hf == 0) {
+                    sDt[j] = dtj;
+                    dt_tile_put(dtt, j, dtj);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(barO);
+                epi_sync256();  // every dt_i is in sDt
+                ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x40A);
+                if (!ok) break;
+                tc_fence_after();
+                {  // columns are query rows i of the chunk: keep i >= j.  Each half rewrites only the R0 columns it
+                   // has read: P^T of its 64 rows i into R0 + 64 hf + [0, 32), U^T into R0 + 64 hf + [32, 64)
+                    uint32_t pk[32];
+                    tmem_half_to_bf16(R0 + lo, hf, [&](int i, float x) { return i >= j ? 1.f + x : 0.f; }, pk);
+                    tmem_st32(R0 + lo + 64 * hf, pk);
+                    tmem_half_to_bf16(R1 + lo, hf, [&](int i, float x) { return i >= j ? x - sDt[i] : 0.f; }, pk);
+                    tmem_st32(R0 + lo + 64 * hf + 32, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(barP);
+                }
+                // dK_j = [R2]_j - y, staged in the V tile (its last reader, dK += V Pb^T, is done)
+                ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
+                if (!ok) break;
+                tc_fence_after();
+                tmem_half_to_out(R2 + lo, hf, yc, -1.f, vt, j);
+                tc_fence_before();
+                mbar_arrive(barKf);
+                fence_proxy_async_smem();
+                if (u == 0) bulk_wait_read0();  // the previous chunk's dV has left its staging tile
+                epi_sync256();
+                if (u == 0) store_tile(&P.tmdK, vt, (int)row0, (int)pc.h);
+                // dV_j = [R1]_j + e
+                ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x40C);
+                if (!ok) break;
+                tc_fence_after();
+                tmem_half_to_out(R1 + lo, hf, ec, 1.f, dvt, j);
+                fence_proxy_async_smem();
+                epi_sync256();  // dV rows staged; every read of yc and ec for this chunk is done
+                if (u == 0) {
+                    store_tile(&P.tmdV, dvt, (int)row0, (int)pc.h);
+                    bulk_wait_read1();  // dK has left the V tile
+                    mbar_arrive(empty);
+                }
+                // the chunk's column sums; P (with this chunk's rows, for the earlier chunks) -> Pb
+                ok = wait_or_abort(barC, ph, abort_flag, P.status, 0x40D);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t s0, s1;
+                tmem_ld2(hf == 0 ? cY + lo : cE + lo, s0, s1);
+                tmem_wait_ld(s0, s1);
+                if (c > pc.a) {
+                    tmem_half_to_tile(R3 + lo, Pb, j, hf);
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before();
+                mbar_arrive(barR);
+                if (c > pc.a) mbar_arrive(barPb);
+                if (hf == 0)
+                    yc[j] += __uint_as_float(s0) + __uint_as_float(s1);
+                else
+                    ec[j] += __uint_as_float(s0);
+                epi_sync256();
+            }
+        }
+    }
+    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ----------------------------------------------------------------------------------------------------
+// dK / dV walk, non-causal: dK = V Pb^T - y and dV = K Pb + e with the head's totals P, y, e
+// (tc_scan_slots mode 2), so only K and V are read.  Three TMA stages of (K, V); R2 accumulates dK,
+// then dV; dK leaves through the V tile and dV through the K tile.
+// ----------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(const __grid_constant__ TcParams P) {
+    constexpr int D = 128, NB = D / 64, NST = 3;
+    constexpr uint32_t TB = NB * kBox;
+    constexpr uint32_t STAGE = 2 * TB;  // K, V
+    constexpr uint32_t E = kEpiThreads;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     bool aligned;
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
@@ -524,15 +1063,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     unsigned char *Pb = sm + NST * STAGE;
     float *yc = (float *)(Pb + TB);
     float *ec = yc + D;
-    float *sIg = ec + D;                  // causal only: 1/g_i and dt_i of the chunk's rows
-    float *sDt = sIg + (CAUSAL ? kC : 0);
-    float *cs = sDt + (CAUSAL ? kC : 0);  // causal only: [2][2][128] column-sum partials
-    uint64_t *full = (uint64_t *)(cs + (CAUSAL ? 4 * D : 0));
+    uint64_t *full = (uint64_t *)(ec + D);
     uint64_t *empty = full + NST;
     uint64_t *bar = empty + NST;
-    uint64_t *barT = bar, *barP = bar + 1, *barPb = bar + 2, *barK = bar + 3, *barKf = bar + 4, *barV = bar + 5,
-             *barDt = bar + 6, *barS = bar + 7, *barVf = bar + 8;
-    uint32_t *tslot = (uint32_t *)(bar + 9);
+    uint64_t *barPb = bar, *barK = bar + 1, *barKf = bar + 2, *barV = bar + 3, *barVf = bar + 4;
+    uint32_t *tslot = (uint32_t *)(bar + 5);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
@@ -542,9 +1077,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 2);  // MMA commit + the epilogue once its dK, dV tiles have left shared memory
         }
-        const uint32_t E = kEpiThreads;
-        const uint32_t counts[9] = {1, E, E, 1, E, 1, E, 1, E};
-        for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
+        const uint32_t counts[5] = {E, 1, E, 1, E};
+        for (int k = 0; k < 5; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -556,35 +1090,27 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
+    const uint32_t R2 = tmem + 256;
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer (chunks of each piece in reverse order)
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
-        if (CAUSAL) {
-            prefetch_tmap(&P.tmQ);
-            prefetch_tmap(&P.tmdO);
-        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 const int s = it % NST;
-                if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x401)) {
+                if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x421)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + OFF_K + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(st + OFF_V + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
-                    if (CAUSAL) {
-                        tma_load_3d(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, (int)pc.h);
-                        tma_load_3d(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, (int)pc.h);
-                    }
+                    tma_load_3d(st + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tma_load_3d(st + TB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
                 }
             }
         }
@@ -595,75 +1121,34 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         // ---- MMA issuer
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
-        const uint32_t idMM = idesc_bf16(128, 128, true, true);
         const uint32_t pb = smem_u32(Pb);
         int it = 0, pno = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            if (!CAUSAL && !wait_or_abort(barPb, pno & 1, abort_flag, P.status, 0x402)) break;
+            if (!wait_or_abort(barPb, pno & 1, abort_flag, P.status, 0x422)) break;
             for (int c = pc.e - 1; c >= pc.a && ok; --c, ++it) {
                 const int s = it % NST;
                 const uint32_t ph = it & 1;
-                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x403);
+                ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x423);
+                if (ok && it > 0) ok = wait_or_abort(barVf, ph ^ 1, abort_flag, P.status, 0x424);  // R2 drained
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t base = smem_u32(stages + s * STAGE);
-                const uint32_t qb = base, ob = base + TB, kb = base + OFF_K, vb = base + OFF_V;
-                if (CAUSAL) {
+                const uint32_t kb = smem_u32(stages + s * STAGE), vb = kb + TB;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {  // T^T = K Q^T ; W^T = V dO^T
-                        const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
-                        mma_ss(R0, sdesc_sw128(kb + o, 16, 1024), sdesc_sw128(qb + o, 16, 1024), idKK, k > 0);
-                        mma_ss(R1, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(ob + o, 16, 1024), idKK, k > 0);
-                    }
-                    mma_commit(barT);
-                    ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x404);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)  // dK = U^T Q
-                        mma_ts(R2, R1 + 8 * k, sdesc_sw128(qb + 2048 * k, kBox, 1024), idKM, k > 0);
-                    ok = wait_or_abort(barPb, ph, abort_flag, P.status, 0x405);
-                    if (!ok) break;
-                    tc_fence_after();
-                } else if (it > 0) {
-                    ok = wait_or_abort(barVf, (it - 1) & 1, abort_flag, P.status, 0x406);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // dK += V Pb^T
+                for (int k = 0; k < 8; ++k) {  // dK = V Pb^T
                     const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
-                    mma_ss(R2, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(pb + o, 16, 1024), idKK,
-                           (CAUSAL || k > 0) ? 1u : 0u);
+                    mma_ss(R2, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(pb + o, 16, 1024), idKK, k > 0);
                 }
                 mma_commit(barK);
-                ok = wait_or_abort(barKf, ph, abort_flag, P.status, 0x407);
+                ok = wait_or_abort(barKf, ph, abort_flag, P.status, 0x425);
                 if (!ok) break;
                 tc_fence_after();
-                if (CAUSAL) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)  // dV = (P/g)^T dO
-                        mma_ts(R2, R0 + 8 * k, sdesc_sw128(ob + 2048 * k, kBox, 1024), idKM, k > 0);
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k)  // dV += K Pb
+                for (int k = 0; k < 8; ++k)  // dV = K Pb
                     mma_ss(R2, sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(pb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
+                           sdesc_sw128(pb + 2048 * k, kBox, 1024), idKM, k > 0);
                 mma_commit(barV);
-                if (CAUSAL) {
-                    ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x408);  // dOt is in place of dO
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (c > pc.a) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)  // P += Q^T dOt
-                            mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024),
-                                   idMM, 1u);
-                    }
-                    mma_commit(barS);
-                }
                 mma_commit(&empty[s]);
             }
         }
@@ -672,132 +1157,49 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         const int u = threadIdx.x - 64;
         const int q4 = warp & 3, hf = (warp - 2) >> 2;
         const int j = 32 * q4 + lane;
-        const int which = u >> 7, cp = u & 63, rh = (u >> 6) & 1;
         const uint32_t lo = (uint32_t)(32 * q4) << 16;
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried reverse sums (causal: later pieces of the head; non-causal: the whole head), combined
-            // into this piece's own slot by tc_scan_slots
-            if (CAUSAL && it > 0) {
-                if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x409)) break;
-                tc_fence_after();
-            }
-            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, R3 + lo, 0u, 0u, Pb, yc,
-                            ec, CAUSAL, /*vec_to_tmem=*/false);
+            // the head's totals (every piece of a head carries the same sums); the previous piece's MMAs
+            // on Pb are complete (its last barV)
+            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, 0u, 0u, 0u, Pb, yc, ec,
+                            false, false);
             fence_proxy_async_smem();
-            tc_fence_before();
             epi_sync256();
             mbar_arrive(barPb);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 const int s = it % NST;
                 const uint32_t ph = it & 1;
                 unsigned char *st = stages + s * STAGE;
-                unsigned char *qt = st, *ot = st + TB;
-                const long long row0 = (long long)c * kC;
-                const int nvalid = (int)min((long long)kC, P.N - row0);
-                if (CAUSAL) {
-                    if (hf == 0) {
-                        const bool ok_row = j < nvalid;
-                        const size_t grow = (size_t)pc.h * P.N + row0 + j;
-                        sIg[j] = ok_row ? 1.f / P.rs_g[grow] : 0.f;
-                        sDt[j] = ok_row ? P.rs_dt[grow] : 0.f;
-                    }
-                    epi_sync256();
-                    ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x40A);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // columns are query rows i of the chunk: keep i >= j
-                    uint32_t pk0[32], pk1[32];
-                    tmem_half_to_bf16(R0 + lo, hf, [&](int i, float x) { return i >= j ? (1.f + x) * sIg[i] : 0.f; }, pk0);
-                    tmem_half_to_bf16(R1 + lo, hf, [&](int i, float x) { return i >= j ? x * sIg[i] - sDt[i] : 0.f; }, pk1);
-                    tc_fence_before();
-                    epi_sync256();
-                    tc_fence_after();
-                    tmem_st32(R0 + lo + 32 * hf, pk0);
-                    tmem_st32(R1 + lo + 32 * hf, pk1);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(barP);
-                }
-                // dK_j = [accumulator]_j - y, staged in the V tile (its last reader, dK += V Pb^T, is done)
-                ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
+                const int row0 = c * kC;
+                // dK_j = [R2]_j - y, staged in the V tile (its last reader, dK = V Pb^T, is done)
+                ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x426);
                 if (!ok) break;
                 tc_fence_after();
-                tmem_half_to_out(R2 + lo, hf, yc, -1.f, st + OFF_V, j);
+                tmem_half_to_out(R2 + lo, hf, yc, -1.f, st + TB, j);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(barKf);
                 epi_sync256();
-                if (u == 0) store_tile(&P.tmdK, st + OFF_V, (int)row0, (int)pc.h);
-                // dV_j = [accumulator]_j + e, staged in the K tile (its last reader, dV += K Pb, is done)
-                ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x40C);
+                if (u == 0) store_tile(&P.tmdK, st + TB, row0, (int)pc.h);
+                // dV_j = [R2]_j + e, staged in the K tile (its last reader, dV = K Pb, is done)
+                ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x427);
                 if (!ok) break;
                 tc_fence_after();
-                tmem_half_to_out(R2 + lo, hf, ec, 1.f, st + OFF_K, j);
+                tmem_half_to_out(R2 + lo, hf, ec, 1.f, st, j);
                 fence_proxy_async_smem();
                 tc_fence_before();
-                if (!CAUSAL) mbar_arrive(barVf);
+                mbar_arrive(barVf);
                 epi_sync256();
-                if (u == 0) store_tile(&P.tmdV, st + OFF_K, (int)row0, (int)pc.h);
-                if (!CAUSAL) {
-                    if (u == 0) {
-                        bulk_wait_read0();
-                        mbar_arrive(&empty[s]);
-                    }
-                    continue;
-                }
-                // dO row -> dOt row in place, for P += Q^T dOt and the e sums
-                {
-                    const float igj = sIg[j];
-                    unsigned char *tile = ot + hf * kBox;
-#pragma unroll
-                    for (int g8 = 0; g8 < 8; ++g8) {
-                        uint4 *p4 = (uint4 *)(tile + sw128_off(j, g8));
-                        uint4 w = *p4;
-                        uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * igj, bf16hi(wv[q]) * igj);
-                        *p4 = w;
-                    }
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(barDt);
-                epi_sync256();  // every row of dOt is in shared memory
-                {  // this chunk's rows: y += sum dt_i q_i (which 0), e += sum dOt_i (which 1)
-                    const float2 v = colsum_half(which == 0 ? qt : ot, cp, rh, which == 0 ? sDt : nullptr);
-                    cs[(which * 2 + rh) * D + 2 * cp] = v.x;
-                    cs[(which * 2 + rh) * D + 2 * cp + 1] = v.y;
-                }
-                epi_sync256();
-                float2 yn = make_float2(0.f, 0.f);
-                if (rh == 0) {
-                    const float *base = which == 0 ? yc : ec;
-                    const float *c0 = cs + (which * 2) * D, *c1 = c0 + D;
-                    yn = make_float2(base[2 * cp] + c0[2 * cp] + c1[2 * cp], base[2 * cp + 1] + c0[2 * cp + 1] + c1[2 * cp + 1]);
-                }
                 if (u == 0) {
-                    bulk_wait_read0();  // dK and dV have left the V and K tiles
+                    store_tile(&P.tmdV, st, row0, (int)pc.h);
+                    bulk_wait_read0();
                     mbar_arrive(&empty[s]);
                 }
-                ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x40D);
-                if (!ok) break;
-                tc_fence_after();
-                if (c > pc.a) {
-                    tmem_half_to_tile(R3 + lo, Pb, j, hf);
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(barPb);
-                }
-                if (rh == 0) {
-                    float *base = which == 0 ? yc : ec;
-                    base[2 * cp] = yn.x;
-                    base[2 * cp + 1] = yn.y;
-                }
-                epi_sync256();
             }
+            epi_sync256();  // every read of Pb, yc, ec is done before the next piece's carry
         }
     }
     if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
@@ -808,9 +1210,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     }
 }
 
-template __global__ void tc_bwd_dkdv_kernel<true>(const __grid_constant__ TcParams P);
-template __global__ void tc_bwd_dkdv_kernel<false>(const __grid_constant__ TcParams P);
-
 }  // namespace tc
 
 // ======================================================================================== host ===
@@ -818,21 +1217,21 @@ template __global__ void tc_bwd_dkdv_kernel<false>(const __grid_constant__ TcPar
 namespace {
 
 constexpr size_t kTB = 2 * (size_t)tc::kBox;
-constexpr size_t kEpiSmemDq = 2 * 128 * 4 + 128 * 4 + 4 * 128 * 4 + 4 * 128 * 4;  // z, a, dt, 2 x-arrays, cs
-constexpr size_t kSmemDq = 4 * kTB + kTB + kEpiSmemDq + 512;         // causal: 1 stage of Q, dO, K, V
-constexpr size_t kSmemDqNc = 2 * 2 * kTB + kTB + kEpiSmemDq + 512;   // 2 stages of Q, dO
-constexpr size_t kSmemDkdv = 4 * kTB + kTB + 4 * 128 * 4 + 4 * 128 * 4 + 512;  // y, e, 1/g, dt, cs
+constexpr size_t kEpiSmemDq = 2 * 128 * 4 + 4 * 128 * 4;  // z, a, 2 row-partial arrays
+constexpr size_t kSmemDq = 4 * kTB + 2 * kTB + 1024 + 2048 + kEpiSmemDq + 512;    // 1 stage of Q, dO, K, V; Sb; dQ; ones; dt
+constexpr size_t kSmemDqNc = 2 * 2 * kTB + 2 * kTB + 1024 + 4096 + kEpiSmemDq + 512;  // 2 stages of Q, dO; Sb; dQ; ones; 2 dt
+constexpr size_t kSmemDkdv = 4 * kTB + 2 * kTB + 1024 + 2048 + 3 * 128 * 4 + 512;  // stage; Pb; dV; ones; dt; y, e, dt
 constexpr size_t kSmemDkdvNc = 3 * 2 * kTB + kTB + 2 * 128 * 4 + 512;         // 3 stages of K, V
-static_assert(kSmemDkdvNc <= 232448 && kSmemDq <= 232448, "backward kernel exceeds the shared-memory limit");
+static_assert(kSmemDkdvNc <= 232448 && kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemDqNc <= 232448, "backward kernel exceeds the shared-memory limit");
 
 bool set_bwd_attrs() {
     static int done = 0;
     if (done) return done > 0;
     const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    bool ok = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<true>, A, (int)kSmemDq) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dq_kernel<false>, A, (int)kSmemDqNc) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<true>, A, (int)kSmemDkdv) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel<false>, A, (int)kSmemDkdvNc) == cudaSuccess;
+    bool ok = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel, A, (int)kSmemDq) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dq_nc_kernel, A, (int)kSmemDqNc) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel, A, (int)kSmemDkdv) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_bwd_dkdv_nc_kernel, A, (int)kSmemDkdvNc) == cudaSuccess;
     done = ok ? 1 : -1;
     return ok;
 }
@@ -860,15 +1259,15 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     if (e == cudaSuccess) e = tc_host::launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
     if (e != cudaSuccess) return e;
     if (p.causal)
-        tc::tc_bwd_dq_kernel<true><<<P.sl.G, nthr, kSmemDq, s>>>(P);
+        tc::tc_bwd_dq_kernel<<<P.sl.G, nthr, kSmemDq, s>>>(P);
     else
-        tc::tc_bwd_dq_kernel<false><<<P.sl.G, nthr, kSmemDqNc, s>>>(P);
+        tc::tc_bwd_dq_nc_kernel<<<P.sl.G, nthr, kSmemDqNc, s>>>(P);
     e = tc_host::launch_scan(P.slots_rev, P, p.BH, p.causal ? 1 : 2, s);
     if (e != cudaSuccess) return e;
     if (p.causal)
-        tc::tc_bwd_dkdv_kernel<true><<<P.sl.G, nthr, kSmemDkdv, s>>>(P);
+        tc::tc_bwd_dkdv_kernel<<<P.sl.G, nthr, kSmemDkdv, s>>>(P);
     else
-        tc::tc_bwd_dkdv_kernel<false><<<P.sl.G, nthr, kSmemDkdvNc, s>>>(P);
+        tc::tc_bwd_dkdv_nc_kernel<<<P.sl.G, nthr, kSmemDkdvNc, s>>>(P);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(5);
     return e;

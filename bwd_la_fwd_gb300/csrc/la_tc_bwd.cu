@@ -9,10 +9,11 @@
 // where S_c, z_c (earlier rows) are the forward state and P_c = sum q_i dOt_i^T, y_c = sum dt_i q_i,
 // e_c = sum dOt_i run over the later rows.  Non-causal: every sum runs over the whole head.
 //
-// Launches: the per-piece K^T V sums and their scan (shared with the forward), the dQ walk in chunk
-// order (it forms g_i and delta_i from the chunk's own products and the carried state, so the stored O
-// is not read; it also writes each piece's reverse sums P, y, e and, causal, the per-row g_i, dt_i), the
-// scan of the reverse sums, and the dK / dV walk in reverse chunk order.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
+// Launches: the per-piece K^T V sums (shared with the forward), the dQ walk in chunk order (it forms g_i
+// and delta_i from the chunk's own products and the carried state, so the stored O is not read; it also
+// writes each piece's reverse sums P, y, e and, causal, the per-row g_i, dt_i), and the dK / dV walk in
+// reverse chunk order.  Each walk adds up the slots of the head's other pieces itself when it loads the
+// state carried into a piece.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
 // per TMEM lane quarter, each owning 64 of the 128 columns).
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -433,10 +434,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried forward state of the piece, combined into its own slot by tc_scan_slots (the previous
+            // forward state carried into the piece, from the head's earlier pieces (the previous
             // piece's MMAs on R2 are complete: its last barX has been waited for)
-            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, R2 + lo, 0u, 0u, Sb, zc,
-                            ac, true, /*vec_to_tmem=*/false);
+            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryEarlier, i, hf, R2 + lo, 0u, 0u,
+                                Sb, zc, ac, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
 }
 
 // ----------------------------------------------------------------------------------------------------
-// dQ walk, non-causal.  Every row sees the head's totals S, z, a (tc_scan_slots mode 2), so the chunks
+// dQ walk, non-causal.  Every row sees the head's totals S, z, a (all its pieces' slots), so the chunks
 // of a piece are independent apart from the piece sums Ppiece = sum_i q_i (dO_i / g_i)^T, y and e:
 //   g_i = N + q_i . z,   delta_i g_i = dO_i . a + q_i . Y_i,   dQ_i = Y_i / g_i - dt_i z,   Y = dO Sb^T.
 // Two TMA stages of (Q, dO).  Y alternates between TMEM blocks R0 and R1, so that the MMA of the next
@@ -704,8 +705,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, 0u, 0u, 0u, Sb, zc, ac,
-                            false, false);
+            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryAll, i, hf, 0u, 0u, 0u, Sb, zc,
+                                ac, false, false);
             fence_proxy_async_smem();
             epi_sync256();
             mbar_arrive(barSb);
@@ -952,10 +953,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried reverse sums (the later pieces of the head), combined into this piece's own slot by
-            // tc_scan_slots; the previous piece's MMAs on R3 and Pb are complete (its last barC)
-            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, R3 + lo, 0u, 0u, Pb, yc,
-                            ec, true, /*vec_to_tmem=*/false);
+            // carried reverse sums (the later pieces of the head); the previous piece's MMAs on R3 and Pb are
+            // complete (its last barC)
+            load_carry_sum_half(P.slots_rev, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryLater, j, hf, R3 + lo, 0u,
+                                0u, Pb, yc, ec, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
@@ -1048,7 +1049,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
 
 // ----------------------------------------------------------------------------------------------------
 // dK / dV walk, non-causal: dK = V Pb^T - y and dV = K Pb + e with the head's totals P, y, e
-// (tc_scan_slots mode 2), so only K and V are read.  Three TMA stages of (K, V); R2 accumulates dK,
+// (the sum of all its pieces' slots), so only K and V are read.  Three TMA stages of (K, V); R2 accumulates dK,
 // then dV; dK leaves through the V tile and dV through the K tile.
 // ----------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(const __grid_constant__ TcParams P) {
@@ -1164,8 +1165,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
             const Piece pc = pi.get();
             // the head's totals (every piece of a head carries the same sums); the previous piece's MMAs
             // on Pb are complete (its last barV)
-            load_carry_half(P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride, j, hf, 0u, 0u, 0u, Pb, yc, ec,
-                            false, false);
+            load_carry_sum_half(P.slots_rev, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryAll, j, hf, 0u, 0u, 0u, Pb,
+                                yc, ec, false, false);
             fence_proxy_async_smem();
             epi_sync256();
             mbar_arrive(barPb);
@@ -1256,20 +1257,17 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dV = dV;
     const unsigned nthr = 64 + tc::kEpiThreads;
     cudaError_t e = tc_host::launch_agg(P, s);
-    if (e == cudaSuccess) e = tc_host::launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
     if (e != cudaSuccess) return e;
     if (p.causal)
         tc::tc_bwd_dq_kernel<<<P.sl.G, nthr, kSmemDq, s>>>(P);
     else
         tc::tc_bwd_dq_nc_kernel<<<P.sl.G, nthr, kSmemDqNc, s>>>(P);
-    e = tc_host::launch_scan(P.slots_rev, P, p.BH, p.causal ? 1 : 2, s);
-    if (e != cudaSuccess) return e;
     if (p.causal)
         tc::tc_bwd_dkdv_kernel<<<P.sl.G, nthr, kSmemDkdv, s>>>(P);
     else
         tc::tc_bwd_dkdv_nc_kernel<<<P.sl.G, nthr, kSmemDkdvNc, s>>>(P);
     e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(5);
+    if (e == cudaSuccess) count_launches(3);
     return e;
 }
 

@@ -336,14 +336,13 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
-            // carried state (causal: the earlier pieces of the head; non-causal: the whole head), already
-            // combined into this piece's own slot by tc_scan_slots
+            // carried state (causal: the earlier pieces of the head; non-causal: the whole head)
             if (CAUSAL && it > 0) {  // the previous piece's last MMAs must be done before TMEM S is reset
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x206)) break;
                 tc_fence_after();
             }
-            load_carry_half(P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride, i, hf, tS + lo, tZ + lo, tA + lo,
-                            Sb, zc, ac, CAUSAL);
+            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, CAUSAL ? kCarryEarlier : kCarryAll, i,
+                                hf, tS + lo, tZ + lo, tA + lo, Sb, zc, ac, CAUSAL, true);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
@@ -470,48 +469,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
 template __global__ void tc_fwd_kernel<true>(const __grid_constant__ TcParams P);
 template __global__ void tc_fwd_kernel<false>(const __grid_constant__ TcParams P);
 
-// ----------------------------------------------------------------------------------------------------
-// In-place scan of the per-piece state sums of each head, so that every piece then reads exactly one
-// slot (its own): mode 0 = exclusive prefix over the head's pieces (causal forward direction),
-// 1 = exclusive suffix (causal reverse direction), 2 = the head's total in every slot (non-causal).
-// grid = (ceil(used4 / 256), BH); thread x owns float4 x of the state.  A head's slots are read in groups
-// of eight with every load of a group issued before any store.
-// ----------------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_scan_slots(float *slots, long long stride, Slices sl, int mode,
-                                                      int used4) {
-    const int x = blockIdx.x * 256 + threadIdx.x;
-    if (x >= used4) return;
-    const long long h = blockIdx.y;
-    const long long h0 = h * sl.nchunk;
-    const int b0 = cta_of(sl, h0), b1 = cta_of(sl, h0 + sl.nchunk - 1);
-    const int n = b1 - b0 + 1;
-    float4 *base = (float4 *)slots + x;
-    const long long s4 = stride / 4;
-    auto at = [&](int k) -> float4 * {  // k-th slot of the head in scan order
-        const int b = mode == 1 ? b1 - k : b0 + k;
-        return base + slot_of(h, b) * s4;
-    };
-    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int g0 = 0; g0 < n; g0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (g0 + k < n) v[k] = *at(g0 + k);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if (g0 + k < n) {
-                if (mode != 2) *at(g0 + k) = run;
-                run.x += v[k].x;
-                run.y += v[k].y;
-                run.z += v[k].z;
-                run.w += v[k].w;
-            }
-        }
-    }
-    if (mode == 2)
-        for (int k = 0; k < n; ++k) *at(k) = run;
-}
-
 }  // namespace tc
 
 // ======================================================================================== host ===
@@ -594,12 +551,6 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     return true;
 }
 
-cudaError_t launch_scan(float *slots, const tc::TcParams &P, int BH, int mode, cudaStream_t s) {
-    const int used4 = (128 * 128 + 2 * 128) / 4;
-    tc::tc_scan_slots<<<dim3((used4 + 255) / 256, BH), 256, 0, s>>>(slots, P.slot_stride, P.sl, mode, used4);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
     if (!set_smem_attrs()) return cudaErrorInvalidValue;
     tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
@@ -625,14 +576,12 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     P.O = O;
     P.g = g;
     tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
-    cudaError_t e0 = launch_scan(P.slots, P, p.BH, p.causal ? 0 : 2, s);
-    if (e0 != cudaSuccess) return e0;
     if (p.causal)
         tc::tc_fwd_kernel<true><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s>>>(P);
     else
         tc::tc_fwd_kernel<false><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s>>>(P);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) count_launches(3);
+    if (e == cudaSuccess) count_launches(2);
     return e;
 }
 

@@ -34,8 +34,6 @@ namespace tc_host {
 bool make_map(CUtensorMap *m, const void *ptr, const Plan &p);
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
-// mode 0: exclusive prefix per head, 1: exclusive suffix, 2: head total in every slot
-cudaError_t launch_scan(float *slots, const tc::TcParams &P, int BH, int mode, cudaStream_t s);
 }  // namespace tc_host
 
 // bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.

@@ -23,60 +23,43 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" :::
 constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane quarter
 __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-// The whole carried state `slot` ([S row-major | z | a], fp32) for row d (four-warp epilogues): row d of S
-// into TMEM (if to_tmem) and, as bf16, into row d of the operand tile Sb; z[d] to zc, a[d] to ac.
-// The loads of each 64-column half are issued together.
-__device__ __forceinline__ void load_carry1(const float *slot, int d, uint32_t tS, unsigned char *Sb, float *zc,
-                                            float *ac, bool to_tmem) {
+// Which of a head's pieces make up the state carried into a piece.
+enum CarryMode { kCarryEarlier = 0, kCarryLater = 1, kCarryAll = 2 };
+
+// Half `hf` of the state carried into CTA b's piece of head h, summed here from the per-piece slots
+// ([S row-major | z | a], fp32, `stride` floats apart) of the head's other pieces: the earlier ones
+// (causal, chunk order), the later ones (causal, reverse order) or all of them (non-causal); a head
+// spans only a few slices, so this is a handful of slots read from L2.  Row d, columns [64 hf, 64 hf + 64)
+// of S go into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes
+// z[d] to zc (and TMEM column tZ if to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and column tA).
+__device__ __forceinline__ void load_carry_sum_half(const float *slots, long long stride, const Slices &sl,
+                                                    long long h, int b, CarryMode mode, int d, int hf, uint32_t tS,
+                                                    uint32_t tZ, uint32_t tA, unsigned char *Sb, float *zc,
+                                                    float *ac, bool to_tmem, bool vec_to_tmem) {
     constexpr int D = 128;
-    const float zv = slot[(size_t)D * D + d], av = slot[(size_t)D * D + D + d];
+    const long long x0 = h * sl.nchunk;
+    const int b0 = cta_of(sl, x0), b1 = cta_of(sl, x0 + sl.nchunk - 1);
+    const int first = mode == kCarryLater ? b + 1 : b0, last = mode == kCarryEarlier ? b - 1 : b1;
+    float acc[64];
+#pragma unroll
+    for (int q = 0; q < 64; ++q) acc[q] = 0.f;
+    float vsum = 0.f;
 #pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
+    for (int bb = first; bb <= last; ++bb) {
+        const float *slot = slots + slot_of(h, bb) * stride;
         const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
         float4 v4[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) v4[q] = src[q];
-        const float *acc = (const float *)v4;
+        vsum += slot[(size_t)D * D + hf * D + d];
 #pragma unroll
-        for (int half32 = 0; half32 < 2; ++half32) {
-            const float *a32 = acc + 32 * half32;
-            if (to_tmem) {
-                uint32_t r[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(a32[j]);
-                tmem_st32(tS + 64 * hf + 32 * half32, r);
-            }
-            unsigned char *tile = Sb + hf * kBox;
-#pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-                uint4 w;
-                w.x = pack_bf16(a32[8 * g4 + 0], a32[8 * g4 + 1]);
-                w.y = pack_bf16(a32[8 * g4 + 2], a32[8 * g4 + 3]);
-                w.z = pack_bf16(a32[8 * g4 + 4], a32[8 * g4 + 5]);
-                w.w = pack_bf16(a32[8 * g4 + 6], a32[8 * g4 + 7]);
-                *(uint4 *)(tile + sw128_off(d, 4 * half32 + g4)) = w;
-            }
+        for (int q = 0; q < 16; ++q) {
+            acc[4 * q] += v4[q].x;
+            acc[4 * q + 1] += v4[q].y;
+            acc[4 * q + 2] += v4[q].z;
+            acc[4 * q + 3] += v4[q].w;
         }
     }
-    zc[d] = zv;
-    ac[d] = av;
-    if (to_tmem) tmem_st_wait();
-}
-
-// Half `hf` of the carried state `slot` ([S row-major | z | a], fp32) for row d: columns [64 hf, 64 hf + 64)
-// of S into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes z[d]
-// to zc (and TMEM column tZ if to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and TMEM column tA).  All loads are issued
-// before any is used.
-__device__ __forceinline__ void load_carry_half(const float *slot, int d, int hf, uint32_t tS, uint32_t tZ,
-                                                uint32_t tA, unsigned char *Sb, float *zc, float *ac, bool to_tmem,
-                                                bool vec_to_tmem = true) {
-    constexpr int D = 128;
-    const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
-    float4 v4[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) v4[q] = src[q];
-    const float vsum = slot[(size_t)D * D + hf * D + d];
-    const float *acc = (const float *)v4;
 #pragma unroll
     for (int half32 = 0; half32 < 2; ++half32) {
         const float *a32 = acc + 32 * half32;

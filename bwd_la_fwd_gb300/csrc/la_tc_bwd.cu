@@ -313,6 +313,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     // column sums of the chunk (N = 16 each; column 0 of each holds the sum, column 1 of cY the dt remainder),
@@ -618,6 +622,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256, R3 = tmem + 384;
     const uint32_t cY = R2, cE = R2 + 16;  // piece sums y (columns 0, 1: two parts) and e (column 0)
@@ -825,6 +833,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     const uint32_t cY = R2, cE = R2 + 16;  // the chunk's y (columns 0, 1: two parts) and e (column 0)
@@ -1090,6 +1102,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256;
 
@@ -1257,16 +1273,12 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dV = dV;
     const unsigned nthr = 64 + tc::kEpiThreads;
     cudaError_t e = tc_host::launch_agg(P, s);
-    if (e != cudaSuccess) return e;
-    if (p.causal)
-        tc::tc_bwd_dq_kernel<<<P.sl.G, nthr, kSmemDq, s>>>(P);
-    else
-        tc::tc_bwd_dq_nc_kernel<<<P.sl.G, nthr, kSmemDqNc, s>>>(P);
-    if (p.causal)
-        tc::tc_bwd_dkdv_kernel<<<P.sl.G, nthr, kSmemDkdv, s>>>(P);
-    else
-        tc::tc_bwd_dkdv_nc_kernel<<<P.sl.G, nthr, kSmemDkdvNc, s>>>(P);
-    e = cudaGetLastError();
+    if (e == cudaSuccess)
+        e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dq_kernel, P.sl.G, nthr, kSmemDq, s, P)
+                     : tc_host::launch_tc(tc::tc_bwd_dq_nc_kernel, P.sl.G, nthr, kSmemDqNc, s, P);
+    if (e == cudaSuccess)
+        e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dkdv_kernel, P.sl.G, nthr, kSmemDkdv, s, P)
+                     : tc_host::launch_tc(tc::tc_bwd_dkdv_nc_kernel, P.sl.G, nthr, kSmemDkdvNc, s, P);
     if (e == cudaSuccess) count_launches(3);
     return e;
 }

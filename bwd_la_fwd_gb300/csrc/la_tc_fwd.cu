@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
 
     if (warp == 0 && lane == 0) {
@@ -228,6 +232,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Everything above touches only this CTA's shared memory and TMEM; every global access comes after
+    // the previous kernel of the stream has completed.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t tT = tmem, tS = tmem + 256, tZ = tmem + 384, tA = tmem + 400;
     const uint32_t tX = tmem + (CAUSAL ? 416 : 256);
@@ -551,10 +559,25 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     return true;
 }
 
+cudaError_t launch_tc(void (*kernel)(const tc::TcParams), unsigned grid, unsigned block, size_t smem,
+                      cudaStream_t s, const tc::TcParams &P) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
     if (!set_smem_attrs()) return cudaErrorInvalidValue;
-    tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
-    return cudaGetLastError();
+    return launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
 }
 
 }  // namespace tc_host
@@ -575,12 +598,10 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
         return cudaErrorInvalidValue;
     P.O = O;
     P.g = g;
-    tc::tc_agg_kernel<<<P.sl.G, 192, kSmemAgg, s>>>(P);
-    if (p.causal)
-        tc::tc_fwd_kernel<true><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s>>>(P);
-    else
-        tc::tc_fwd_kernel<false><<<P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s>>>(P);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
+    if (e == cudaSuccess)
+        e = p.causal ? launch_tc(tc::tc_fwd_kernel<true>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s, P)
+                     : launch_tc(tc::tc_fwd_kernel<false>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s, P);
     if (e == cudaSuccess) count_launches(2);
     return e;
 }

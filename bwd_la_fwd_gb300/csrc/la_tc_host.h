@@ -34,6 +34,10 @@ namespace tc_host {
 bool make_map(CUtensorMap *m, const void *ptr, const Plan &p);
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
+// Launches a tensor-core kernel as a programmatic dependent of the previous kernel in the stream (the
+// kernels order their global accesses after griddepcontrol.wait, so stream order is kept).
+cudaError_t launch_tc(void (*kernel)(const tc::TcParams), unsigned grid, unsigned block, size_t smem,
+                      cudaStream_t s, const tc::TcParams &P);
 }  // namespace tc_host
 
 // bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.

@@ -42,6 +42,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 def config_dict():
     return {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "passes_per_step": list(PASSES),
             "tokens_per_step": 2 * B * N, "l2": "inputs larger than L2 (4 x 67 MB per step), no flush",
+            "backward": "la_backward_with_forward_state: per-piece K^T V sums taken from the forward's workspace",
             "seed": 1}
 
 
@@ -229,7 +230,10 @@ def run_ours(args):
             if evs is not None:
                 evs[p + "_fwd"][1].record(stream)
                 evs[p + "_bwd"][0].record(stream)
-            la.la_backward(Q, K, V, o["O"], dO, causal, dQ=o["dQ"], dK=o["dK"], dV=o["dV"], workspace=ws)
+            # the backward takes the per-piece state sums the forward just left in `ws` (a training step's
+            # saved activations), as la_backward_with_forward_state allows
+            la.la_backward(Q, K, V, o["O"], dO, causal, dQ=o["dQ"], dK=o["dK"], dV=o["dV"], workspace=ws,
+                           reuse_forward_state=True)
             if evs is not None:
                 evs[p + "_bwd"][1].record(stream)
 

@@ -83,6 +83,12 @@ bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 Range range_of(const void *ptr, size_t bytes) { return Range{(uintptr_t)ptr, (uintptr_t)ptr + bytes}; }
 
+// The SIMT path leaves no tensor-core state sums in the workspace: clear the tag that names them.
+cudaError_t clear_state_tag(void *ws, cudaStream_t s) {
+    return cudaMemsetAsync((unsigned char *)ws + offsetof(la::WsHeader, state_tag), 0,
+                           sizeof(((la::WsHeader *)nullptr)->state_tag), s);
+}
+
 int check_workspace(const Plan &p, void *ws, size_t ws_bytes, bool backward) {
     if (!ws || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
     if (ws_bytes < (backward ? p.bytes_bwd : p.bytes_fwd)) return LA_ERR_WORKSPACE;
@@ -117,6 +123,7 @@ const char *la_status_string(int status) {
         case LA_ERR_CUDA: return "LA_ERR_CUDA";
         case LA_ERR_TIMEOUT: return "LA_ERR_TIMEOUT";
         case LA_ERR_BOUNDS: return "LA_ERR_BOUNDS";
+        case LA_ERR_STATE: return "LA_ERR_STATE";
         default: return "LA_UNKNOWN_STATUS";
     }
 }
@@ -145,13 +152,14 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
     if ((rc = check_aliasing(outs, normaliser ? 2 : 1, ins, 4))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s)
-                             : la::simt_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s);
+                             : clear_state_tag(workspace, s);
+    if (e == cudaSuccess && !p.use_tc) e = la::simt_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
-int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
-                void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
-                size_t workspace_bytes, void *stream) {
+static int backward_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ,
+                         void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
+                         size_t workspace_bytes, void *stream, bool reuse_fwd_state) {
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || D < 1) return LA_ERR_INVALID_ARG;
     if (!la::supported_d(D)) return LA_ERR_UNSUPPORTED;
@@ -168,9 +176,26 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
     const Range outs[] = {range_of(dQ, tb), range_of(dK, tb), range_of(dV, tb)};
     if ((rc = check_aliasing(outs, 3, ins, 6))) return rc;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = p.use_tc ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, (unsigned char *)workspace, s)
-                             : la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, (unsigned char *)workspace, s);
+    cudaError_t e = p.use_tc
+                        ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, (unsigned char *)workspace, s, reuse_fwd_state)
+                        : clear_state_tag(workspace, s);
+    if (e == cudaSuccess && !p.use_tc)
+        e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, (unsigned char *)workspace, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
+int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
+                void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
+                size_t workspace_bytes, void *stream) {
+    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, workspace, workspace_bytes, stream,
+                         false);
+}
+
+int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                   void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, workspace, workspace_bytes, stream,
+                         true);
 }
 
 int la_get_status(void *workspace, void *stream) {

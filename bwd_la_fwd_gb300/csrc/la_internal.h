@@ -8,7 +8,7 @@
 namespace la {
 
 // Device status codes written into the workspace's sticky status word (same values as la_status).
-enum : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBounds = 6 };
+enum : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBounds = 6, kDevState = 7 };
 
 // Workspace header: the first 256 bytes of every workspace.
 struct WsHeader {
@@ -17,8 +17,10 @@ struct WsHeader {
     uint32_t ticket[8];   // per-kernel ticket counters (reset by the last block of each launch)
     uint32_t done[8];     // per-kernel completion counters
     uint32_t epoch[8];    // per-kernel launch epochs (flags compare against these)
+    uint64_t state_tag[6]; // which K, V and slicing the per-piece state sums belong to (tensor-core path)
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
+static_assert(offsetof(WsHeader, state_tag) == 128, "the state tag sits 128 bytes into the header");
 
 // How one call splits each head's N rows into segments whose D x D states are carried in the
 // workspace.  Chosen on the host from (N, D) only, so la_workspace_bytes and the launch agree.

@@ -317,13 +317,23 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
+        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+            *abort_flag = 1;
+            report(P.status, kDevState, 0x5A7Eu);
+        }
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     // column sums of the chunk (N = 16 each; column 0 of each holds the sum, column 1 of cY the dt remainder),
     // in the R1 columns that U' (R1 + [0, 32) and R1 + [64, 96)) leaves free
     const uint32_t cZ = R1 + 32, cA = R1 + 48, cY = R1 + 96, cE = R1 + 112;
 
-    if (warp == 0 && lane == 0) {
+    if (skip) {
+        // the state this call relies on is not in the workspace: nothing to compute
+    } else if (warp == 0 && lane == 0) {
         // ---- TMA producer
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
@@ -626,11 +636,21 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
+        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+            *abort_flag = 1;
+            report(P.status, kDevState, 0x5A7Eu);
+        }
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256, R3 = tmem + 384;
     const uint32_t cY = R2, cE = R2 + 16;  // piece sums y (columns 0, 1: two parts) and e (column 0)
 
-    if (warp == 0 && lane == 0) {
+    if (skip) {
+        // the state this call relies on is not in the workspace: nothing to compute
+    } else if (warp == 0 && lane == 0) {
         // ---- TMA producer
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
@@ -837,11 +857,21 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
+        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+            *abort_flag = 1;
+            report(P.status, kDevState, 0x5A7Eu);
+        }
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     const uint32_t cY = R2, cE = R2 + 16;  // the chunk's y (columns 0, 1: two parts) and e (column 0)
 
-    if (warp == 0 && lane == 0) {
+    if (skip) {
+        // the state this call relies on is not in the workspace: nothing to compute
+    } else if (warp == 0 && lane == 0) {
         // ---- TMA producer (chunks of each piece in reverse order)
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
@@ -1106,10 +1136,20 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
+        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+            *abort_flag = 1;
+            report(P.status, kDevState, 0x5A7Eu);
+        }
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256;
 
-    if (warp == 0 && lane == 0) {
+    if (skip) {
+        // the state this call relies on is not in the workspace: nothing to compute
+    } else if (warp == 0 && lane == 0) {
         // ---- TMA producer (chunks of each piece in reverse order)
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
@@ -1256,7 +1296,7 @@ bool set_bwd_attrs() {
 }  // namespace
 
 cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
-                        void *dK, void *dV, unsigned char *ws, cudaStream_t s) {
+                        void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state) {
     if (!set_bwd_attrs()) return cudaErrorInvalidValue;
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
@@ -1271,15 +1311,18 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dQ = dQ;
     P.dK = dK;
     P.dV = dV;
+    P.Kp = K;
+    P.Vp = V;
+    P.check_tag = reuse_fwd_state ? 1 : 0;
     const unsigned nthr = 64 + tc::kEpiThreads;
-    cudaError_t e = tc_host::launch_agg(P, s);
+    cudaError_t e = reuse_fwd_state ? cudaSuccess : tc_host::launch_agg(P, s);
     if (e == cudaSuccess)
         e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dq_kernel, P.sl.G, nthr, kSmemDq, s, P)
                      : tc_host::launch_tc(tc::tc_bwd_dq_nc_kernel, P.sl.G, nthr, kSmemDqNc, s, P);
     if (e == cudaSuccess)
         e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dkdv_kernel, P.sl.G, nthr, kSmemDkdv, s, P)
                      : tc_host::launch_tc(tc::tc_bwd_dkdv_nc_kernel, P.sl.G, nthr, kSmemDkdvNc, s, P);
-    if (e == cudaSuccess) count_launches(3);
+    if (e == cudaSuccess) count_launches(reuse_fwd_state ? 2 : 3);
     return e;
 }
 

@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
+    if (blockIdx.x == 0 && threadIdx.x == 0) write_state_tag(P);  // the slots below belong to P.Kp, P.Vp
     const uint32_t tmem = *tslot;
 
     if (warp == 0 && lane == 0) {
@@ -598,6 +599,8 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
         return cudaErrorInvalidValue;
     P.O = O;
     P.g = g;
+    P.Kp = K;
+    P.Vp = V;
     cudaError_t e = launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
     if (e == cudaSuccess)
         e = p.causal ? launch_tc(tc::tc_fwd_kernel<true>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s, P)

@@ -25,7 +25,39 @@ struct TcParams {
     float *g;               // forward normaliser (may be null)
     void *dQ, *dK, *dV;     // backward outputs (bf16)
     float *rs_g, *rs_dt;    // backward row statistics: g_i and delta_i / g_i
+    const void *Kp, *Vp;    // K and V: with the shape they identify the per-piece sums in the workspace
+    int check_tag;          // backward reusing the forward's sums: check the workspace tag first
 };
+
+// The per-piece sums kernel records in the workspace header which K, V and slicing the slots hold; a
+// backward that reuses them instead of recomputing them checks the record first (state_tag_matches).
+constexpr size_t kTagOffset = 128;  // bytes into the workspace header
+static_assert(kTagOffset == offsetof(WsHeader, state_tag), "tag offset");
+constexpr int kTagWords = 6;
+__host__ __device__ inline void state_tag(const TcParams &P, uint64_t *t) {
+    t[0] = 0x4C415F5354415445ull;  // marker ("LA_STATE")
+    t[1] = (uint64_t)(uintptr_t)P.Kp;
+    t[2] = (uint64_t)(uintptr_t)P.Vp;
+    t[3] = (uint64_t)P.sl.T;
+    t[4] = (uint64_t)P.N;
+    t[5] = (uint64_t)P.sl.G;
+}
+#ifdef __CUDACC__
+__device__ inline void write_state_tag(const TcParams &P) {
+    uint64_t t[kTagWords];
+    state_tag(P, t);
+    volatile uint64_t *w = (volatile uint64_t *)((unsigned char *)P.status + kTagOffset);
+    for (int k = 0; k < kTagWords; ++k) w[k] = t[k];
+}
+__device__ inline bool state_tag_matches(const TcParams &P) {
+    uint64_t t[kTagWords];
+    state_tag(P, t);
+    const volatile uint64_t *w = (const volatile uint64_t *)((const unsigned char *)P.status + kTagOffset);
+    bool ok = true;
+    for (int k = 0; k < kTagWords; ++k) ok = ok && w[k] == t[k];
+    return ok;
+}
+#endif
 
 }  // namespace tc
 
@@ -46,7 +78,9 @@ bool tc_supported(const Plan &p);
 size_t tc_slot_bytes(const Plan &p);
 cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
                        unsigned char *ws, cudaStream_t s);
+// reuse_fwd_state: take the per-piece K^T V sums the forward left in the workspace (tag checked on the
+// device, LA_ERR_STATE when it does not match) instead of recomputing them.
 cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
-                        void *dK, void *dV, unsigned char *ws, cudaStream_t s);
+                        void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state);
 
 }  // namespace la

@@ -19,7 +19,7 @@ _lock = threading.Lock()
 _lib = None
 
 _STATUS = {0: "LA_OK", 1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_WORKSPACE", 4: "LA_ERR_CUDA",
-           5: "LA_ERR_TIMEOUT", 6: "LA_ERR_BOUNDS"}
+           5: "LA_ERR_TIMEOUT", 6: "LA_ERR_BOUNDS", 7: "LA_ERR_STATE"}
 
 
 class LAError(RuntimeError):
@@ -56,6 +56,8 @@ def load_library():
         lib.la_forward.restype = i
         lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
         lib.la_backward.restype = i
+        lib.la_backward_with_forward_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+        lib.la_backward_with_forward_state.restype = i
         lib.la_get_status.argtypes = [vp, vp]
         lib.la_get_status.restype = i
         _lib = lib
@@ -141,8 +143,13 @@ def la_forward(Q, K, V, causal: bool, O=None, normaliser=None, workspace=None, s
     return O, normaliser
 
 
-def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspace=None, stream=None):
-    """dQ, dK, dV = la_backward(Q, K, V, O, dO, causal): gradients of sum(dO * O)."""
+def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspace=None, stream=None,
+                reuse_forward_state: bool = False):
+    """dQ, dK, dV = la_backward(Q, K, V, O, dO, causal): gradients of sum(dO * O).
+
+    With ``reuse_forward_state`` the call is la_backward_with_forward_state: it takes the per-piece state
+    sums that the last la_forward on ``workspace`` (same K, V, shape) left there instead of recomputing
+    them; the workspace must then be given (and sized for the backward at that forward)."""
     import torch
     B, H, N, D = _shape(Q)
     _check_like(Q, K, V, O, dO, dQ, dK, dV)
@@ -151,12 +158,15 @@ def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspa
     dK = torch.empty_like(Q) if dK is None else dK
     dV = torch.empty_like(Q) if dV is None else dV
     if workspace is None:
+        if reuse_forward_state:
+            raise ValueError("reuse_forward_state needs the workspace the forward ran with")
         workspace = new_workspace(B, H, N, D, causal, dt, True, Q.device)
-    st = load_library().la_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV),
-                                    int(bool(causal)), B, H, N, D, dt, _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    lib = load_library()
+    fn = lib.la_backward_with_forward_state if reuse_forward_state else lib.la_backward
+    st = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), int(bool(causal)), B, H, N, D,
+            dt, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != 0:
-        raise LAError(st, "la_backward")
+        raise LAError(st, "la_backward_with_forward_state" if reuse_forward_state else "la_backward")
     return dQ, dK, dV
 
 

@@ -51,7 +51,8 @@ typedef enum {
     LA_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than la_workspace_bytes() */
     LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     LA_ERR_TIMEOUT = 5,     /* device: a bounded inter-block wait gave up (reported by la_get_status) */
-    LA_ERR_BOUNDS = 6       /* device: an internal index check failed (reported by la_get_status) */
+    LA_ERR_BOUNDS = 6,      /* device: an internal index check failed (reported by la_get_status) */
+    LA_ERR_STATE = 7        /* device: la_backward_with_forward_state found no matching forward state */
 } la_status;
 
 typedef enum { LA_F32 = 0, LA_BF16 = 1 } la_dtype;
@@ -102,6 +103,22 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
                 size_t workspace_bytes, void *stream);
 
 /*
+ * Backward pass that reuses what the forward computed.  The forward's first kernel sums k_j v_j^T, k_j
+ * and v_j over each piece of rows (the tensor-core path's work split), and both passes need exactly those
+ * sums; la_backward recomputes them, this entry point takes them from `workspace` instead, the way an
+ * autograd backward takes tensors saved by its forward.  Arguments, checks and results are those of
+ * la_backward, with one more condition: the last call that computed state sums in this workspace must
+ * have been la_forward or la_backward on the same K and V buffers (same pointers, unchanged contents) and
+ * the same B, H, N, D and dtype.  The workspace records which K, V and shape its sums belong to; when the
+ * record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.  Unchanged
+ * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or D != 128)
+ * there are no such sums to reuse and this call is la_backward.
+ */
+int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                                   void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Forward pass without a caller-supplied workspace, for callers that cannot allocate device memory (a
  * plugin that its host framework gives only input and output buffers, code that must not call cudaMalloc
  * because it can block and synchronise the device, a fixed memory budget).  The paper has no counterpart:
@@ -120,7 +137,8 @@ int la_forward_noalloc(const void *Q, const void *K, const void *V, int causal, 
 
 /*
  * Synchronises `stream`, then returns and clears the sticky device status recorded in `workspace`
- * by earlier calls (LA_OK, LA_ERR_TIMEOUT or LA_ERR_BOUNDS), or LA_ERR_CUDA if the stream failed.
+ * by earlier calls (LA_OK, LA_ERR_TIMEOUT, LA_ERR_BOUNDS or LA_ERR_STATE), or LA_ERR_CUDA if the stream
+ * failed.
  */
 int la_get_status(void *workspace, void *stream);
 

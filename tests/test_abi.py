@@ -39,7 +39,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_version_and_status_strings(lib):
     assert lib.la_version() >= 100
     for code, name in [(0, "LA_OK"), (1, "LA_ERR_INVALID_ARG"), (2, "LA_ERR_UNSUPPORTED"),
-                       (3, "LA_ERR_WORKSPACE"), (4, "LA_ERR_CUDA"), (5, "LA_ERR_TIMEOUT"), (6, "LA_ERR_BOUNDS")]:
+                       (3, "LA_ERR_WORKSPACE"), (4, "LA_ERR_CUDA"), (5, "LA_ERR_TIMEOUT"), (6, "LA_ERR_BOUNDS"),
+                       (7, "LA_ERR_STATE")]:
         assert lib.la_status_string(code).decode() == name
     assert lib.la_status_string(99).decode() == "LA_UNKNOWN_STATUS"
 
@@ -82,12 +83,14 @@ def test_forward_rejects_bad_arguments_on_host(lib):
     assert _fwd(lib, g=0x6000_0000 + 64) == 1         # normaliser inside O
 
 
-def test_backward_rejects_bad_arguments_on_host(lib):
+@pytest.mark.parametrize("entry", ["la_backward", "la_backward_with_forward_state"])
+def test_backward_rejects_bad_arguments_on_host(lib, entry):
     vp = ctypes.c_void_p
     base = [0x1000_0000 * (i + 1) for i in range(8)]
+    fn = getattr(lib, entry)
 
     def call(ptrs=base, D=64, ws=0xA000_0000, wsb=1 << 30):
-        return lib.la_backward(*[vp(p) for p in ptrs], 1, 1, 2, 16, D, 1, vp(ws), wsb, vp(0))
+        return fn(*[vp(p) for p in ptrs], 1, 1, 2, 16, D, 1, vp(ws), wsb, vp(0))
 
     assert call(D=24) == 2
     bad = list(base)

@@ -1,0 +1,111 @@
+"""la_backward_with_forward_state: the backward that takes the per-piece state sums from the forward.
+
+The forward's first kernel sums k_j v_j^T, k_j and v_j over each piece of rows; the backward needs the
+same sums.  The reusing entry point must give exactly what la_backward gives (the sums are the same
+numbers, so the gradients are bit-identical), must refuse (LA_ERR_STATE, nothing computed) when the
+workspace holds sums of other K, V or of another work split, and is plain la_backward on the SIMT path.
+"""
+import pytest
+
+import la_testutil as U
+from bwd_la_fwd_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+LA_ERR_STATE = 7
+
+
+def _tensors(B, H, N, D, dtype, seed):
+    x = inputs.generate(B, H, N, D, seed=seed, dtype=dtype)
+    return x, {n: U.to_device(x[n], dtype) for n in ("Q", "K", "V", "dO")}
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_reuse_is_bit_identical_to_la_backward(causal, dtype, D):
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N = 2, 3, 777
+    _, t = _tensors(B, H, N, D, dtype, seed=71)
+    code = la.LA_BF16 if dtype == "bf16" else la.LA_F32
+    ws = la.new_workspace(B, H, N, D, causal, code, True)
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], causal, workspace=ws)
+    got = la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], causal, workspace=ws, reuse_forward_state=True)
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    ref = la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], causal)
+    torch.cuda.synchronize()
+    for a, r in zip(got, ref):
+        assert torch.equal(a, r)
+
+
+def test_reuse_matches_the_oracle(oracle_lib):
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D, causal = 1, 2, 300, 128, 1
+    x, t = _tensors(B, H, N, D, "bf16", seed=72)
+    ws = la.new_workspace(B, H, N, D, causal, la.LA_BF16, True)
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], causal, workspace=ws)
+    dQ, dK, dV = la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], causal, workspace=ws, reuse_forward_state=True)
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    f = U.stored_to_f64(x, "bf16")
+    r = oracle_lib.backward(f["Q"], f["K"], f["V"], f["dO"], True)
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dQ, dK, dV), r):
+        U.assert_close(name, U.to_f64(got), ref, "bf16")
+
+
+def test_reuse_without_a_forward_reports_state_error():
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 2, 513, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=73)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)  # zero-filled: no state recorded
+    dQ = torch.full_like(t["Q"], 7.0)
+    la.la_backward(t["Q"], t["K"], t["V"], t["Q"], t["dO"], True, dQ=dQ, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+    assert bool((dQ == 7.0).all())  # nothing was computed
+    assert la.la_get_status(ws) == 0  # the status is cleared once read
+
+
+def test_reuse_after_a_forward_on_other_keys_reports_state_error():
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 2, 513, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=74)
+    K2 = t["K"].clone()
+    ws = la.new_workspace(B, H, N, D, 0, la.LA_BF16, True)
+    O, _ = la.la_forward(t["Q"], K2, t["V"], False, workspace=ws)
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], False, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+
+
+def test_reuse_with_another_work_split_reports_state_error(monkeypatch):
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 3, 1000, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=75)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)
+    monkeypatch.setenv("LA_TC_MAX_CTAS", "5")
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], True, workspace=ws)
+    monkeypatch.delenv("LA_TC_MAX_CTAS")
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+
+
+def test_simt_call_on_the_workspace_clears_the_record():
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 2, 513, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=76)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], True, workspace=ws)
+    # an fp32 call (SIMT kernels, another layout of the same workspace bytes) in between
+    small = {n: torch.randn(1, 1, 64, 64, device="cuda") for n in ("Q", "K", "V")}
+    assert la.la_workspace_bytes(1, 1, 64, 64, True, la.LA_F32, False) <= ws.numel()
+    la.la_forward(small["Q"], small["K"], small["V"], True, workspace=ws)
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+    # a fresh forward records the state again
+    la.la_forward(t["Q"], t["K"], t["V"], True, O=O, workspace=ws)
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == 0

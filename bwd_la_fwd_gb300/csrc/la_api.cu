@@ -51,8 +51,10 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
         p->off_states2 = round_up(p->off_states + slots, 256);
         p->off_flags = round_up(p->off_states2 + slots, 256);
         p->off_rowstats = p->off_flags;
+        p->off_chunkye = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
+        const size_t nchunk = ((size_t)N + 127) / 128;
         p->bytes_fwd = p->off_states2;
-        p->bytes_bwd = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
+        p->bytes_bwd = round_up(p->off_chunkye + (size_t)BH * nchunk * 256 * sizeof(float), 256);
         return true;
     }
     const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;

@@ -237,14 +237,17 @@ __device__ __forceinline__ bool next_rev_chunk(const PieceIter &pi, const Piece 
     return true;
 }
 
-// g and dt of row j of chunk c of head h, from the dQ walk's row statistics (0 past the end of the head).
-// Loads only: the values are used one chunk later.
-__device__ __forceinline__ void load_row_stats(const TcParams &P, long long h, int c, int j, float *g, float *dt) {
+// g_j and dt_j of row j of chunk c of head h, from the dQ walk's row statistics (0 past the end of the
+// head), and component j of that chunk's column sum y_c (hf 0) or e_c (hf 1).  Loads only: the values are
+// used one chunk later.
+__device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h, int c, int j, int hf, float *g,
+                                                 float *dt, float *ye) {
     const long long r = (long long)c * kC + j;
     const bool in = r < P.N;
     const size_t x = (size_t)h * P.N + (in ? r : 0);
     *g = in ? P.rs_g[x] : 0.f;
     *dt = in ? P.rs_dt[x] : 0.f;
+    *ye = P.chunk_ye[((size_t)h * P.sl.nchunk + c) * 256 + hf * 128 + j];
 }
 
 // Issues the TMA stores of a two-box output tile from shared memory and commits them.  One thread.
@@ -289,8 +292,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     uint64_t *empty = full + 1;
     uint64_t *bar = empty + 1;
     uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barU = bar + 4, *barDt = bar + 5,
-             *barX = bar + 6, *barR = bar + 7, *barPPf = bar + 8;
-    uint32_t *tslot = (uint32_t *)(bar + 9);
+             *barX = bar + 6, *barR = bar + 7, *barPPf = bar + 8, *barC = bar + 9;
+    uint32_t *tslot = (uint32_t *)(bar + 10);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
@@ -298,8 +301,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     if (threadIdx.x == 0) {
         mbar_init(full, 1);
         mbar_init(empty, 1);  // the chunk's last MMA commit: every epilogue read of the stage precedes barDt
-        const uint32_t counts[9] = {1, E, E, 1, E, E, 1, E, E};
-        for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
+        const uint32_t counts[10] = {1, E, E, 1, E, E, 1, E, E, 1};
+        for (int k = 0; k < 10; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -420,6 +423,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     mma_ss(cZ, sdesc_sw128(kb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
                     mma_ss(cA, sdesc_sw128(vb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
                 }
+                mma_commit(barX);
                 ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x309);  // dO / g in place, dt_i in dtt
                 if (!ok) break;
                 if (c == pc.a && pno > 0) ok = wait_or_abort(barPPf, (pno - 1) & 1, abort_flag, P.status, 0x303);
@@ -433,7 +437,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     mma_ss(cY, qa, sdesc_sw128(dtb + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idZ, k > 0);
                     mma_ss(cE, oa, sdesc_sw128(on + 32 * (k & 3), 16, 0), idZ, k > 0);
                 }
-                mma_commit(barX);
+                mma_commit(barC);
                 mma_commit(empty);
             }
         }
@@ -526,17 +530,17 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 fence_proxy_async_smem();
                 mbar_arrive(barDt);
                 // dQ_i = X_i / g_i - dt_i z (X = Y + U' K), and the chunk's column sums
-                ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);
+                ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);  // X = Y + U' K, z_c, a_c
                 if (!ok) break;
                 tc_fence_after();
                 tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
-                uint32_t s0, s1, s2, s3;
-                tmem_ld2(hf == 0 ? cZ + lo : cY + lo, s0, s1);  // half 0: z_c, -; half 1: y_c (two parts)
-                tmem_ld2(hf == 0 ? cA + lo : cE + lo, s2, s3);  // half 0: a_c, -; half 1: e_c, -
-                tmem_wait_ld(s0, s1);
-                tmem_wait_ld(s2, s3);
-                tc_fence_before();
-                mbar_arrive(barR);
+                uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+                if (hf == 0) {  // z_c, a_c (component i)
+                    tmem_ld2(cZ + lo, s0, s1);
+                    tmem_ld2(cA + lo, s2, s3);
+                    tmem_wait_ld(s0, s1);
+                    tmem_wait_ld(s2, s3);
+                }
                 fence_proxy_async_smem();
                 epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
                 if (u == 0) store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
@@ -549,14 +553,28 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 if (hf == 0) {  // z and a after this chunk
                     zc[i] += __uint_as_float(s0);
                     ac[i] += __uint_as_float(s2);
-                } else {
-                    yacc += __uint_as_float(s0) + __uint_as_float(s1);
-                    eacc += __uint_as_float(s2);
                 }
+                ok = wait_or_abort(barC, ph, abort_flag, P.status, 0x30D);  // Ppiece, y_c, e_c
+                if (!ok) break;
+                tc_fence_after();
+                if (hf == 1) {  // y_c, e_c (component i): into the piece sums, and kept per chunk for the dK / dV walk
+                    tmem_ld2(cY + lo, s0, s1);
+                    tmem_ld2(cE + lo, s2, s3);
+                    tmem_wait_ld(s0, s1);
+                    tmem_wait_ld(s2, s3);
+                    const float yv = __uint_as_float(s0) + __uint_as_float(s1), ev = __uint_as_float(s2);
+                    float *cye = P.chunk_ye + ((size_t)pc.h * P.sl.nchunk + c) * 256;
+                    cye[i] = yv;
+                    cye[128 + i] = ev;
+                    yacc += yv;
+                    eacc += ev;
+                }
+                tc_fence_before();
+                mbar_arrive(barR);
                 epi_sync256();
             }
             if (!ok) break;
-            piece_rev_sums(P, pc, R3 + lo, i, hf, yacc, eacc);  // Ppiece is complete (last barX)
+            piece_rev_sums(P, pc, R3 + lo, i, hf, yacc, eacc);  // Ppiece is complete (last barC)
             tc_fence_before();
             mbar_arrive(barPPf);
         }
@@ -799,15 +817,16 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
 
 // ----------------------------------------------------------------------------------------------------
 // dK / dV walk (reverse chunk order), causal, with lane = key row j of the chunk.  Per chunk:
-//   the epilogue first rewrites dO as dOt = dO / g in place (g_i and dt_i are the dQ walk's row
-//   statistics, loaded one chunk ahead); T^T = K Q^T (R0) and Wt^T = V dOt^T (R1);
-//   P^T = [i >= j](1 + T^T) and U^T = [i >= j](Wt^T - dt_i), both bf16, into R0 (per 64 rows i: P^T in
-//   the first 32 columns of the 64, U^T in the next 32);
-//   dK = U^T Q + V Pb^T (R2, then - y) and dV = P^T dOt + K Pb (R1, then + e);
-//   P += Q^T dOt (R3: the sum over later rows, for the earlier chunks), and the chunk's column sums
-//   y_c = Q^T dt, e_c = dOt^T 1 (N = 16 MMAs into R2 once dK has been drained).
-// Pb is the bf16 copy of P.  dK leaves through the V tile, dV through its own staging tile.  One TMA stage
-// (Q, dO, K, V); the next chunk's tiles are prefetched into L2 meanwhile.
+//   the epilogue first rewrites dO as dOt = dO / g in place (g_i, dt_i and the chunk's column sums
+//   y_c, e_c come from the dQ walk and are loaded one chunk ahead); T^T = K Q^T (R0) and
+//   Wt^T = V dOt^T (R1); P^T = [i >= j](1 + T^T) as soon as T^T is in, and U^T = [i >= j](Wt^T - dt_i)
+//   once Wt^T is, both bf16 into R0 (per 64 rows i: P^T in the first 32 columns of the 64, U^T in the
+//   next 32); dV = P^T dOt + K Pb (R2, then + e) while U^T is formed, then dK = U^T Q + V Pb^T (R1,
+//   over the consumed Wt^T, then - y); P += Q^T dOt (R3: the sum over later rows, for the earlier
+//   chunks); then y += y_c, e += e_c.
+// Pb is the bf16 copy of P.  dK and dV leave through staging tiles of their own, so the stage is released
+// as soon as dK, the last MMA reading it, is done.  One TMA stage (Q, dO, K, V); the next chunk's tiles
+// are prefetched into L2 meanwhile.
 // ----------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
@@ -819,17 +838,16 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
     unsigned char *stage = sm;
     unsigned char *Pb = sm + STAGE;
-    unsigned char *dvt = Pb + TB;      // dV staging tile
-    unsigned char *ones = dvt + TB;    // 8 rows x 128 B of bf16 1.0
-    unsigned char *dtt = ones + 1024;  // dt_i of the chunk's rows as an N = 16 operand (dt_tile_put)
-    float *yc = (float *)(dtt + 2048); // y over the later rows (fp32, D)
-    float *ec = yc + D;                // e over the later rows
-    float *sDt = ec + D;               // dt_i of the chunk's rows
+    unsigned char *dvt = Pb + TB;     // dV staging tile
+    unsigned char *dkt = dvt + TB;    // dK staging tile
+    float *yc = (float *)(dkt + TB);  // y over the later rows (fp32, D)
+    float *ec = yc + D;               // e over the later rows
+    float *sDt = ec + D;              // dt_i of the chunk's rows
     uint64_t *full = (uint64_t *)(sDt + kC);
     uint64_t *empty = full + 1;
     uint64_t *bar = empty + 1;
-    uint64_t *barO = bar, *barT = bar + 1, *barP = bar + 2, *barPb = bar + 3, *barK = bar + 4, *barV = bar + 5,
-             *barKf = bar + 6, *barC = bar + 7, *barR = bar + 8;
+    uint64_t *barO = bar, *barT1 = bar + 1, *barT2 = bar + 2, *barP1 = bar + 3, *barP2 = bar + 4, *barPb = bar + 5,
+             *barK = bar + 6, *barV = bar + 7, *barR = bar + 8;
     uint32_t *tslot = (uint32_t *)(bar + 9);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
@@ -837,15 +855,12 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(full, 1);
-        mbar_init(empty, 2);  // the chunk's last MMA commit + the epilogue once dK has left the V tile
-        const uint32_t counts[9] = {E, 1, E, E, 1, 1, E, 1, E};
+        mbar_init(empty, 1);  // the chunk's last MMA commit (every epilogue read of the stage precedes barO)
+        const uint32_t counts[9] = {E, 1, 1, E, E, E, 1, 1, E};
         for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
-    for (int k = threadIdx.x; k < 512; k += blockDim.x) ((uint32_t *)dtt)[k] = 0u;
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -867,7 +882,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
-    const uint32_t cY = R2, cE = R2 + 16;  // the chunk's y (columns 0, 1: two parts) and e (column 0)
 
     if (skip) {
         // the state this call relies on is not in the workspace: nothing to compute
@@ -911,8 +925,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
         const uint32_t idMM = idesc_bf16(128, 128, true, true);
-        const uint32_t idZ = idesc_bf16(128, 16, true, false);
-        const uint32_t pb = smem_u32(Pb), on = smem_u32(ones), dtb = smem_u32(dtt);
+        const uint32_t pb = smem_u32(Pb);
         const uint32_t qb = smem_u32(stage), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
         int it = 0;
         bool ok = true;
@@ -929,6 +942,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                     const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
                     mma_ss(R0, sdesc_sw128(kb + o, 16, 1024), sdesc_sw128(qb + o, 16, 1024), idKK, k > 0);
                 }
+                mma_commit(barT1);
                 ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x404);  // dOt is in place of dO
                 if (!ok) break;
                 tc_fence_after();
@@ -937,43 +951,35 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                     const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
                     mma_ss(R1, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(ob + o, 16, 1024), idKK, k > 0);
                 }
-                mma_commit(barT);
+                mma_commit(barT2);
                 if (c > pc.a) {
 #pragma unroll
                     for (int k = 0; k < 8; ++k)  // P += Q^T dOt
                         mma_ss(R3, sdesc_sw128(qb + 2048 * k, kBox, 1024), sdesc_sw128(ob + 2048 * k, kBox, 1024),
                                idMM, 1u);
                 }
-                ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x405);
+                ok = wait_or_abort(barP1, ph, abort_flag, P.status, 0x405);  // P^T is in R0
                 if (ok) ok = wait_or_abort(barPb, ph, abort_flag, P.status, 0x406);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {  // dV = P^T dOt + K Pb
+                    mma_ts(R2, R0 + 64 * (k >> 2) + 8 * (k & 3), sdesc_sw128(ob + 2048 * k, kBox, 1024), idKM, k > 0);
+                    mma_ss(R2, sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                           sdesc_sw128(pb + 2048 * k, kBox, 1024), idKM, 1u);
+                }
+                mma_commit(barV);
+                ok = wait_or_abort(barP2, ph, abort_flag, P.status, 0x407);  // U^T is in R0, Wt^T has been read
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {  // dK = U^T Q + V Pb^T
                     const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
-                    mma_ts(R2, R0 + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_sw128(qb + 2048 * k, kBox, 1024), idKM, k > 0);
-                    mma_ss(R2, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(pb + o, 16, 1024), idKK, 1u);
+                    mma_ts(R1, R0 + 64 * (k >> 2) + 32 + 8 * (k & 3), sdesc_sw128(qb + 2048 * k, kBox, 1024), idKM, k > 0);
+                    mma_ss(R1, sdesc_sw128(vb + o, 16, 1024), sdesc_sw128(pb + o, 16, 1024), idKK, 1u);
                 }
                 mma_commit(barK);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // dV = P^T dOt + K Pb
-                    mma_ts(R1, R0 + 64 * (k >> 2) + 8 * (k & 3), sdesc_sw128(ob + 2048 * k, kBox, 1024), idKM, k > 0);
-                    mma_ss(R1, sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(pb + 2048 * k, kBox, 1024), idKM, 1u);
-                }
-                mma_commit(barV);
-                ok = wait_or_abort(barKf, ph, abort_flag, P.status, 0x407);  // dK has been read out of R2
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {  // y_c = Q^T dt ; e_c = dOt^T 1
-                    mma_ss(cY, sdesc_sw128(qb + 2048 * k, kBox, 1024),
-                           sdesc_sw128(dtb + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idZ, k > 0);
-                    mma_ss(cE, sdesc_sw128(ob + 2048 * k, kBox, 1024), sdesc_sw128(on + 32 * (k & 3), 16, 0), idZ,
-                           k > 0);
-                }
-                mma_commit(barC);
-                mma_commit(empty);
+                mma_commit(empty);  // dK was the last MMA to read the stage
             }
         }
     } else if (warp >= 2) {
@@ -982,13 +988,14 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         const int q4 = warp & 3, hf = (warp - 2) >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t lo = (uint32_t)(32 * q4) << 16;
-        unsigned char *ot = stage + TB, *vt = stage + 3 * TB;
-        float ng = 0.f, ndt = 0.f;  // g_j and dt_j of row j of the next chunk to be walked
+        unsigned char *ot = stage + TB;
+        // g_j, dt_j and component j of y_c (half 0) or e_c (half 1) for the next chunk to be walked
+        float ng = 0.f, ndt = 0.f, nye = 0.f;
         {
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid()) {
                 const Piece q = p0.get();
-                load_row_stats(P, q.h, q.e - 1, j, &ng, &ndt);
+                load_chunk_stats(P, q.h, q.e - 1, j, hf, &ng, &ndt, &nye);
             }
         }
         int it = 0;
@@ -996,7 +1003,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             // carried reverse sums (the later pieces of the head); the previous piece's MMAs on R3 and Pb are
-            // complete (its last barC)
+            // complete (its last barV)
             load_carry_sum_half(P.slots_rev, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryLater, j, hf, R3 + lo, 0u,
                                 0u, Pb, yc, ec, true, false);
             fence_proxy_async_smem();
@@ -1006,66 +1013,61 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 const uint32_t ph = it & 1;
                 const long long row0 = (long long)c * kC;
-                const float igj = row0 + j < P.N ? 1.f / ng : 0.f, dtj = ndt;
+                const float igj = row0 + j < P.N ? 1.f / ng : 0.f, dtj = ndt, yej = nye;
                 {
                     long long nh;
                     int nc;
-                    if (next_rev_chunk(pi, pc, c, &nh, &nc)) load_row_stats(P, nh, nc, j, &ng, &ndt);
+                    if (next_rev_chunk(pi, pc, c, &nh, &nc)) load_chunk_stats(P, nh, nc, j, hf, &ng, &ndt, &nye);
                 }
                 ok = wait_or_abort(full, ph, abort_flag, P.status, 0x408);
                 if (!ok) break;
                 scale_row_half(ot, j, hf, igj);  // dO row -> dOt row in place
-                if (hf == 0) {
-                    sDt[j] = dtj;
-                    dt_tile_put(dtt, j, dtj);
-                }
+                if (hf == 0) sDt[j] = dtj;
                 fence_proxy_async_smem();
                 mbar_arrive(barO);
+                if (u == 0) bulk_wait_read0();  // the previous chunk's dV and dK have left their staging tiles
                 epi_sync256();  // every dt_i is in sDt
-                ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x40A);
+                // columns are query rows i of the chunk: keep i >= j.  Each half rewrites only the R0 columns it has
+                // read: P^T of its 64 rows i into R0 + 64 hf + [0, 32), then U^T into R0 + 64 hf + [32, 64)
+                ok = wait_or_abort(barT1, ph, abort_flag, P.status, 0x40A);
                 if (!ok) break;
                 tc_fence_after();
-                {  // columns are query rows i of the chunk: keep i >= j.  Each half rewrites only the R0 columns it
-                   // has read: P^T of its 64 rows i into R0 + 64 hf + [0, 32), U^T into R0 + 64 hf + [32, 64)
+                {
                     uint32_t pk[32];
                     tmem_half_to_bf16(R0 + lo, hf, [&](int i, float x) { return i >= j ? 1.f + x : 0.f; }, pk);
                     tmem_st32(R0 + lo + 64 * hf, pk);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(barP1);
+                }
+                ok = wait_or_abort(barT2, ph, abort_flag, P.status, 0x409);
+                if (!ok) break;
+                tc_fence_after();
+                {
+                    uint32_t pk[32];
                     tmem_half_to_bf16(R1 + lo, hf, [&](int i, float x) { return i >= j ? x - sDt[i] : 0.f; }, pk);
                     tmem_st32(R0 + lo + 64 * hf + 32, pk);
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(barP);
+                    mbar_arrive(barP2);
                 }
-                // dK_j = [R2]_j - y, staged in the V tile (its last reader, dK += V Pb^T, is done)
-                ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
-                if (!ok) break;
-                tc_fence_after();
-                tmem_half_to_out(R2 + lo, hf, yc, -1.f, vt, j);
-                tc_fence_before();
-                mbar_arrive(barKf);
-                fence_proxy_async_smem();
-                if (u == 0) bulk_wait_read0();  // the previous chunk's dV has left its staging tile
-                epi_sync256();
-                if (u == 0) store_tile(&P.tmdK, vt, (int)row0, (int)pc.h);
-                // dV_j = [R1]_j + e
+                // dV_j = [R2]_j + e
                 ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x40C);
                 if (!ok) break;
                 tc_fence_after();
-                tmem_half_to_out(R1 + lo, hf, ec, 1.f, dvt, j);
+                tmem_half_to_out(R2 + lo, hf, ec, 1.f, dvt, j);
                 fence_proxy_async_smem();
-                epi_sync256();  // dV rows staged; every read of yc and ec for this chunk is done
-                if (u == 0) {
-                    store_tile(&P.tmdV, dvt, (int)row0, (int)pc.h);
-                    bulk_wait_read1();  // dK has left the V tile
-                    mbar_arrive(empty);
-                }
-                // the chunk's column sums; P (with this chunk's rows, for the earlier chunks) -> Pb
-                ok = wait_or_abort(barC, ph, abort_flag, P.status, 0x40D);
+                epi_sync256();
+                if (u == 0) store_tile(&P.tmdV, dvt, (int)row0, (int)pc.h);
+                // dK_j = [R1]_j - y
+                ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t s0, s1;
-                tmem_ld2(hf == 0 ? cY + lo : cE + lo, s0, s1);
-                tmem_wait_ld(s0, s1);
+                tmem_half_to_out(R1 + lo, hf, yc, -1.f, dkt, j);
+                fence_proxy_async_smem();
+                epi_sync256();  // dK rows staged; every read of yc and ec for this chunk is done
+                if (u == 0) store_tile(&P.tmdK, dkt, (int)row0, (int)pc.h);
+                // P (with this chunk's rows, for the earlier chunks) -> Pb: its update finished before dV
                 if (c > pc.a) {
                     tmem_half_to_tile(R3 + lo, Pb, j, hf);
                     fence_proxy_async_smem();
@@ -1073,10 +1075,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 tc_fence_before();
                 mbar_arrive(barR);
                 if (c > pc.a) mbar_arrive(barPb);
-                if (hf == 0)
-                    yc[j] += __uint_as_float(s0) + __uint_as_float(s1);
-                else
-                    ec[j] += __uint_as_float(s0);
+                (hf == 0 ? yc : ec)[j] += yej;  // this chunk's rows join the later ones
                 epi_sync256();
             }
         }
@@ -1277,7 +1276,7 @@ constexpr size_t kTB = 2 * (size_t)tc::kBox;
 constexpr size_t kEpiSmemDq = 2 * 128 * 4 + 4 * 128 * 4;  // z, a, 2 row-partial arrays
 constexpr size_t kSmemDq = 4 * kTB + 2 * kTB + 1024 + 2048 + kEpiSmemDq + 512;    // 1 stage of Q, dO, K, V; Sb; dQ; ones; dt
 constexpr size_t kSmemDqNc = 2 * 2 * kTB + 2 * kTB + 1024 + 4096 + kEpiSmemDq + 512;  // 2 stages of Q, dO; Sb; dQ; ones; 2 dt
-constexpr size_t kSmemDkdv = 4 * kTB + 2 * kTB + 1024 + 2048 + 3 * 128 * 4 + 512;  // stage; Pb; dV; ones; dt; y, e, dt
+constexpr size_t kSmemDkdv = 4 * kTB + 3 * kTB + 3 * 128 * 4 + 512;  // stage; Pb; dV; dK; y, e, dt
 constexpr size_t kSmemDkdvNc = 3 * 2 * kTB + kTB + 2 * 128 * 4 + 512;         // 3 stages of K, V
 static_assert(kSmemDkdvNc <= 232448 && kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemDqNc <= 232448, "backward kernel exceeds the shared-memory limit");
 
@@ -1308,6 +1307,7 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.slots_rev = (float *)(ws + p.off_states2);
     P.rs_g = (float *)(ws + p.off_rowstats);
     P.rs_dt = P.rs_g + (size_t)p.BH * p.N;
+    P.chunk_ye = (float *)(ws + p.off_chunkye);
     P.dQ = dQ;
     P.dK = dK;
     P.dV = dV;

@@ -25,6 +25,7 @@ struct TcParams {
     float *g;               // forward normaliser (may be null)
     void *dQ, *dK, *dV;     // backward outputs (bf16)
     float *rs_g, *rs_dt;    // backward row statistics: g_i and delta_i / g_i
+    float *chunk_ye;        // causal backward: per chunk, y_c = sum dt_i q_i then e_c = sum dO_i / g_i
     const void *Kp, *Vp;    // K and V: with the shape they identify the per-piece sums in the workspace
     int check_tag;          // backward reusing the forward's sums: check the workspace tag first
 };

@@ -79,6 +79,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *m, int c0, in
                  : "memory");
 }
 
+// Prefetch of `bytes` (a multiple of 16) contiguous global bytes into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 3-D tiled store shared -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *src, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
@@ -221,7 +226,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t &a, uint32_t &b) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(a), "+r"(b) : : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a bf16 operand stored with the 128-byte swizzle (the layout a

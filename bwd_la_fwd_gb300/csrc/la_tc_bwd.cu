@@ -171,11 +171,11 @@ __device__ __forceinline__ void piece_rev_sums(const TcParams &P, const Piece &p
         uint32_t v[32];
         tmem_ld32(taddr + 64 * hf + 32 * half32, v);
         tmem_wait_ld(v);
-        float4 *dst = (float4 *)(slot + (size_t)i * D + 64 * hf + 32 * half32);
+        float4 *dst = (float4 *)slot;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            dst[slot_f4(i, hf, 8 * half32 + q)] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
     }
     if (hf == 1) {
         slot[(size_t)D * D + i] = y;
@@ -343,11 +343,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
         const long long hi = slice_lo(P.sl, blockIdx.x + 1);
+        {  // the first piece's carry slots
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid())
+                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryEarlier);
+        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
+                                    kCarryEarlier);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x301)) {
                     ok = false;
                     break;
@@ -672,11 +679,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         // ---- TMA producer
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
+        {  // the first piece's carry slots
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid())
+                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryAll);
+        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
+                                    kCarryAll);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x321)) {
                     ok = false;
@@ -891,11 +905,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         prefetch_tmap(&P.tmdO);
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
+        {  // the first piece's carry slots
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid())
+                prefetch_carry(P.slots_rev, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryLater);
+        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, P.sl, blockIdx.x,
+                                    kCarryLater);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x401)) {
                     ok = false;
                     break;
@@ -1152,11 +1173,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         // ---- TMA producer (chunks of each piece in reverse order)
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
+        {  // the first piece's carry slots
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid())
+                prefetch_carry(P.slots_rev, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryAll);
+        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, P.sl, blockIdx.x,
+                                    kCarryAll);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x421)) {
                     ok = false;

@@ -41,6 +41,12 @@ __device__ __forceinline__ int cta_of(const Slices &s, long long x) {
 // Workspace slot of CTA b's piece of head h.
 __host__ __device__ __forceinline__ long long slot_of(long long h, int b) { return h + b; }
 
+// Layout of a slot's D x D matrix (D = 128): the float4 holding columns [4 (16 hf + q), +4) of row d is
+// float4 number (2 q + hf) * 128 + d, so that one float4 of a half of all 128 rows is contiguous and the
+// threads that own rows d (one per TMEM lane) read or write it in one coalesced access.  The two D-vectors
+// follow at float offsets D*D and D*D + D.
+__host__ __device__ __forceinline__ long long slot_f4(int d, int hf, int q) { return (long long)(2 * q + hf) * 128 + d; }
+
 struct Piece {
     long long h;  // head (b * H + h flattened)
     int a, e;     // chunk range [a, e) within the head

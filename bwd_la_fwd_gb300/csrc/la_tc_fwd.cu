@@ -28,7 +28,7 @@ using namespace sm100;
 // ----------------------------------------------------------------------------------------------------
 // Per-piece state sums: for every piece (head h, chunks [a, e)) of this CTA's slice,
 //   S = sum k_j v_j^T (D x D),  z = sum k_j,  a = sum v_j   (fp32, rows of the piece)
-// written to workspace slot (h + blockIdx.x) as [S row-major | z | a].
+// written to workspace slot (h + blockIdx.x) as [S (slot_f4 layout) | z | a].
 // TMEM: two accumulator sets of 160 columns (S 128, z 16, a 16) so that one piece's read-out overlaps
 // the next piece's MMAs.  z and a come from MMAs against a tile of ones (N = 16).
 // ----------------------------------------------------------------------------------------------------
@@ -148,17 +148,19 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 uint32_t r[16];
                 tmem_ld16(ta + c16 * 16, r);
-                tmem_ld_wait();
-                float4 *dst = (float4 *)(slot + (size_t)d * D + c16 * 16);
+                tmem_wait_ld(r);
+                float4 *dst = (float4 *)slot;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                for (int q = 0; q < 4; ++q)  // columns 16 c16 + 4 q: half c16 / 4, float4 4 (c16 % 4) + q of the half
+                    dst[slot_f4(d, c16 >> 2, 4 * (c16 & 3) + q)] =
+                        make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                    __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
             uint32_t rz[16], ra[16];
             tmem_ld16(ta + 128, rz);
             tmem_ld16(ta + 144, ra);
-            tmem_ld_wait();
+            tmem_wait_ld(rz);
+            tmem_wait_ld(ra);
             slot[(size_t)D * D + d] = __uint_as_float(rz[0]);
             slot[(size_t)D * D + D + d] = __uint_as_float(ra[0]);
             tc_fence_before();
@@ -248,11 +250,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
             prefetch_tmap(&P.tmK);
             prefetch_tmap(&P.tmV);
         }
+        {  // the first piece's carry slots
+            PieceIter p0(P.sl, blockIdx.x);
+            if (p0.valid())
+                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, CAUSAL ? kCarryEarlier : kCarryAll);
+        }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
+                                    CAUSAL ? kCarryEarlier : kCarryAll);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x201)) {
                     ok = false;
@@ -340,7 +349,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         const int q4 = warp & 3, hf = (warp - 2) >> 2;
         const int i = 32 * q4 + lane;
         const uint32_t lo = (uint32_t)(32 * q4) << 16;
-        __nv_bfloat16 *Og = (__nv_bfloat16 *)P.O;
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
@@ -393,6 +401,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(barP);
+                }
+                if (!CAUSAL) {  // the Q tile is read below; causal chunks know it has landed from barT
+                    ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x20B);
+                    if (!ok) break;
                 }
                 part += dot_half(st, i, hf, zc);  // q_i . z over this half's d
                 // exchange columns alternate by chunk parity: the barrier below then orders every read of

@@ -27,7 +27,7 @@ __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" 
 enum CarryMode { kCarryEarlier = 0, kCarryLater = 1, kCarryAll = 2 };
 
 // Half `hf` of the state carried into CTA b's piece of head h, summed here from the per-piece slots
-// ([S row-major | z | a], fp32, `stride` floats apart) of the head's other pieces: the earlier ones
+// ([S (slot_f4 layout) | z | a], fp32, `stride` floats apart) of the head's other pieces: the earlier ones
 // (causal, chunk order), the later ones (causal, reverse order) or all of them (non-causal); a head
 // spans only a few slices, so this is a handful of slots read from L2.  Row d, columns [64 hf, 64 hf + 64)
 // of S go into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes
@@ -47,10 +47,10 @@ __device__ __forceinline__ void load_carry_sum_half(const float *slots, long lon
 #pragma unroll 1
     for (int bb = first; bb <= last; ++bb) {
         const float *slot = slots + slot_of(h, bb) * stride;
-        const float4 *src = (const float4 *)(slot + (size_t)d * D + 64 * hf);
+        const float4 *src = (const float4 *)slot;
         float4 v4[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) v4[q] = src[q];
+        for (int q = 0; q < 16; ++q) v4[q] = src[slot_f4(d, hf, q)];  // coalesced over the rows d of a warp
         vsum += slot[(size_t)D * D + hf * D + d];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -83,6 +83,30 @@ __device__ __forceinline__ void load_carry_sum_half(const float *slots, long lon
     (hf == 0 ? zc : ac)[d] = vsum;
     if (to_tmem && vec_to_tmem) tmem_st1(hf == 0 ? tZ : tA, __float_as_uint(vsum));
     if (to_tmem) tmem_st_wait();
+}
+
+// Brings into L2 the slots load_carry_sum_half will read for CTA b's piece of head h.  The slots were
+// written by an earlier kernel and the walks stream far more than L2 holds, so without this a carry load
+// waits on HBM one slot after another, with a small share of the bandwidth.  One thread.
+__device__ __forceinline__ void prefetch_carry(const float *slots, long long stride, const Slices &sl, long long h,
+                                               int b, CarryMode mode) {
+    constexpr int D = 128;
+    const long long x0 = h * sl.nchunk;
+    const int b0 = cta_of(sl, x0), b1 = cta_of(sl, x0 + sl.nchunk - 1);
+    const int first = mode == kCarryLater ? b + 1 : b0, last = mode == kCarryEarlier ? b - 1 : b1;
+    for (int bb = first; bb <= last; ++bb)
+        bulk_prefetch_l2(slots + slot_of(h, bb) * stride, (uint32_t)((D * D + 2 * D) * sizeof(float)));
+}
+
+// Prefetches, from the TMA producer, the carry slots of the piece that follows `pi` in the slice, when
+// `remaining` chunks of the current piece are still to be issued (two, or all of a shorter piece).
+__device__ __forceinline__ void prefetch_next_carry(const PieceIter &pi, int remaining, int piece_len,
+                                                    const float *slots, long long stride, const Slices &sl, int b,
+                                                    CarryMode mode) {
+    if (remaining != (piece_len > 2 ? 2 : piece_len - 1)) return;
+    PieceIter pn = pi;
+    pn.next();
+    if (pn.valid()) prefetch_carry(slots, stride, sl, pn.get().h, b, mode);
 }
 
 // Row d's 64 columns [64 hf, 64 hf + 64) of an fp32 TMEM block, rounded into box hf of a bf16 operand tile.

@@ -70,3 +70,24 @@ def test_repeatable_and_workspace_reusable():
     for a, b in zip(*outs):
         assert torch.equal(a, b)
     assert la.la_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("ctas", [1, 3])
+def test_first_chunk_of_each_piece_waits_for_its_tiles(oracle_lib, monkeypatch, ctas):
+    """Non-causal forward, few CTAs, fresh workspaces: the first chunk of every piece (right after a short
+    carry load) must read its Q tile only after the tile has landed; repeated, so that a read that races
+    the copy shows up as a wrong normaliser in that chunk."""
+    import torch
+    from bwd_la_fwd_gb300 import la
+    monkeypatch.setenv("LA_TC_MAX_CTAS", str(ctas))
+    x = inputs.generate(1, 3, 549, 128, 31 + ctas, dtype="bf16")
+    f = U.stored_to_f64(x, "bf16")
+    O_ref, g_ref = oracle_lib.forward(f["Q"], f["K"], f["V"], False)
+    Q, K, V = (U.to_device(x[n], "bf16") for n in ("Q", "K", "V"))
+    for _ in range(4):
+        ws = la.new_workspace(1, 3, 549, 128, False, la.LA_BF16, False)
+        O, g = la.la_forward(Q, K, V, False, workspace=ws)
+        torch.cuda.synchronize()
+        assert la.la_get_status(ws) == 0
+        U.assert_close("g", U.to_f64(g), g_ref, "bf16")
+        U.assert_close("O", U.to_f64(O), O_ref, "bf16")

@@ -71,7 +71,9 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    if force or procs or not os.path.exists(LIB):
+    # relink whenever an object is newer than the library (also after a link that failed part-way)
+    lib_stale = not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs)
+    if force or procs or lib_stale:
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-L" + cuda_lib_dir(nvcc), "-lcudart", "-ldl"]
         subprocess.run(cmd, check=True)

@@ -17,7 +17,7 @@ struct WsHeader {
     uint32_t ticket[8];   // per-kernel ticket counters (reset by the last block of each launch)
     uint32_t done[8];     // per-kernel completion counters
     uint32_t epoch[8];    // per-kernel launch epochs (flags compare against these)
-    uint64_t state_tag[6]; // which K, V and slicing the per-piece state sums belong to (tensor-core path)
+    uint64_t state_tag[7]; // which K, V and slicing the per-piece state sums belong to, and their form
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
 static_assert(offsetof(WsHeader, state_tag) == 128, "the state tag sits 128 bytes into the header");

@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     griddep_wait();
     griddep_launch_dependents();
     if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -343,18 +343,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
         const long long hi = slice_lo(P.sl, blockIdx.x + 1);
-        {  // the first piece's carry slots
+        {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid())
-                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryEarlier);
+                bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
+                                 (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
-                                    kCarryEarlier);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x301)) {
                     ok = false;
                     break;
@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
             const Piece pc = pi.get();
             // forward state carried into the piece, from the head's earlier pieces (the previous
             // piece's MMAs on R2 are complete: its last barX has been waited for)
-            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryEarlier, i, hf, R2 + lo, 0u, 0u,
+            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, R2 + lo, 0u, 0u,
                                 Sb, zc, ac, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     griddep_wait();
     griddep_launch_dependents();
     if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -679,18 +679,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         // ---- TMA producer
         prefetch_tmap(&P.tmQ);
         prefetch_tmap(&P.tmdO);
-        {  // the first piece's carry slots
+        {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid())
-                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryAll);
+                bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
+                                 (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
-                                    kCarryAll);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x321)) {
                     ok = false;
@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryAll, i, hf, 0u, 0u, 0u, Sb, zc,
+            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, 0u, 0u, 0u, Sb, zc,
                                 ac, false, false);
             fence_proxy_async_smem();
             epi_sync256();
@@ -887,7 +887,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     griddep_wait();
     griddep_launch_dependents();
     if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -905,18 +905,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         prefetch_tmap(&P.tmdO);
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
-        {  // the first piece's carry slots
+        {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid())
-                prefetch_carry(P.slots_rev, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryLater);
+                bulk_prefetch_l2(P.slots_rev + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
+                                 (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
-                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, P.sl, blockIdx.x,
-                                    kCarryLater);
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x401)) {
                     ok = false;
                     break;
@@ -1025,7 +1025,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
             const Piece pc = pi.get();
             // carried reverse sums (the later pieces of the head); the previous piece's MMAs on R3 and Pb are
             // complete (its last barV)
-            load_carry_sum_half(P.slots_rev, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryLater, j, hf, R3 + lo, 0u,
+            load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, R3 + lo, 0u,
                                 0u, Pb, yc, ec, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1157,7 +1157,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
     griddep_wait();
     griddep_launch_dependents();
     if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P)) {
+        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -1173,18 +1173,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         // ---- TMA producer (chunks of each piece in reverse order)
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
-        {  // the first piece's carry slots
+        {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid())
-                prefetch_carry(P.slots_rev, P.slot_stride, P.sl, p0.get().h, blockIdx.x, kCarryAll);
+                bulk_prefetch_l2(P.slots_rev + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
+                                 (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
-                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, P.sl, blockIdx.x,
-                                    kCarryAll);
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x421)) {
                     ok = false;
@@ -1248,7 +1248,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
             const Piece pc = pi.get();
             // the head's totals (every piece of a head carries the same sums); the previous piece's MMAs
             // on Pb are complete (its last barV)
-            load_carry_sum_half(P.slots_rev, P.slot_stride, P.sl, pc.h, blockIdx.x, kCarryAll, j, hf, 0u, 0u, 0u, Pb,
+            load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, 0u, 0u, 0u, Pb,
                                 yc, ec, false, false);
             fence_proxy_async_smem();
             epi_sync256();
@@ -1341,16 +1341,35 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.dV = dV;
     P.Kp = K;
     P.Vp = V;
-    P.check_tag = reuse_fwd_state ? 1 : 0;
+    // reusing the forward's sums: they must be in the form this pass expects (raw piece sums for causal,
+    // head totals for non-causal)
+    P.check_tag = reuse_fwd_state ? (int)(p.causal ? tc::kTagPrefix : tc::kTagTotals) + 1 : 0;
     const unsigned nthr = 64 + tc::kEpiThreads;
-    cudaError_t e = reuse_fwd_state ? cudaSuccess : tc_host::launch_agg(P, s);
-    if (e == cudaSuccess)
+    unsigned launches = 0;
+    cudaError_t e = cudaSuccess;
+    if (!reuse_fwd_state) {
+        e = tc_host::launch_agg(P, s);
+        ++launches;
+        if (e == cudaSuccess) {
+            e = tc_host::launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal, true, s);
+            ++launches;
+        }
+    }
+    if (e == cudaSuccess) {
         e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dq_kernel, P.sl.G, nthr, kSmemDq, s, P)
                      : tc_host::launch_tc(tc::tc_bwd_dq_nc_kernel, P.sl.G, nthr, kSmemDqNc, s, P);
-    if (e == cudaSuccess)
+        ++launches;
+    }
+    if (e == cudaSuccess) {
+        e = tc_host::launch_combine(P, P.slots_rev, p.causal ? tc::kCombineSuffix : tc::kCombineTotal, false, s);
+        ++launches;
+    }
+    if (e == cudaSuccess) {
         e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dkdv_kernel, P.sl.G, nthr, kSmemDkdv, s, P)
                      : tc_host::launch_tc(tc::tc_bwd_dkdv_nc_kernel, P.sl.G, nthr, kSmemDkdvNc, s, P);
-    if (e == cudaSuccess) count_launches(reuse_fwd_state ? 2 : 3);
+        ++launches;
+    }
+    if (e == cudaSuccess) count_launches(launches);
     return e;
 }
 

@@ -7,8 +7,9 @@
 // boundary) where one CTA per head would leave most SMs idle.  The part of a slice that lies in one head
 // is a "piece".  A piece's D x D state sum is stored in workspace slot (head + b): the slots of one CTA's
 // pieces are consecutive and never collide with another CTA's, and a head's slots are found from the
-// CTAs that cover it.  Later kernels add the slots of a head's earlier (or later) pieces to obtain the
-// state carried into a piece, so no CTA ever waits for another inside a kernel.
+// CTAs that cover it.  A small kernel between two walks turns each head's slots into the state carried
+// into each piece (the sum over its earlier pieces, its later pieces, or all of them), so no CTA ever
+// waits for another inside a kernel.
 #pragma once
 
 #include <stdint.h>
@@ -38,6 +39,9 @@ __device__ __forceinline__ int cta_of(const Slices &s, long long x) {
     return b;
 }
 
+// float4 elements of a slot's data: the D x D matrix and the two D-vectors (D = 128).
+constexpr int kSlotF4 = (128 * 128 + 2 * 128) / 4;
+
 // Workspace slot of CTA b's piece of head h.
 __host__ __device__ __forceinline__ long long slot_of(long long h, int b) { return h + b; }
 
@@ -45,7 +49,9 @@ __host__ __device__ __forceinline__ long long slot_of(long long h, int b) { retu
 // float4 number (2 q + hf) * 128 + d, so that one float4 of a half of all 128 rows is contiguous and the
 // threads that own rows d (one per TMEM lane) read or write it in one coalesced access.  The two D-vectors
 // follow at float offsets D*D and D*D + D.
-__host__ __device__ __forceinline__ long long slot_f4(int d, int hf, int q) { return (long long)(2 * q + hf) * 128 + d; }
+__host__ __device__ __forceinline__ long long slot_f4(int d, int hf, int q) {
+    return (long long)(2 * q + hf) * 128 + d;
+}
 
 struct Piece {
     long long h;  // head (b * H + h flattened)

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) write_state_tag(P);  // the slots below belong to P.Kp, P.Vp
+    if (blockIdx.x == 0 && threadIdx.x == 0) write_state_tag(P, kTagRaw);  // the slots below belong to P.Kp, P.Vp (until combined)
     const uint32_t tmem = *tslot;
 
     if (warp == 0 && lane == 0) {
@@ -250,18 +250,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
             prefetch_tmap(&P.tmK);
             prefetch_tmap(&P.tmV);
         }
-        {  // the first piece's carry slots
+        {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
             if (p0.valid())
-                prefetch_carry(P.slots, P.slot_stride, P.sl, p0.get().h, blockIdx.x, CAUSAL ? kCarryEarlier : kCarryAll);
+                bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
+                                 (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, P.sl, blockIdx.x,
-                                    CAUSAL ? kCarryEarlier : kCarryAll);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x201)) {
                     ok = false;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x206)) break;
                 tc_fence_after();
             }
-            load_carry_sum_half(P.slots, P.slot_stride, P.sl, pc.h, blockIdx.x, CAUSAL ? kCarryEarlier : kCarryAll, i,
+            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
                                 hf, tS + lo, tZ + lo, tA + lo, Sb, zc, ac, CAUSAL, true);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -490,6 +490,51 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
 template __global__ void tc_fwd_kernel<true>(const __grid_constant__ TcParams P);
 template __global__ void tc_fwd_kernel<false>(const __grid_constant__ TcParams P);
 
+// ----------------------------------------------------------------------------------------------------
+// Carries: in place over the piece slots of each head, in piece order, so that a walk then reads exactly
+// one slot (its own) per piece: kCombinePrefix gives each piece the sum over the head's earlier pieces
+// (causal, chunk order), kCombineSuffix over the later ones (causal, reverse order), kCombineTotal the
+// head's total (non-causal).  grid = (ceil(kSlotF4 / 256), heads; heads beyond the grid's y extent loop);
+// thread x owns float4 x of every slot of its head, and reads each slot before it writes it.
+// ----------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ TcParams P) {
+    griddep_wait();  // the slots come from the previous kernel of the stream
+    griddep_launch_dependents();
+    if (P.combine_tag && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        write_state_tag(P, P.combine_mode == kCombineTotal ? kTagTotals : kTagPrefix);
+    const int x = blockIdx.x * 256 + threadIdx.x;
+    if (x >= kSlotF4) return;
+    const long long BH = P.sl.T / P.sl.nchunk, s4 = P.slot_stride / 4;
+    const int mode = P.combine_mode;
+    float4 *base = (float4 *)P.combine_slots + x;
+    for (long long h = blockIdx.y; h < BH; h += gridDim.y) {
+        const long long x0 = h * P.sl.nchunk;
+        const int b0 = cta_of(P.sl, x0), b1 = cta_of(P.sl, x0 + P.sl.nchunk - 1);
+        const int n = b1 - b0 + 1;
+        auto at = [&](int k) -> float4 * {  // k-th slot of the head in the order of the sums
+            return base + slot_of(h, mode == kCombineSuffix ? b1 - k : b0 + k) * s4;
+        };
+        float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g = 0; g < n; g += 8) {  // up to eight loads in flight; each slot read before it is written
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (g + k < n) v[k] = *at(g + k);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (g + k < n) {
+                    if (mode != kCombineTotal) *at(g + k) = run;  // exclusive: the sum before this piece
+                    run.x += v[k].x;
+                    run.y += v[k].y;
+                    run.z += v[k].z;
+                    run.w += v[k].w;
+                }
+        }
+        if (mode == kCombineTotal)
+            for (int k = 0; k < n; ++k) *at(k) = run;
+    }
+}
+
 }  // namespace tc
 
 // ======================================================================================== host ===
@@ -572,11 +617,11 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     return true;
 }
 
-cudaError_t launch_tc(void (*kernel)(const tc::TcParams), unsigned grid, unsigned block, size_t smem,
+cudaError_t launch_tc(void (*kernel)(const tc::TcParams), dim3 grid, unsigned block, size_t smem,
                       cudaStream_t s, const tc::TcParams &P) {
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -586,6 +631,15 @@ cudaError_t launch_tc(void (*kernel)(const tc::TcParams), unsigned grid, unsigne
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
+cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cudaStream_t s) {
+    P.combine_slots = slots;
+    P.combine_mode = mode;
+    P.combine_tag = tag ? 1 : 0;
+    const long long BH = P.sl.T / P.sl.nchunk;
+    const dim3 grid((tc::kSlotF4 + 255) / 256, (unsigned)(BH < 65535 ? BH : 65535));
+    return launch_tc(tc::tc_combine_kernel, grid, 256, 0, s, P);
 }
 
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
@@ -615,9 +669,11 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     P.Vp = V;
     cudaError_t e = launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
     if (e == cudaSuccess)
+        e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal, true, s);
+    if (e == cudaSuccess)
         e = p.causal ? launch_tc(tc::tc_fwd_kernel<true>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s, P)
                      : launch_tc(tc::tc_fwd_kernel<false>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s, P);
-    if (e == cudaSuccess) count_launches(2);
+    if (e == cudaSuccess) count_launches(3);
     return e;
 }
 

@@ -27,32 +27,41 @@ struct TcParams {
     float *rs_g, *rs_dt;    // backward row statistics: g_i and delta_i / g_i
     float *chunk_ye;        // causal backward: per chunk, y_c = sum dt_i q_i then e_c = sum dO_i / g_i
     const void *Kp, *Vp;    // K and V: with the shape they identify the per-piece sums in the workspace
-    int check_tag;          // backward reusing the forward's sums: check the workspace tag first
+    int check_tag;          // backward reusing the forward's sums: 0 no check, else the form expected + 1
+    float *combine_slots;   // tc_combine_kernel: the slot array it turns into carries
+    int combine_mode;       // tc_combine_kernel: kCombinePrefix, kCombineSuffix or kCombineTotal
+    int combine_tag;        // tc_combine_kernel: also record the new form in the workspace tag
 };
 
-// The per-piece sums kernel records in the workspace header which K, V and slicing the slots hold; a
-// backward that reuses them instead of recomputing them checks the record first (state_tag_matches).
+// Forms of the slot arrays (tc_combine_kernel).
+enum : int { kCombinePrefix = 0, kCombineSuffix = 1, kCombineTotal = 2 };
+// The per-piece sums kernel records in the workspace header which K, V and slicing the slots hold, and
+// tc_combine_kernel in which form (kTagRaw: each piece's own sums; kTagPrefix: the sums over the head's
+// earlier pieces; kTagTotals: the head's total); a backward that reuses them instead of recomputing them
+// checks the record first.
+constexpr uint64_t kTagRaw = 1, kTagPrefix = 2, kTagTotals = 3;
 constexpr size_t kTagOffset = 128;  // bytes into the workspace header
 static_assert(kTagOffset == offsetof(WsHeader, state_tag), "tag offset");
-constexpr int kTagWords = 6;
-__host__ __device__ inline void state_tag(const TcParams &P, uint64_t *t) {
+constexpr int kTagWords = 7;
+__host__ __device__ inline void state_tag(const TcParams &P, uint64_t form, uint64_t *t) {
     t[0] = 0x4C415F5354415445ull;  // marker ("LA_STATE")
     t[1] = (uint64_t)(uintptr_t)P.Kp;
     t[2] = (uint64_t)(uintptr_t)P.Vp;
     t[3] = (uint64_t)P.sl.T;
     t[4] = (uint64_t)P.N;
     t[5] = (uint64_t)P.sl.G;
+    t[6] = form;
 }
 #ifdef __CUDACC__
-__device__ inline void write_state_tag(const TcParams &P) {
+__device__ inline void write_state_tag(const TcParams &P, uint64_t form) {
     uint64_t t[kTagWords];
-    state_tag(P, t);
+    state_tag(P, form, t);
     volatile uint64_t *w = (volatile uint64_t *)((unsigned char *)P.status + kTagOffset);
     for (int k = 0; k < kTagWords; ++k) w[k] = t[k];
 }
-__device__ inline bool state_tag_matches(const TcParams &P) {
+__device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
     uint64_t t[kTagWords];
-    state_tag(P, t);
+    state_tag(P, form, t);
     const volatile uint64_t *w = (const volatile uint64_t *)((const unsigned char *)P.status + kTagOffset);
     bool ok = true;
     for (int k = 0; k < kTagWords; ++k) ok = ok && w[k] == t[k];
@@ -69,8 +78,10 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
 // Launches a tensor-core kernel as a programmatic dependent of the previous kernel in the stream (the
 // kernels order their global accesses after griddepcontrol.wait, so stream order is kept).
-cudaError_t launch_tc(void (*kernel)(const tc::TcParams), unsigned grid, unsigned block, size_t smem,
+cudaError_t launch_tc(void (*kernel)(const tc::TcParams), dim3 grid, unsigned block, size_t smem,
                       cudaStream_t s, const tc::TcParams &P);
+// Turns the piece slots of `slots` into carries (mode: tc::kCombine*; tag: record the form).
+cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cudaStream_t s);
 }  // namespace tc_host
 
 // bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.

@@ -24,42 +24,22 @@ constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane qua
 __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Which of a head's pieces make up the state carried into a piece.
-enum CarryMode { kCarryEarlier = 0, kCarryLater = 1, kCarryAll = 2 };
-
-// Half `hf` of the state carried into CTA b's piece of head h, summed here from the per-piece slots
-// ([S (slot_f4 layout) | z | a], fp32, `stride` floats apart) of the head's other pieces: the earlier ones
-// (causal, chunk order), the later ones (causal, reverse order) or all of them (non-causal); a head
-// spans only a few slices, so this is a handful of slots read from L2.  Row d, columns [64 hf, 64 hf + 64)
-// of S go into TMEM (if to_tmem) and, as bf16, into box hf of the operand tile Sb.  Half 0 also writes
-// z[d] to zc (and TMEM column tZ if to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and column tA).
-__device__ __forceinline__ void load_carry_sum_half(const float *slots, long long stride, const Slices &sl,
-                                                    long long h, int b, CarryMode mode, int d, int hf, uint32_t tS,
-                                                    uint32_t tZ, uint32_t tA, unsigned char *Sb, float *zc,
-                                                    float *ac, bool to_tmem, bool vec_to_tmem) {
+// Half `hf` of the state carried into CTA b's piece of head h, from the piece's own slot ([S (slot_f4
+// layout) | z | a], fp32), which tc_combine_kernel has set to the sum over the head's earlier pieces,
+// later pieces or all of them.  Row d, columns [64 hf, 64 hf + 64) of S go into TMEM (if to_tmem) and,
+// as bf16, into box hf of the operand tile Sb.  Half 0 also writes z[d] to zc (and TMEM column tZ if
+// to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and column tA).
+static __device__ __noinline__ void load_carry_half(const float *slots, long long stride, long long h, int b, int d,
+                                                int hf, uint32_t tS, uint32_t tZ, uint32_t tA, unsigned char *Sb,
+                                                float *zc, float *ac, bool to_tmem, bool vec_to_tmem) {
     constexpr int D = 128;
-    const long long x0 = h * sl.nchunk;
-    const int b0 = cta_of(sl, x0), b1 = cta_of(sl, x0 + sl.nchunk - 1);
-    const int first = mode == kCarryLater ? b + 1 : b0, last = mode == kCarryEarlier ? b - 1 : b1;
-    float acc[64];
+    const float *slot = slots + slot_of(h, b) * stride;
+    const float4 *src = (const float4 *)slot;
+    float4 v4[16];
 #pragma unroll
-    for (int q = 0; q < 64; ++q) acc[q] = 0.f;
-    float vsum = 0.f;
-#pragma unroll 1
-    for (int bb = first; bb <= last; ++bb) {
-        const float *slot = slots + slot_of(h, bb) * stride;
-        const float4 *src = (const float4 *)slot;
-        float4 v4[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) v4[q] = src[slot_f4(d, hf, q)];  // coalesced over the rows d of a warp
-        vsum += slot[(size_t)D * D + hf * D + d];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            acc[4 * q] += v4[q].x;
-            acc[4 * q + 1] += v4[q].y;
-            acc[4 * q + 2] += v4[q].z;
-            acc[4 * q + 3] += v4[q].w;
-        }
-    }
+    for (int q = 0; q < 16; ++q) v4[q] = src[slot_f4(d, hf, q)];  // coalesced over the rows d of a warp
+    const float vsum = slot[(size_t)D * D + hf * D + d];
+    const float *acc = (const float *)v4;
 #pragma unroll
     for (int half32 = 0; half32 < 2; ++half32) {
         const float *a32 = acc + 32 * half32;
@@ -85,28 +65,16 @@ __device__ __forceinline__ void load_carry_sum_half(const float *slots, long lon
     if (to_tmem) tmem_st_wait();
 }
 
-// Brings into L2 the slots load_carry_sum_half will read for CTA b's piece of head h.  The slots were
-// written by an earlier kernel and the walks stream far more than L2 holds, so without this a carry load
-// waits on HBM one slot after another, with a small share of the bandwidth.  One thread.
-__device__ __forceinline__ void prefetch_carry(const float *slots, long long stride, const Slices &sl, long long h,
-                                               int b, CarryMode mode) {
-    constexpr int D = 128;
-    const long long x0 = h * sl.nchunk;
-    const int b0 = cta_of(sl, x0), b1 = cta_of(sl, x0 + sl.nchunk - 1);
-    const int first = mode == kCarryLater ? b + 1 : b0, last = mode == kCarryEarlier ? b - 1 : b1;
-    for (int bb = first; bb <= last; ++bb)
-        bulk_prefetch_l2(slots + slot_of(h, bb) * stride, (uint32_t)((D * D + 2 * D) * sizeof(float)));
-}
-
-// Prefetches, from the TMA producer, the carry slots of the piece that follows `pi` in the slice, when
-// `remaining` chunks of the current piece are still to be issued (two, or all of a shorter piece).
+// Brings into L2 the carry slot of the piece that follows `pi` in the slice, when `remaining` chunks of
+// the current piece are still to be issued (two, or all of a shorter piece).  The slots were written by
+// an earlier kernel and the walks stream far more than L2 holds.  One thread (the TMA producer).
 __device__ __forceinline__ void prefetch_next_carry(const PieceIter &pi, int remaining, int piece_len,
-                                                    const float *slots, long long stride, const Slices &sl, int b,
-                                                    CarryMode mode) {
+                                                    const float *slots, long long stride, int b) {
     if (remaining != (piece_len > 2 ? 2 : piece_len - 1)) return;
     PieceIter pn = pi;
     pn.next();
-    if (pn.valid()) prefetch_carry(slots, stride, sl, pn.get().h, b, mode);
+    if (pn.valid())
+        bulk_prefetch_l2(slots + slot_of(pn.get().h, b) * stride, (uint32_t)(kSlotF4 * sizeof(float4)));
 }
 
 // Row d's 64 columns [64 hf, 64 hf + 64) of an fp32 TMEM block, rounded into box hf of a bf16 operand tile.

@@ -109,3 +109,16 @@ def test_simt_call_on_the_workspace_clears_the_record():
     la.la_forward(t["Q"], t["K"], t["V"], True, O=O, workspace=ws)
     la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
     assert la.la_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("fwd_causal", [1, 0])
+def test_reuse_after_a_forward_with_the_other_mask_reports_state_error(fwd_causal):
+    """A causal forward leaves each piece's own sums, a non-causal one the head totals; a backward with the
+    other mask must not take them."""
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 2, 700, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=77)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], bool(fwd_causal), workspace=ws)
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], not fwd_causal, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE

@@ -36,6 +36,7 @@ struct Plan {
     size_t off_flags;
     size_t off_rowstats;
     size_t off_chunkye; // tensor-core causal backward: each chunk's column sums y_c, e_c
+    size_t off_chunkza; // tensor-core path: each chunk's column sums z_c = sum k_j, a_c = sum v_j
     size_t bytes_fwd;   // workspace bytes for the forward / for the backward
     size_t bytes_bwd;
     bool use_tc;        // tcgen05 kernels (bf16) rather than the SIMT kernels

@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
     // column sums of the chunk (N = 16 each; column 0 of each holds the sum, column 1 of cY the dt remainder),
     // in the R1 columns that U' (R1 + [0, 32) and R1 + [64, 96)) leaves free
-    const uint32_t cZ = R1 + 32, cA = R1 + 48, cY = R1 + 96, cE = R1 + 112;
+    const uint32_t cY = R1 + 96, cE = R1 + 112;
 
     if (skip) {
         // the state this call relies on is not in the workspace: nothing to compute
@@ -424,12 +424,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {  // X = Y + U' K ; z_c = K^T 1 ; a_c = V^T 1
-                    const uint64_t o1 = sdesc_sw128(on + 32 * (k & 3), 16, 0);
+                for (int k = 0; k < 8; ++k)  // X = Y + U' K
                     mma_ts(R0, R1 + 64 * (k >> 2) + 8 * (k & 3), sdesc_sw128(kb + 2048 * k, kBox, 1024), idKM, 1u);
-                    mma_ss(cZ, sdesc_sw128(kb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
-                    mma_ss(cA, sdesc_sw128(vb + 2048 * k, kBox, 1024), o1, idZ, k > 0);
-                }
                 mma_commit(barX);
                 ok = wait_or_abort(barDt, ph, abort_flag, P.status, 0x309);  // dO / g in place, dt_i in dtt
                 if (!ok) break;
@@ -472,6 +468,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 const uint32_t ph = it & 1;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
+                // this chunk's z_c[i] (half 0) or a_c[i] (half 1), from the sums kernel; used at the chunk's end
+                const float zav = P.chunk_za[((size_t)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i];
                 float gpart = 0.f, dpart = 0.f;  // partial g_i and partial delta_i g_i over this half
                 {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
@@ -537,17 +535,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 fence_proxy_async_smem();
                 mbar_arrive(barDt);
                 // dQ_i = X_i / g_i - dt_i z (X = Y + U' K), and the chunk's column sums
-                ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);  // X = Y + U' K, z_c, a_c
+                ok = wait_or_abort(barX, ph, abort_flag, P.status, 0x30E);  // X = Y + U' K
                 if (!ok) break;
                 tc_fence_after();
                 tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
-                uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-                if (hf == 0) {  // z_c, a_c (component i)
-                    tmem_ld2(cZ + lo, s0, s1);
-                    tmem_ld2(cA + lo, s2, s3);
-                    tmem_wait_ld(s0, s1);
-                    tmem_wait_ld(s2, s3);
-                }
                 fence_proxy_async_smem();
                 epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
                 if (u == 0) store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
@@ -557,13 +548,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     tc_fence_before();
                     mbar_arrive(barSb);
                 }
-                if (hf == 0) {  // z and a after this chunk
-                    zc[i] += __uint_as_float(s0);
-                    ac[i] += __uint_as_float(s2);
-                }
+                (hf == 0 ? zc : ac)[i] += zav;  // z and a after this chunk
                 ok = wait_or_abort(barC, ph, abort_flag, P.status, 0x30D);  // Ppiece, y_c, e_c
                 if (!ok) break;
                 tc_fence_after();
+                uint32_t s0, s1, s2, s3;
                 if (hf == 1) {  // y_c, e_c (component i): into the piece sums, and kept per chunk for the dK / dV walk
                     tmem_ld2(cY + lo, s0, s1);
                     tmem_ld2(cE + lo, s2, s3);

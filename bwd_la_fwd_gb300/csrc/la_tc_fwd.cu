@@ -28,9 +28,11 @@ using namespace sm100;
 // ----------------------------------------------------------------------------------------------------
 // Per-piece state sums: for every piece (head h, chunks [a, e)) of this CTA's slice,
 //   S = sum k_j v_j^T (D x D),  z = sum k_j,  a = sum v_j   (fp32, rows of the piece)
-// written to workspace slot (h + blockIdx.x) as [S (slot_f4 layout) | z | a].
-// TMEM: two accumulator sets of 160 columns (S 128, z 16, a 16) so that one piece's read-out overlaps
-// the next piece's MMAs.  z and a come from MMAs against a tile of ones (N = 16).
+// written to workspace slot (h + blockIdx.x) as [S (slot_f4 layout) | z | a], and every chunk's own
+// z_c, a_c to the chunk_za array (the walks take them from there instead of forming them again).
+// TMEM: two S accumulators (128 columns each) so that one piece's read-out overlaps the next piece's
+// MMAs, and two per-chunk z_c, a_c blocks (16 + 16 columns) from MMAs against a tile of ones (N = 16);
+// the epilogue drains z_c, a_c every chunk and adds them up for the piece in fp32 registers.
 // ----------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64, NST = 3;
@@ -44,7 +46,9 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     uint64_t *empty = full + NST;
     uint64_t *accfull = empty + NST;
     uint64_t *accfree = accfull + 2;
-    uint32_t *tslot = (uint32_t *)(accfree + 2);
+    uint64_t *zafull = accfree + 2;  // [2] the chunk's z_c, a_c are in TMEM block it & 1
+    uint64_t *zafree = zafull + 2;   // [2] the epilogue has read them
+    uint32_t *tslot = (uint32_t *)(zafree + 2);
     volatile int *abort_flag = (volatile int *)(tslot + 1);
     if (!aligned) return;
 
@@ -57,6 +61,8 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accfull[b], 1);
             mbar_init(&accfree[b], 128);
+            mbar_init(&zafull[b], 1);
+            mbar_init(&zafree[b], 128);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -105,45 +111,71 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && !*abort_flag; pi.next(), ++p) {
             const Piece pc = pi.get();
             const int buf = p & 1;
-            const uint32_t acc = tmem + buf * 256;
+            const uint32_t acc = tmem + buf * 128;
             if (p >= 2 && !wait_or_abort(&accfree[buf], ((p >> 1) - 1) & 1, abort_flag, P.status, 0x102)) break;
             tc_fence_after();
             bool ok = true;
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                const int s = it % NST;
-                if (!wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x103)) {
+                const int s = it % NST, zb = it & 1;
+                if (!wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x103) ||
+                    (it >= 2 && !wait_or_abort(&zafree[zb], ((it >> 1) - 1) & 1, abort_flag, P.status, 0x105))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t kb = smem_u32(stages + s * STAGE), vb = kb + NB * kBox;
+                const uint32_t za = tmem + 256 + 32 * zb;
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k) {
                     const uint64_t kt = sdesc_sw128(kb + 2048 * k, kBox, 1024);  // K^T, MN-major, 16 rows
                     const uint64_t vt = sdesc_sw128(vb + 2048 * k, kBox, 1024);  // V,   MN-major, 16 rows
                     const uint64_t on = sdesc_sw128(ones_a + 32 * (k & 3), 16, 1024);
-                    const uint32_t accum = (c > pc.a || k > 0) ? 1u : 0u;
-                    mma_ss(acc, kt, vt, idS, accum);         // S += K^T V
-                    mma_ss(acc + 128, kt, on, idZ, accum);   // z += K^T 1
-                    mma_ss(acc + 144, vt, on, idZ, accum);   // a += V^T 1
+                    mma_ss(acc, kt, vt, idS, (c > pc.a || k > 0) ? 1u : 0u);  // S += K^T V
+                    mma_ss(za, kt, on, idZ, k > 0 ? 1u : 0u);                // z_c = K^T 1
+                    mma_ss(za + 16, vt, on, idZ, k > 0 ? 1u : 0u);           // a_c = V^T 1
                 }
+                mma_commit(&zafull[zb]);
                 mma_commit(&empty[s]);
             }
             if (!ok) break;
             mma_commit(&accfull[buf]);
         }
     } else if (warp >= 2) {
-        // ---- epilogue: TMEM -> workspace slot
+        // ---- epilogue: per chunk z_c, a_c (TMEM -> chunk_za, running piece sums); per piece S -> slot
         const int lb = 32 * (warp & 3);
         const int d = lb + lane;
-        int p = 0;
-        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && !*abort_flag; pi.next(), ++p) {
+        int p = 0, it = 0;
+        bool ok = true;
+        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++p) {
             const Piece pc = pi.get();
             const int buf = p & 1;
+            float zs = 0.f, as = 0.f;  // the piece's z[d], a[d]
+            for (int c = pc.a; c < pc.e; ++c, ++it) {
+                const int zb = it & 1;
+                if (!wait_or_abort(&zafull[zb], (it >> 1) & 1, abort_flag, P.status, 0x106)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t z0, z1, a0, a1;
+                const uint32_t za = tmem + ((uint32_t)lb << 16) + 256 + 32 * zb;
+                tmem_ld2(za, z0, z1);
+                tmem_ld2(za + 16, a0, a1);
+                tmem_wait_ld(z0, z1);
+                tmem_wait_ld(a0, a1);
+                tc_fence_before();
+                mbar_arrive(&zafree[zb]);
+                float *cza = P.chunk_za + ((size_t)pc.h * P.sl.nchunk + c) * 256;
+                cza[d] = __uint_as_float(z0);
+                cza[128 + d] = __uint_as_float(a0);
+                zs += __uint_as_float(z0);
+                as += __uint_as_float(a0);
+            }
+            if (!ok) break;
             if (!wait_or_abort(&accfull[buf], (p >> 1) & 1, abort_flag, P.status, 0x104)) break;
             tc_fence_after();
             float *slot = P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride;
-            const uint32_t ta = tmem + ((uint32_t)lb << 16) + buf * 256;
+            const uint32_t ta = tmem + ((uint32_t)lb << 16) + buf * 128;
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
                 uint32_t r[16];
@@ -156,13 +188,8 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                         make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
-            uint32_t rz[16], ra[16];
-            tmem_ld16(ta + 128, rz);
-            tmem_ld16(ta + 144, ra);
-            tmem_wait_ld(rz);
-            tmem_wait_ld(ra);
-            slot[(size_t)D * D + d] = __uint_as_float(rz[0]);
-            slot[(size_t)D * D + D + d] = __uint_as_float(ra[0]);
+            slot[(size_t)D * D + d] = zs;
+            slot[(size_t)D * D + D + d] = as;
             tc_fence_before();
             mbar_arrive(&accfree[buf]);
         }
@@ -177,13 +204,13 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
 
 // ----------------------------------------------------------------------------------------------------
 // Forward output.  Per chunk (causal): T = Q K^T -> P = [j <= i](1 + T) (bf16, in place in TMEM) ->
-// O = P V + Q Sb (Sb = bf16 state before the chunk) -> S += K^T V, z += K^T 1, a += V^T 1 (TMEM), from
-// which the epilogue writes the next Sb and the fp32 z, a it broadcasts.  The epilogue forms q_i . z and
-// the normaliser.  Non-causal: O = Q Sb with the head's totals (no T, P or state update) into two
+// O = P V + Q Sb (Sb = bf16 state before the chunk) -> S += K^T V (TMEM), from which the epilogue writes
+// the next Sb; the running fp32 z, a advance by each chunk's z_c, a_c from the sums kernel.  The epilogue
+// forms q_i . z and the normaliser.  Non-causal: O = Q Sb with the head's totals (no T, P or state update) into two
 // alternating TMEM accumulators, so the MMA of one chunk overlaps the epilogue of the previous one.
 // Eight epilogue warps: two per TMEM lane quarter, each owning half of the columns; the row sums they
 // share (r_i and q_i . z) are exchanged through two TMEM columns.
-// TMEM: causal  T 0-127, O 128-255, S 256-383, z 384, a 400, exchange 416-419;
+// TMEM: causal  T 0-127, O 128-255, S 256-383, exchange 416-419;
 //       non-causal  O 0-127 / 128-255, exchange 256-259.
 // ----------------------------------------------------------------------------------------------------
 template <bool CAUSAL>
@@ -197,8 +224,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
     unsigned char *stages = sm;
     unsigned char *Sb = sm + NST * STAGE;               // bf16 state, [d][e], two 64-column boxes
-    unsigned char *ones = Sb + QB;                      // 8 rows x 128 B of bf16 1.0 (the N = 16 operand)
-    float *zc = (float *)(ones + 1024);                 // running z (fp32, D)
+    float *zc = (float *)(Sb + QB);                     // running z (fp32, D)
     float *ac = zc + D;                                 // running a (fp32, D)
     uint64_t *full = (uint64_t *)(ac + D);
     uint64_t *empty = full + NST;
@@ -226,8 +252,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -240,7 +264,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     griddep_wait();
     griddep_launch_dependents();
     const uint32_t tmem = *tslot;
-    const uint32_t tT = tmem, tS = tmem + 256, tZ = tmem + 384, tA = tmem + 400;
+    const uint32_t tT = tmem, tS = tmem + 256;
     const uint32_t tX = tmem + (CAUSAL ? 416 : 256);
 
     if (warp == 0 && lane == 0) {
@@ -286,8 +310,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
         const uint32_t idMM = idesc_bf16(128, 128, true, true);
-        const uint32_t idZ = idesc_bf16(128, 16, true, false);
-        const uint32_t sb = smem_u32(Sb), on = smem_u32(ones);
+        const uint32_t sb = smem_u32(Sb);
         int it = 0, pno = 0;
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
@@ -330,14 +353,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 if (CAUSAL) {
                     if (c + 1 < pc.e) {
 #pragma unroll
-                        for (int k = 0; k < kC / 16; ++k) {  // S += K^T V, z += K^T 1, a += V^T 1
-                            const uint64_t kt = sdesc_sw128(kb + 2048 * k, kBox, 1024);
-                            const uint64_t vt = sdesc_sw128(vb + 2048 * k, kBox, 1024);
-                            const uint64_t o1 = sdesc_sw128(on + 32 * (k & 3), 16, 0);
-                            mma_ss(tS, kt, vt, idMM, 1u);
-                            mma_ss(tZ, kt, o1, idZ, 1u);
-                            mma_ss(tA, vt, o1, idZ, 1u);
-                        }
+                        for (int k = 0; k < kC / 16; ++k)  // S += K^T V
+                            mma_ss(tS, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
+                                   idMM, 1u);
                     }
                     mma_commit(barS);
                 }
@@ -359,7 +377,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 tc_fence_after();
             }
             load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
-                                hf, tS + lo, tZ + lo, tA + lo, Sb, zc, ac, CAUSAL, true);
+                                hf, tS + lo, 0u, 0u, Sb, zc, ac, CAUSAL, false);
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
@@ -373,6 +391,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 unsigned char *st = stages + s * STAGE;
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
+                // this chunk's z_c[i] (half 0) or a_c[i] (half 1), from the sums kernel (causal)
+                const float zav = CAUSAL ? P.chunk_za[((size_t)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i] : 0.f;
                 float part = 0.f;
                 if (CAUSAL) {
                     // P = [j <= i](1 + T) for this half's columns j; r_i partial sum in fp32
@@ -418,10 +438,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                     tc_fence_after();
                     if (c + 1 < pc.e) {
                         tmem_half_to_tile(tS + lo, Sb, i, hf);
-                        uint32_t za, zb;
-                        tmem_ld2((hf == 0 ? tZ : tA) + lo, za, zb);
-                        tmem_wait_ld(za, zb);
-                        vn = __uint_as_float(za);
+                        vn = (hf == 0 ? zc : ac)[i] + zav;  // z_c, a_c of this chunk from the sums kernel
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(barSb);
@@ -580,8 +597,8 @@ bool make_map(CUtensorMap *m, const void *ptr, const Plan &p) {
 }
 
 constexpr size_t kSmemAgg = 3 * 2 * 2 * (size_t)tc::kBox + 2048 + 256;
-constexpr size_t kSmemFwdCausal = 2 * 3 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 1024 + 256;
-constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 1024 + 256;
+constexpr size_t kSmemFwdCausal = 2 * 3 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
+constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
 static_assert(kSmemFwdCausal <= 232448, "forward kernel exceeds the shared-memory limit");
 
 bool set_smem_attrs() {
@@ -613,6 +630,7 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     P.N = p.N;
     P.slot_stride = p.stride;
     P.slots = (float *)(ws + p.off_states);
+    P.chunk_za = (float *)(ws + p.off_chunkza);
     P.status = (uint32_t *)ws;
     return true;
 }

@@ -26,6 +26,7 @@ struct TcParams {
     void *dQ, *dK, *dV;     // backward outputs (bf16)
     float *rs_g, *rs_dt;    // backward row statistics: g_i and delta_i / g_i
     float *chunk_ye;        // causal backward: per chunk, y_c = sum dt_i q_i then e_c = sum dO_i / g_i
+    float *chunk_za;        // per chunk: z_c = sum k_j then a_c = sum v_j (written by the sums kernel)
     const void *Kp, *Vp;    // K and V: with the shape they identify the per-piece sums in the workspace
     int check_tag;          // backward reusing the forward's sums: 0 no check, else the form expected + 1
     float *combine_slots;   // tc_combine_kernel: the slot array it turns into carries

@@ -58,6 +58,10 @@ def load_library():
         lib.la_backward.restype = i
         lib.la_backward_with_forward_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
         lib.la_backward_with_forward_state.restype = i
+        lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.la_decode_step.restype = i
+        lib.la_state_append.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+        lib.la_state_append.restype = i
         lib.la_get_status.argtypes = [vp, vp]
         lib.la_get_status.restype = i
         _lib = lib
@@ -173,3 +177,58 @@ def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspa
 def la_get_status(workspace, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status recorded in the workspace."""
     return int(load_library().la_get_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+class DecodeState:
+    """The carried state of the recurrent (decode) form, per (b, h): S [B,H,D,D], z [B,H,D], a [B,H,D] of
+    the accumulator type (float32 for bf16 tokens, float64 for float32 tokens) and the count n (int32
+    [B,H]).  Zero-filled is the empty state; the library updates the tensors in place."""
+
+    def __init__(self, B: int, H: int, D: int, token_dtype, device="cuda"):
+        import torch
+        acc = torch.float32 if token_dtype == torch.bfloat16 else torch.float64
+        if token_dtype not in (torch.bfloat16, torch.float32):
+            raise TypeError(f"unsupported dtype {token_dtype}: use torch.bfloat16 or torch.float32")
+        self.B, self.H, self.D, self.token_dtype = B, H, D, token_dtype
+        self.S = torch.zeros((B, H, D, D), dtype=acc, device=device)
+        self.z = torch.zeros((B, H, D), dtype=acc, device=device)
+        self.a = torch.zeros((B, H, D), dtype=acc, device=device)
+        self.n = torch.zeros((B, H), dtype=torch.int32, device=device)
+
+    def _args(self):
+        return _ptr(self.S), _ptr(self.z), _ptr(self.a), _ptr(self.n)
+
+
+def la_decode_step(state: DecodeState, q, k, v, o=None, normaliser=None, stream=None):
+    """o, g = la_decode_step(state, q, k, v): append one token per (b, h) ([B,H,D] tensors) to ``state``
+    and return its output and normaliser (row n - 1 of the causal forward over the tokens taken so far)."""
+    import torch
+    if q.dim() != 3 or tuple(q.shape) != (state.B, state.H, state.D):
+        raise ValueError(f"expected [B, H, D] = {(state.B, state.H, state.D)} tokens, got {tuple(q.shape)}")
+    for t in (k, v, o):
+        if t is not None and (t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous()):
+            raise ValueError("q, k, v, o must share shape and dtype and be contiguous")
+    if q.dtype != state.token_dtype:
+        raise ValueError("token dtype does not match the state")
+    o = torch.empty_like(q) if o is None else o
+    if normaliser is None:
+        normaliser = torch.empty((state.B, state.H), dtype=torch.float32, device=q.device)
+    st = load_library().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(normaliser), *state._args(),
+                                       state.B, state.H, state.D, _dtype_code(q), _stream_ptr(stream))
+    if st != 0:
+        raise LAError(st, "la_decode_step")
+    return o, normaliser
+
+
+def la_state_append(state: DecodeState, K, V, stream=None):
+    """Append N tokens per (b, h) ([B,H,N,D] tensors) to ``state``: S += K^T V, z += sum k, a += sum v,
+    n += N."""
+    B, H, N, D = _shape(K)
+    _check_like(K, V)
+    if (B, H, D) != (state.B, state.H, state.D) or K.dtype != state.token_dtype:
+        raise ValueError("K, V do not match the state's B, H, D and token dtype")
+    st = load_library().la_state_append(_ptr(K), _ptr(V), *state._args(), B, H, N, D, _dtype_code(K),
+                                        _stream_ptr(stream))
+    if st != 0:
+        raise LAError(st, "la_state_append")
+    return state

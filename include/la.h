@@ -136,6 +136,38 @@ int la_forward_noalloc(const void *Q, const void *K, const void *V, int causal, 
                        int H, int N, int D, int dtype, void *stream);
 
 /*
+ * Recurrent (decode) form of the causal head.  The causal forward carries, per (b, h), the state of the
+ * tokens taken so far (sciencestack.ai page, TL;DR: O(N D^2) time with an O(D^2) state); a decoder can
+ * keep that state and take one token at a time instead of re-running the forward:
+ *   S = sum_j k_j v_j^T  (S[d][e] = sum_j k_j[d] v_j[e]),  z = sum_j k_j,  a = sum_j v_j,  n = count.
+ * State arrays (device, owned by the caller, updated in place; zero-filled = the empty state):
+ *   S  [B,H,D,D],  z [B,H,D],  a [B,H,D]  of the accumulator type: float for LA_BF16, double for LA_F32
+ *   n  int [B,H]
+ * Rows are independent over (b, h); different heads may hold different counts n.  Pointers must be
+ * 16-byte aligned, the state arrays must not overlap each other or any token input or output.  Neither
+ * call needs a workspace or reports device-side status.
+ */
+
+/*
+ * One token per (b, h): appends (k, v) to the state, then
+ *   g = n + q . z,   o = (a + S^T q) / g        (state after the append; o rounded once to dtype)
+ * which is row n - 1 of la_forward(causal = 1) over the tokens taken so far.
+ *   q, k, v     in : [B,H,D] of `dtype`
+ *   o           out: [B,H,D] of `dtype`
+ *   normaliser  out: float [B,H] with g, or NULL
+ */
+int la_decode_step(const void *q, const void *k, const void *v, void *o, float *normaliser, void *S, void *z,
+                   void *a, int *n, int B, int H, int D, int dtype, void *stream);
+
+/*
+ * Appends N >= 0 tokens per (b, h) to the state (a prompt, or a block of tokens whose outputs the caller
+ * takes from la_forward): S += K^T V, z += sum k, a += sum v, n += N.
+ *   K, V  in : [B,H,N,D] of `dtype` (may be NULL when N = 0)
+ */
+int la_state_append(const void *K, const void *V, void *S, void *z, void *a, int *n, int B, int H, int N, int D,
+                    int dtype, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the sticky device status recorded in `workspace`
  * by earlier calls (LA_OK, LA_ERR_TIMEOUT, LA_ERR_BOUNDS or LA_ERR_STATE), or LA_ERR_CUDA if the stream
  * failed.

@@ -186,3 +186,36 @@ def prefix_backward(Q, K, V, dO, causal: bool, c: float = 1.0, threads: int = 0)
     _check(_load().la_prefix_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, H, N, D, int(causal), c, _ptr(dQ),
                                       _ptr(dK), _ptr(dV), threads), "prefix_backward")
     return dQ, dK, dV
+
+
+# ---------------------------------------------------------------- recurrent (decode) form ---
+# The causal forward written as a recurrence over tokens.  The state of the tokens taken so far is
+# S = sum_j k_j v_j^T (S[d][e] = sum_j k_j[d] v_j[e]), z = sum_j k_j, a = sum_j v_j and their count n:
+# the d x d state that accumulates one outer product k_t v_t^T per time step (cloud.baidu.com article
+# 9404082, section 2, the state-matrix recurrence), with the normalisation of the reading above, so that
+# token t's output g_t = c n + q_t . z, o_t = (c a + S^T q_t) / g_t equals row t of the causal forward.
+# Plain numpy in float64; every array is [B, H, ...].
+
+def state_append(S, z, a, n, K, V):
+    """State after appending tokens K, V ([B,H,T,D]) to (S [B,H,D,D], z [B,H,D], a [B,H,D], n [B,H])."""
+    K, V = _f64(K), _f64(V)
+    S2 = _f64(S) + np.einsum("bhtd,bhte->bhde", K, V)
+    z2 = _f64(z) + K.sum(axis=2)
+    a2 = _f64(a) + V.sum(axis=2)
+    n2 = np.asarray(n, dtype=np.int64) + K.shape[2]
+    return S2, z2, a2, n2
+
+
+def decode_step(S, z, a, n, q, k, v, c: float = 1.0):
+    """One token per (b, h) (q, k, v [B,H,D]): appends (k, v), then g = c n + q . z and
+    o = (c a + S^T q) / g on the new state.  Returns (o [B,H,D], g [B,H], S, z, a, n)."""
+    S2, z2, a2, n2 = state_append(S, z, a, n, _f64(k)[:, :, None, :], _f64(v)[:, :, None, :])
+    q = _f64(q)
+    g = c * n2 + np.einsum("bhd,bhd->bh", q, z2)
+    o = (c * a2 + np.einsum("bhde,bhd->bhe", S2, q)) / g[..., None]
+    return o, g, S2, z2, a2, n2
+
+
+def empty_state(B: int, H: int, D: int):
+    """The state of no tokens."""
+    return (np.zeros((B, H, D, D)), np.zeros((B, H, D)), np.zeros((B, H, D)), np.zeros((B, H), dtype=np.int64))

@@ -103,3 +103,30 @@ def test_backward_rejects_bad_arguments_on_host(lib, entry):
     bad[5] = base[0] + 16                             # dQ overlaps Q
     assert call(bad) == 1
     assert call(wsb=100) == 3
+
+
+def test_decode_entries_reject_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+    tok = [0x1000_0000 * (i + 1) for i in range(4)]          # q, k, v, o
+    st = [0x9000_0000 + 0x100_0000 * i for i in range(4)]     # S, z, a, n
+
+    def step(t=tok, s=st, g=0, B=1, H=2, D=64, dt=1):
+        return lib.la_decode_step(*[vp(p) for p in t], vp(g), *[vp(p) for p in s], B, H, D, dt, vp(0))
+
+    def append(K=0x1000_0000, V=0x2000_0000, s=st, N=8, D=64, dt=1):
+        return lib.la_state_append(vp(K), vp(V), *[vp(p) for p in s], 1, 2, N, D, dt, vp(0))
+
+    assert step(D=48) == 2
+    assert step(dt=5) == 1
+    assert step(B=0) == 1
+    assert step(t=[0] + tok[1:]) == 1                          # null q
+    assert step(t=tok[:3] + [tok[0]]) == 1                     # o aliases q
+    assert step(s=[st[0], st[0] + 64] + st[2:]) == 1           # z inside S
+    assert step(s=st[:3] + [0]) == 1                           # null n
+    assert step(s=[st[0] + 8] + st[1:]) == 1                   # misaligned S
+    assert step(g=tok[0]) == 1                                 # normaliser inside q
+    assert append(D=24) == 2
+    assert append(N=-1) == 1
+    assert append(K=0) == 1
+    assert append(s=[0x1000_0000] + st[1:]) == 1               # S overlaps K
+    assert append(K=0, V=0, N=0) == 0                          # nothing to append: nothing launched

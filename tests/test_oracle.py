@@ -12,7 +12,9 @@ causal mask, or a transposed operand (q_j . k_i).
   * invariants: rows of the normalised weights sum to one; causal outputs ignore future tokens;
     shifting V by a constant row shifts O by it; O is linear in V;
   * closed forms: K = 0 or Q = 0 gives (prefix) means of V, N = 1 gives O = V, c = 0 with D = 1
-    gives a q-independent ratio, and the matching gradients.
+    gives a q-independent ratio, and the matching gradients;
+  * the recurrent (decode) form: token by token it reproduces the hand-worked causal values and the
+    explicit causal rows, and a block append followed by decoding continues the forward.
 """
 import os
 from fractions import Fraction
@@ -245,3 +247,54 @@ def test_conditioning_of_tiny_case(oracle_lib):
     _, g = oracle_lib.forward(x["Q"], x["K"], x["V"], True)
     n = np.arange(1, 65, dtype=np.float64)
     assert np.min(g / n) > 0.1
+
+
+# ------------------------------------------------------------- recurrent (decode) form ---
+
+def _decode_all(oracle_lib, x, start_state=None):
+    B, H, N, D = x["Q"].shape
+    st = oracle_lib.empty_state(B, H, D) if start_state is None else start_state
+    outs, gs = [], []
+    for t in range(N):
+        o, g, *st = oracle_lib.decode_step(*st, x["Q"][:, :, t], x["K"][:, :, t], x["V"][:, :, t])
+        outs.append(o)
+        gs.append(g)
+    return np.stack(outs, axis=2), np.stack(gs, axis=2), st
+
+
+def test_decode_golden_d1_worked_example(oracle_lib):
+    """Token by token, the recurrence reproduces the hand-worked causal outputs and normalisers."""
+    gv = _load_golden()
+    x = {n: np.array([gv[("input", m, i)] for i in range(3)]).reshape(1, 1, 3, 1)
+         for n, m in (("Q", "q"), ("K", "k"), ("V", "v"))}
+    O, g, st = _decode_all(oracle_lib, x)
+    for i in range(3):
+        assert abs(O.reshape(-1)[i] - gv[("1", "O", i)]) <= 1e-15
+        assert abs(g.reshape(-1)[i] - gv[("1", "g", i)]) <= 1e-15
+    assert int(st[3].reshape(-1)[0]) == 3
+
+
+@pytest.mark.parametrize("shape", [(2, 2, 20, 5), (1, 1, 1, 3), (1, 3, 9, 1)])
+def test_decode_matches_explicit_causal_rows(oracle_lib, shape):
+    """Output t of the recurrence is row t of the explicit (N x N weights) causal forward."""
+    B, H, N, D = shape
+    x = _tiny(seed=21, B=B, H=H, N=N, D=D)
+    O_ref, g_ref = oracle_lib.forward(x["Q"], x["K"], x["V"], True)
+    O, g, _ = _decode_all(oracle_lib, x)
+    assert _rel(O, O_ref) < 1e-13 and _rel(g, g_ref) < 1e-13
+
+
+def test_state_append_then_decode_continues_the_forward(oracle_lib):
+    """A block of T tokens appended at once, then the rest decoded one by one: the outputs are rows
+    T.. of the explicit causal forward over all tokens, and the final state equals the token-by-token
+    one (appending is order- and grouping-free)."""
+    x = _tiny(seed=22, B=1, H=2, N=30, D=6)
+    O_ref, _ = oracle_lib.forward(x["Q"], x["K"], x["V"], True)
+    T = 17
+    st = oracle_lib.state_append(*oracle_lib.empty_state(1, 2, 6), x["K"][:, :, :T], x["V"][:, :, :T])
+    rest = {k: v[:, :, T:] for k, v in x.items()}
+    O, _, st_end = _decode_all(oracle_lib, rest, start_state=st)
+    assert _rel(O, O_ref[:, :, T:]) < 1e-13
+    _, _, st_seq = _decode_all(oracle_lib, x)
+    for a_, b_ in zip(st_end, st_seq):
+        assert np.max(np.abs(np.asarray(a_, dtype=np.float64) - b_)) < 1e-12

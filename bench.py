@@ -446,6 +446,105 @@ def run_reference(args):
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ---------------------------------------------------------------------- decode workload ---
+
+DEC_B, DEC_H = 256, 16  # sequences decoded together, heads each (D as above, bf16 tokens, fp32 state)
+
+
+def decode_alg_bytes(bh: int) -> int:
+    """HBM bytes of one decode step: the fp32 state S read and written, z and a read and written, the
+    counts, q, k, v read and o written (bf16), the fp32 normaliser written."""
+    return bh * (2 * D * D * 4 + 4 * D * 4 + 2 * 4 + 4 * D * ELEM + 4)
+
+
+def run_decode(args):
+    """One decode step = one token for each of DEC_B sequences (all DEC_H heads) through la_decode_step,
+    from the state of a 4096-token prompt.  The 268 MB state is larger than L2, so every step streams it
+    from HBM."""
+    import numpy as np
+    import torch
+
+    from bwd_la_fwd_gb300 import inputs, la
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    la.load_library()
+    bh = DEC_B * DEC_H
+    host = inputs.generate(DEC_B, DEC_H, 1, D, seed=2, dtype="bf16")
+    tok = {n: torch.from_numpy(host[n].reshape(DEC_B, DEC_H, D).view(np.int16)).view(torch.bfloat16).pin_memory()
+           for n in ("Q", "K", "V")}
+    q, k, v = (tok[n].to(dev) for n in ("Q", "K", "V"))
+    state = la.DecodeState(DEC_B, DEC_H, D, torch.bfloat16, device=dev)
+    Kp = torch.randn(DEC_B, DEC_H, N, D, device=dev, dtype=torch.bfloat16) / D ** 0.5
+    Vp = torch.randn(DEC_B, DEC_H, N, D, device=dev, dtype=torch.bfloat16)
+    la.la_state_append(state, Kp, Vp)  # the prompt (appended once, untimed)
+    del Kp, Vp
+    o = torch.empty_like(q)
+    g = torch.empty((DEC_B, DEC_H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    for _ in range(max(args.warmup, 3)):
+        la.la_decode_step(state, q, k, v, o=o, normaliser=g)
+    torch.cuda.synchronize()
+    launches0 = la.la_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        la.la_decode_step(state, q, k, v, o=o, normaliser=g)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    launches = la.la_launch_count() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    # end to end: this step's tokens in from pinned host memory, its outputs back, every step
+    host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    host_g = torch.empty(g.shape, dtype=g.dtype, pin_memory=True)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        for dst, n in ((q, "Q"), (k, "K"), (v, "V")):
+            dst.copy_(tok[n], non_blocking=True)
+        la.la_decode_step(state, q, k, v, o=o, normaliser=g)
+        host_o.copy_(o, non_blocking=True)
+        host_g.copy_(g, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    e2e_ms = x0.elapsed_time(x1) / args.steps
+    hbm, _, peak_kind = measured_peaks()
+    achieved = decode_alg_bytes(bh) / (ms * 1e-3) / 1e9
+    clocks = sampler.summary(t0, t1)
+    line = {
+        "metric": f"LA decode tokens/s (one token per sequence per step) at B={DEC_B} H={DEC_H} D={D}",
+        "value": DEC_B / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"LA decode step B={DEC_B} H={DEC_H} D={D} bf16 tokens, fp32 state after a "
+                               f"{N}-token prompt", "l2": "state 268 MB > L2, no flush"},
+        "roofline": {"bound": "hbm", "call": "la_decode_step", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_kind,
+                     "alg_bytes_per_launch": decode_alg_bytes(bh), "avg_us": ms * 1e3},
+        "e2e": {"value": DEC_B / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 3 * q.numel() * ELEM,
+                "d2h_bytes_per_step": o.numel() * ELEM + g.numel() * 4, "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches), "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        st = tuple(t.detach().double().cpu().numpy() if t.dtype != torch.int32 else t.cpu().numpy().astype(np.int64)
+                   for t in (state.S, state.z, state.a, state.n))
+        f = {n: inputs.to_f64(host[n].reshape(DEC_B, DEC_H, D), "bf16") for n in ("Q", "K", "V")}
+        reps, c0 = 0, time.perf_counter()
+        while reps < 2 or (time.perf_counter() - c0 < 10.0 and reps < 50):
+            oracle.decode_step(*st, f["Q"], f["K"], f["V"])
+            reps += 1
+        sec = (time.perf_counter() - c0) / reps
+        line["cpu_baseline"] = {"value": DEC_B / sec, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+                                "sample": f"fp64 numpy decode_step over the whole batch, {reps} steps ({sec:.2f} s each)"}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,12 +553,17 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=0, help="heads per reference step (default: one per core)")
+    ap.add_argument("--workload", choices=("attention", "decode"), default="attention",
+                    help="attention: the fwd+bwd hot path (default); decode: the recurrent decode step")
     ap.add_argument("--profile", action="store_true",
                     help="run only warm-up + timed steps of the hot path (for ncu); prints a reduced line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.workload == "decode":
+        line = run_decode(args) if args.impl == "ours" and dist_env()[0] == 0 else None
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
     rank, world, _ = dist_env()

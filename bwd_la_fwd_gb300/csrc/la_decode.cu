@@ -11,18 +11,19 @@
 // which is row t of the causal forward (W_tj = 1 + q_t . k_j over j <= t).
 //
 // A step reads and writes the D x D state once and touches O(D) of everything else, so it is bound by
-// HBM (or by launch latency for few heads).  Each head is spread over a thread-block cluster of R CTAs
-// (R = D / 32, at least 1, at most 8); CTA r owns rows [r D / R, (r + 1) D / R) of S, updates them in
-// place and forms its partial column sums of S^T q; rank 0 adds the R partials through distributed
-// shared memory and writes o, g, z, a and n.  Every element of the state is read and written by one
-// thread only, so the update is safe in place.  Accumulation type: fp32 for bf16 I/O, fp64 for fp32 I/O
-// (the state carries sums over many tokens).
+// HBM (or by launch latency for few heads).  Each head's S moves as up to 64 KB slabs of contiguous rows,
+// one untiled TMA bulk copy each way per CTA, which keeps three slabs in flight per SM; a head whose
+// state is larger than one slab (D = 256, or fp64 state at D = 128) is spread over a thread-block
+// cluster, whose CTAs combine their partial sums through distributed shared memory.  Every element of
+// the state is written back by the CTA that read it, so the update is safe in place.  Accumulation type:
+// fp32 for bf16 I/O, fp64 for fp32 I/O (the state carries sums over many tokens).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "../../include/la.h"
 #include "la_internal.h"
+#include "la_sm100.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -44,88 +45,126 @@ template <> __device__ __forceinline__ __nv_bfloat16 store_as<__nv_bfloat16, flo
     return __float2bfloat16_rn(x);
 }
 
-__host__ __device__ constexpr int parts_of(int D) { return D / 32 < 1 ? 1 : (D / 32 > 8 ? 8 : D / 32); }
+// How a decode step spreads one head's state over the CTAs of its cluster: each CTA takes ROWS rows of S
+// (at most kSlab bytes, so that it fits in shared memory next to two more CTAs on the SM), and its
+// threads take 16-byte vectors of a row: CG vectors per row, RG rows at a time, RR rows each.
+constexpr int kSlab = 65536;
+template <typename Acc, int D> struct DecSplit {
+    static constexpr int R = (int)(((long long)D * D * sizeof(Acc) + kSlab - 1) / kSlab);  // CTAs per head
+    static constexpr int ROWS = D / R;
+    static constexpr int VEC = 16 / (int)sizeof(Acc);
+    static constexpr int CG = D / VEC;
+    static constexpr int RG = kThreads / CG < ROWS ? kThreads / CG : ROWS;
+    static constexpr int RR = ROWS / RG;
+    static constexpr uint32_t BYTES = (uint32_t)(ROWS * D * sizeof(Acc));
+    static_assert(D % R == 0 && ROWS % RG == 0 && R <= 8, "decode split");
+};
 
-// One decode step.  grid = BH * R CTAs in clusters of R; block = 256 threads: thread t owns column
-// e = t % D and, of this CTA's rows, those congruent to t / D modulo 256 / D.
+// One decode step.  grid = BH * R CTAs in clusters of R (one cluster per head).  CTA r bulk-copies rows
+// [r ROWS, (r + 1) ROWS) of the head's S into shared memory (one TMA transfer), updates them there
+// (S += k v^T), forms its partial column sums of S^T q, and bulk-copies the rows back; rank 0 adds the
+// R partials through distributed shared memory and writes o, g, z, a and n.  A copy that does not land
+// within the bounded wait leaves the state untouched and writes NaN to o.
 template <typename T, typename Acc, int D>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                                                                const T *__restrict__ v, T *__restrict__ o,
                                                                float *__restrict__ g_out, Acc *S, Acc *z, Acc *a,
                                                                int *n) {
-    constexpr int R = parts_of(D);
-    constexpr int ROWS = D / R;          // rows of S per CTA
-    constexpr int RP = kThreads / D;     // row groups per CTA (threads per column)
-    constexpr int RG = RP < ROWS ? RP : ROWS;  // row groups that have rows
-    constexpr int RR = ROWS / RG;        // rows per thread
-    static_assert(ROWS % RG == 0, "rows split evenly");
+    using C = DecSplit<Acc, D>;
+    extern __shared__ __align__(128) unsigned char slab_raw[];
+    Acc *slab = (Acc *)slab_raw;  // ROWS x D, row-major, as in global memory
     __shared__ Acc qs[D], ks[D];
-    __shared__ Acc red[RG][D];
+    __shared__ Acc red[C::RG][D];
     __shared__ Acc part[D];
     __shared__ Acc gsh;
+    __shared__ uint64_t bar;
+    __shared__ int landed;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    const long long head = blockIdx.x / R;
+    const long long head = blockIdx.x / C::R;
     const int t = threadIdx.x;
+    Acc *rows = S + head * D * D + (long long)rank * C::ROWS * D;
+    if (t == 0) {
+        sm100::mbar_init(&bar, 1);
+        sm100::fence_mbar_init();
+        sm100::mbar_arrive_expect_tx(&bar, C::BYTES);
+        sm100::bulk_load(slab, rows, C::BYTES, &bar);
+    }
     for (int x = t; x < D; x += kThreads) {
         qs[x] = load_acc<Acc>(q + head * D + x);
         ks[x] = load_acc<Acc>(k + head * D + x);
     }
-    __syncthreads();
-    const int e = t % D, p = t / D;
-    if (p < RG) {
-        const Acc ve = load_acc<Acc>(v + head * D + e);
-        Acc *Sh = S + head * D * D;
-        const int d0 = rank * ROWS + p;
-        Acc s[RR];
+    if (t == 0) landed = sm100::mbar_wait(&bar, 0, 2000000000ull) ? 1 : 0;
+    __syncthreads();  // q, k in shared memory; the slab has landed (or the wait gave up)
+    const bool ok = landed != 0;
+    const int cgi = t % C::CG, p = t / C::CG;
+    if (ok && p < C::RG) {
+        Acc ve[C::VEC], acc[C::VEC];
 #pragma unroll
-        for (int m = 0; m < RR; ++m) s[m] = Sh[(long long)(d0 + RG * m) * D + e];  // all loads in flight
-        Acc acc = 0;
-#pragma unroll
-        for (int m = 0; m < RR; ++m) {
-            const int d = d0 + RG * m;
-            s[m] += ks[d] * ve;
-            Sh[(long long)d * D + e] = s[m];
-            acc += s[m] * qs[d];
+        for (int j = 0; j < C::VEC; ++j) {
+            ve[j] = load_acc<Acc>(v + head * D + cgi * C::VEC + j);
+            acc[j] = 0;
         }
-        red[p][e] = acc;
+#pragma unroll 4
+        for (int m = 0; m < C::RR; ++m) {
+            const int row = p + C::RG * m, d = rank * C::ROWS + row;
+            uint4 *cell = (uint4 *)(slab + (long long)row * D + cgi * C::VEC);
+            uint4 raw = *cell;
+            Acc *sv = (Acc *)&raw;
+            const Acc kd = ks[d], qd = qs[d];
+#pragma unroll
+            for (int j = 0; j < C::VEC; ++j) {
+                sv[j] += kd * ve[j];
+                acc[j] += sv[j] * qd;
+            }
+            *cell = raw;
+        }
+#pragma unroll
+        for (int j = 0; j < C::VEC; ++j) red[p][cgi * C::VEC + j] = acc[j];
     }
+    sm100::fence_proxy_async_smem();  // the slab's new values, before the bulk store reads them
     __syncthreads();
+    if (ok && t == 0) {
+        sm100::bulk_store(rows, slab, C::BYTES);
+        sm100::bulk_commit();
+    }
     if (t < D) {
         Acc sum = 0;
 #pragma unroll
-        for (int r = 0; r < RG; ++r) sum += red[r][t];
+        for (int r = 0; r < C::RG; ++r) sum += red[r][t];
         part[t] = sum;
     }
-    if (rank == 0) {  // g = n' + q . z' (z' = z + k), over warp 0
-        if (t < 32) {
-            Acc dz = 0;
-            for (int x = t; x < D; x += 32) {
-                const Acc zn = z[head * D + x] + ks[x];
-                z[head * D + x] = zn;
-                dz += qs[x] * zn;
-            }
+    if (rank == 0 && t < 32) {  // g = n' + q . z' (z' = z + k)
+        Acc dz = 0;
+        for (int x = t; x < D; x += 32) {
+            const Acc zn = z[head * D + x] + ks[x];
+            if (ok) z[head * D + x] = zn;
+            dz += qs[x] * zn;
+        }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) dz += __shfl_xor_sync(0xffffffffu, dz, off);
-            if (t == 0) {
-                const int nn = n[head] + 1;
-                n[head] = nn;
-                gsh = (Acc)nn + dz;
-            }
+        for (int off = 16; off > 0; off >>= 1) dz += __shfl_xor_sync(0xffffffffu, dz, off);
+        if (t == 0) {
+            const int nn = n[head] + 1;
+            if (ok) n[head] = nn;
+            gsh = (Acc)nn + dz;
         }
     }
     cluster.sync();  // every CTA's partial sums are in its shared memory
     if (rank == 0 && t < D) {
         Acc tot = part[t];
 #pragma unroll
-        for (int r = 1; r < R; ++r) tot += *cluster.map_shared_rank(&part[t], r);
+        for (int r = 1; r < C::R; ++r) tot += *cluster.map_shared_rank(&part[t], r);
         const Acc an = a[head * D + t] + load_acc<Acc>(v + head * D + t);
-        a[head * D + t] = an;
+        if (ok) a[head * D + t] = an;
         const Acc g = gsh;
-        o[head * D + t] = store_as<T, Acc>((an + tot) / g);
+        o[head * D + t] = ok ? store_as<T, Acc>((an + tot) / g) : store_as<T, Acc>((Acc)NAN);
         if (g_out && t == 0) g_out[head] = (float)g;
     }
     cluster.sync();  // rank 0 has read every partial before any CTA of the cluster exits
+    if (t == 0) {
+        if (ok) sm100::bulk_wait0();                    // the state rows are written back before the CTA exits
+        else sm100::mbar_wait(&bar, 0, 2000000000ull);  // a late copy lands before the slab is released
+    }
 }
 
 // Appends N tokens to the state: S += K^T V, z += sum k, a += sum v, n += N, for each head.
@@ -191,10 +230,19 @@ __global__ void __launch_bounds__(kThreads) state_append_kernel(const T *__restr
 template <typename T, typename Acc, int D>
 cudaError_t launch_step(const void *q, const void *k, const void *v, void *o, float *g, void *S, void *z, void *a,
                         int *n, long long BH, cudaStream_t s) {
-    constexpr int R = parts_of(D);
+    using C = DecSplit<Acc, D>;
+    constexpr int R = C::R;
+    static int attr_set = 0;  // the slab can exceed the 48 KB default window
+    if (!attr_set) {
+        const cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<T, Acc, D>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = 1;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(BH * R));
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -287,7 +335,7 @@ int la_decode_step(const void *q, const void *k, const void *v, void *o, float *
     const size_t ib[5] = {vb, vb, vb, vb, (size_t)(BH > 0 ? BH : 0) * 4};
     int rc = check_state(B, H, D, dtype, S, z, a, n, ins, ib, 5);
     if (rc) return rc;
-    if (BH * parts_of(D) >= (1LL << 31)) return LA_ERR_INVALID_ARG;  // grid size
+    if (BH * 8 >= (1LL << 31)) return LA_ERR_INVALID_ARG;  // grid size (at most 8 CTAs per head)
     // the outputs must not overlap the token inputs either
     if (overlap(o, vb, q, vb) || overlap(o, vb, k, vb) || overlap(o, vb, v, vb)) return LA_ERR_INVALID_ARG;
     if (normaliser && (overlap(normaliser, ib[4], q, vb) || overlap(normaliser, ib[4], k, vb) ||

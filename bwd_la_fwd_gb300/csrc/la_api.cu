@@ -33,6 +33,7 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     p->causal = causal ? 1 : 0;
     p->dtype = dtype;
     p->BH = (int)BH;
+    for (int k = 0; k < kNumOps; ++k) p->lay[k] = Layout{(long long)H * N * D, (long long)N * D, (long long)D};
     long long seg = 256 > 2 * D ? 256 : 2 * D;
     long long min_for_cap = ((long long)N + 63) / 64;
     min_for_cap = (min_for_cap + 31) / 32 * 32;
@@ -98,15 +99,75 @@ int check_workspace(const Plan &p, void *ws, size_t ws_bytes, bool backward) {
     return LA_OK;
 }
 
-// Outputs must not overlap any input, the workspace or each other.
-int check_aliasing(const Range *outs, int n_out, const Range *ins, int n_in) {
-    for (int i = 0; i < n_out; ++i) {
-        for (int j = 0; j < n_in; ++j)
-            if (overlap(outs[i], ins[j])) return LA_ERR_INVALID_ARG;
-        for (int j = i + 1; j < n_out; ++j)
-            if (overlap(outs[i], outs[j])) return LA_ERR_INVALID_ARG;
+// ---- strided operands -------------------------------------------------------------------------
+// Each operand is given by its (batch, head, row) element strides; its D row elements are contiguous.
+// An operand is accepted when its rows cannot overlap one another: ordered by stride, the dimensions of
+// extent > 1 nest (the smallest stride is at least D, each larger one at least the previous stride
+// times its extent), and every stride is a multiple of 16 bytes (the tensor-map rule).
+
+// Sets p.lay[op] from strides[0..2] (batch, head, row); a dimension of extent 1 is never stepped, so its
+// stride is replaced by one that is always valid.
+int set_layout(Plan &p, int op, const long long *st, int elem) {
+    const long long ext[3] = {p.B, p.H, p.N};
+    long long s[3] = {st[0], st[1], st[2]};
+    for (int k = 0; k < 3; ++k) {
+        if (ext[k] == 1) s[k] = p.D;
+        if (s[k] < 1 || s[k] >= (1LL << 40) / elem || (s[k] * elem) % 16 != 0) return LA_ERR_INVALID_ARG;
     }
+    int idx[3] = {0, 1, 2};  // dimensions by increasing stride
+    for (int a = 0; a < 3; ++a)
+        for (int b = a + 1; b < 3; ++b)
+            if (s[idx[b]] < s[idx[a]]) { const int t = idx[a]; idx[a] = idx[b]; idx[b] = t; }
+    long long need = p.D;
+    for (int k = 0; k < 3; ++k) {
+        const int d = idx[k];
+        if (ext[d] == 1) continue;
+        if (s[d] < need) return LA_ERR_INVALID_ARG;  // rows would overlap
+        need = s[d] * ext[d];
+    }
+    p.lay[op] = la::Layout{s[0], s[1], s[2]};
     return LA_OK;
+}
+
+// Elements from an operand's base to one past its last element.
+long long span_of(const Plan &p, const la::Layout &l) {
+    return (p.B - 1) * l.sb + (p.H - 1) * l.sh + (p.N - 1) * l.sn + p.D;
+}
+
+// Whether some row of an operand starting `delta` elements after another one of the same layout meets a
+// row of that one: delta = db sb + dh sh + dn sn + dd with |db| < B, |dh| < H, |dn| < N, |dd| < D.  The
+// dimensions nest (set_layout), so at each level only the quotients next to delta / stride can work.
+bool rows_meet(long long delta, const long long *st, const long long *ext, int n, long long D) {
+    if (n == 0) return delta > -D && delta < D;
+    const long long s = st[0];
+    long long q = delta / s;
+    for (long long c = q - 2; c <= q + 2; ++c)
+        if (c > -ext[0] && c < ext[0] && rows_meet(delta - c * s, st + 1, ext + 1, n - 1, D)) return true;
+    return false;
+}
+
+bool operands_meet(const Plan &p, const void *a, const la::Layout &la_, const void *b, const la::Layout &lb,
+                   int elem) {
+    const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
+    if (!overlap(range_of(a, (size_t)span_of(p, la_) * elem), range_of(b, (size_t)span_of(p, lb) * elem)))
+        return false;
+    if (la_.sb != lb.sb || la_.sh != lb.sh || la_.sn != lb.sn) return true;  // interleaved other layouts: refuse
+    const long long diff = (long long)(pb - pa);
+    if (diff % elem != 0) return true;
+    long long st[3], ext[3];
+    int n = 0;
+    const long long s3[3] = {la_.sb, la_.sh, la_.sn}, e3[3] = {p.B, p.H, p.N};
+    int idx[3] = {0, 1, 2};  // by decreasing stride
+    for (int x = 0; x < 3; ++x)
+        for (int y = x + 1; y < 3; ++y)
+            if (s3[idx[y]] > s3[idx[x]]) { const int t = idx[x]; idx[x] = idx[y]; idx[y] = t; }
+    for (int k = 0; k < 3; ++k)
+        if (e3[idx[k]] > 1) {
+            st[n] = s3[idx[k]];
+            ext[n] = e3[idx[k]];
+            ++n;
+        }
+    return rows_meet(diff / elem, st, ext, n, p.D);
 }
 
 }  // namespace
@@ -137,8 +198,9 @@ size_t la_workspace_bytes(int B, int H, int N, int D, int causal, int dtype, int
     return backward ? p.bytes_bwd : p.bytes_fwd;
 }
 
-int la_forward(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B, int H,
-               int N, int D, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+int la_forward_strided(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B,
+                       int H, int N, int D, int dtype, const long long *strides, void *workspace,
+                       size_t workspace_bytes, void *stream) {
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || D < 1) return LA_ERR_INVALID_ARG;
     if (!la::supported_d(D)) return LA_ERR_UNSUPPORTED;
@@ -147,12 +209,25 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
     if (!Q || !K || !V || !O) return LA_ERR_INVALID_ARG;
     if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16)) return LA_ERR_INVALID_ARG;
     if (normaliser && !aligned(normaliser, 16)) return LA_ERR_INVALID_ARG;
-    int rc = check_workspace(p, workspace, workspace_bytes, false);
-    if (rc) return rc;
-    const size_t tb = (size_t)p.BH * N * D * (dtype == LA_BF16 ? 2 : 4);
-    const Range ins[] = {range_of(Q, tb), range_of(K, tb), range_of(V, tb), range_of(workspace, p.bytes_fwd)};
-    Range outs[2] = {range_of(O, tb), range_of(normaliser, normaliser ? (size_t)p.BH * N * 4 : 0)};
-    if ((rc = check_aliasing(outs, normaliser ? 2 : 1, ins, 4))) return rc;
+    const int elem = dtype == LA_BF16 ? 2 : 4;
+    const int ops[4] = {la::kOpQ, la::kOpK, la::kOpV, la::kOpO};
+    int rc;
+    if (strides)
+        for (int k = 0; k < 4; ++k)
+            if ((rc = set_layout(p, ops[k], strides + 3 * k, elem))) return rc;
+    if ((rc = check_workspace(p, workspace, workspace_bytes, false))) return rc;
+    // O must meet neither an input, the workspace nor the normaliser; the normaliser neither of those
+    const void *ins[3] = {Q, K, V};
+    for (int k = 0; k < 3; ++k)
+        if (operands_meet(p, O, p.lay[la::kOpO], ins[k], p.lay[ops[k]], elem)) return LA_ERR_INVALID_ARG;
+    const Range ws_r = range_of(workspace, p.bytes_fwd), o_r = range_of(O, (size_t)span_of(p, p.lay[la::kOpO]) * elem);
+    if (overlap(o_r, ws_r)) return LA_ERR_INVALID_ARG;
+    if (normaliser) {
+        const Range g_r = range_of(normaliser, (size_t)p.BH * N * 4);
+        if (overlap(g_r, ws_r) || overlap(g_r, o_r)) return LA_ERR_INVALID_ARG;
+        for (int k = 0; k < 3; ++k)
+            if (overlap(g_r, range_of(ins[k], (size_t)span_of(p, p.lay[ops[k]]) * elem))) return LA_ERR_INVALID_ARG;
+    }
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s)
                              : clear_state_tag(workspace, s);
@@ -160,9 +235,16 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
+int la_forward(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B, int H,
+               int N, int D, int dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    return la_forward_strided(Q, K, V, causal, O, normaliser, B, H, N, D, dtype, nullptr, workspace, workspace_bytes,
+                              stream);
+}
+
 static int backward_impl(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ,
-                         void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
-                         size_t workspace_bytes, void *stream, bool reuse_fwd_state) {
+                         void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,
+                         const long long *strides, void *workspace, size_t workspace_bytes, void *stream,
+                         bool reuse_fwd_state) {
     if (dtype != LA_F32 && dtype != LA_BF16) return LA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || D < 1) return LA_ERR_INVALID_ARG;
     if (!la::supported_d(D)) return LA_ERR_UNSUPPORTED;
@@ -171,13 +253,19 @@ static int backward_impl(const void *Q, const void *K, const void *V, const void
     const void *ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
     for (const void *q : ptrs)
         if (!q || !aligned(q, 16)) return LA_ERR_INVALID_ARG;
-    int rc = check_workspace(p, workspace, workspace_bytes, true);
-    if (rc) return rc;
-    const size_t tb = (size_t)p.BH * N * D * (dtype == LA_BF16 ? 2 : 4);
-    const Range ins[] = {range_of(Q, tb), range_of(K, tb), range_of(V, tb), range_of(O, tb), range_of(dO, tb),
-                         range_of(workspace, p.bytes_bwd)};
-    const Range outs[] = {range_of(dQ, tb), range_of(dK, tb), range_of(dV, tb)};
-    if ((rc = check_aliasing(outs, 3, ins, 6))) return rc;
+    const int elem = dtype == LA_BF16 ? 2 : 4;
+    int rc;
+    if (strides)
+        for (int k = 0; k < la::kNumOps; ++k)  // strides follow the argument order, which is the operand order
+            if ((rc = set_layout(p, k, strides + 3 * k, elem))) return rc;
+    if ((rc = check_workspace(p, workspace, workspace_bytes, true))) return rc;
+    // each output meets no input, no other output and not the workspace
+    const Range ws_r = range_of(workspace, p.bytes_bwd);
+    for (int o = la::kOpdQ; o <= la::kOpdV; ++o) {
+        if (overlap(range_of(ptrs[o], (size_t)span_of(p, p.lay[o]) * elem), ws_r)) return LA_ERR_INVALID_ARG;
+        for (int k = 0; k < la::kNumOps; ++k)
+            if (k != o && operands_meet(p, ptrs[o], p.lay[o], ptrs[k], p.lay[k], elem)) return LA_ERR_INVALID_ARG;
+    }
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = p.use_tc
                         ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, (unsigned char *)workspace, s, reuse_fwd_state)
@@ -190,15 +278,22 @@ static int backward_impl(const void *Q, const void *K, const void *V, const void
 int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
                 void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
                 size_t workspace_bytes, void *stream) {
-    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, workspace, workspace_bytes, stream,
-                         false);
+    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, nullptr, workspace, workspace_bytes,
+                         stream, false);
 }
 
 int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                                    void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,
                                    void *workspace, size_t workspace_bytes, void *stream) {
-    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, workspace, workspace_bytes, stream,
-                         true);
+    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, nullptr, workspace, workspace_bytes,
+                         stream, true);
+}
+
+int la_backward_strided(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ,
+                        void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype, const long long *strides,
+                        int reuse_forward_state, void *workspace, size_t workspace_bytes, void *stream) {
+    return backward_impl(Q, K, V, O, dO, dQ, dK, dV, causal, B, H, N, D, dtype, strides, workspace, workspace_bytes,
+                         stream, reuse_forward_state != 0);
 }
 
 int la_get_status(void *workspace, void *stream) {

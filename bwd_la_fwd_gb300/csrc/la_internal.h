@@ -22,6 +22,12 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
 static_assert(offsetof(WsHeader, state_tag) == 128, "the state tag sits 128 bytes into the header");
 
+// Element strides of one [B,H,N,D] operand: batch, head and row; the D elements of a row are contiguous.
+struct Layout {
+    long long sb, sh, sn;
+};
+enum Operand : int { kOpQ = 0, kOpK, kOpV, kOpO, kOpdO, kOpdQ, kOpdK, kOpdV, kNumOps };
+
 // How one call splits each head's N rows into segments whose D x D states are carried in the
 // workspace.  Chosen on the host from (N, D) only, so la_workspace_bytes and the launch agree.
 struct Plan {
@@ -40,6 +46,7 @@ struct Plan {
     size_t bytes_fwd;   // workspace bytes for the forward / for the backward
     size_t bytes_bwd;
     bool use_tc;        // tcgen05 kernels (bf16) rather than the SIMT kernels
+    Layout lay[kNumOps]; // strides of each operand (make_plan: contiguous [B,H,N,D])
 };
 
 // Host-side count of kernels launched by the library (la_launch_count).

@@ -59,11 +59,18 @@ struct Args {
     void *rs_delta;
     void *rs_dpart;     // per-column-block partial sums of dO_i . O_i, [NBLK][BH * N]
     void *states;       // workspace segment states, [BH][nseg][stride] of the accumulator type
+    Layout lq, lk, lv, lo, ldo, lout;  // operand strides (lout: the tensor `out` points to)
+    long long H;
     long long N;
     long long BHN;
     long long stride;
     int nseg, seg_len, causal;
 };
+
+// Element offset of flat head bh = b H + h of an operand with layout l.
+__device__ __forceinline__ long long head_off(const Layout &l, long long bh, long long H) {
+    return (bh / H) * l.sb + (bh % H) * l.sh;
+}
 
 // ------------------------------------------------------------------------------------------------
 // Segment aggregate: for segment s of head bh, X = sum over its rows of u w^T plus two vector sums.
@@ -86,8 +93,9 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
     const int s = blockIdx.x % a.nseg;
     const long long r0 = (long long)s * a.seg_len;
     const long long r1 = min((long long)a.N, r0 + a.seg_len);
-    const T *U = (const T *)(AM == kAggFwd ? a.K : a.Q) + bh * a.N * D;
-    const T *W = (const T *)(AM == kAggFwd ? a.V : a.dO) + bh * a.N * D;
+    const Layout &lu = AM == kAggFwd ? a.lk : a.lq, &lw = AM == kAggFwd ? a.lv : a.ldo;
+    const T *U = (const T *)(AM == kAggFwd ? a.K : a.Q) + head_off(lu, bh, a.H);
+    const T *W = (const T *)(AM == kAggFwd ? a.V : a.dO) + head_off(lw, bh, a.H);
     const Acc *rs_g = (const Acc *)a.rs_g, *rs_delta = (const Acc *)a.rs_delta;
 
     Acc X[C::RPT];
@@ -107,8 +115,8 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
             const int r = idx / D, d = idx % D;
             Acc u = Acc(0), w = Acc(0);
             if (r < nb) {
-                u = (Acc)load_f(U + (b0 + r) * D + d);
-                w = (Acc)load_f(W + (b0 + r) * D + d);
+                u = (Acc)load_f(U + (b0 + r) * lu.sn + d);
+                w = (Acc)load_f(W + (b0 + r) * lw.sn + d);
                 if (AM == kAggRev) w *= sSc[r];
             }
             sU[idx] = u;
@@ -216,9 +224,9 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
     const int s = blockIdx.x % a.nseg;
     const long long r0 = (long long)s * a.seg_len;
     const long long r1 = min(N, r0 + a.seg_len);
-    const long long hoff = bh * N * D;
-    const T *Qh = (const T *)a.Q + hoff, *Kh = (const T *)a.K + hoff, *Vh = (const T *)a.V + hoff;
-    const T *Oh = (const T *)a.O + hoff, *dOh = (const T *)a.dO + hoff;
+    const T *Qh = (const T *)a.Q + head_off(a.lq, bh, a.H), *Kh = (const T *)a.K + head_off(a.lk, bh, a.H);
+    const T *Vh = (const T *)a.V + head_off(a.lv, bh, a.H), *dOh = (const T *)a.dO + head_off(a.ldo, bh, a.H);
+    const long long hout = head_off(a.lout, bh, a.H);
     const Acc *st = (const Acc *)a.states + (bh * a.nseg + s) * a.stride;
     Acc *rs_g = (Acc *)a.rs_g, *rs_delta = (Acc *)a.rs_delta, *rs_dpart = (Acc *)a.rs_dpart;
     constexpr bool FWD = (MODE == kFwdO || MODE == kFwdDelta);
@@ -251,25 +259,25 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
         for (int idx = t; idx < RB * D; idx += kThreads) {
             const int r = idx / D, d = idx % D;
             const bool ok = r < nb;
-            const long long o = (b0 + r) * D + d;
+            const long long rr = b0 + r;
             if (FWD) {
-                sA[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
-                sB[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
-                sT[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
-                if (MODE == kFwdDelta) sX[idx] = ok ? (Acc)load_f(dOh + o) : Acc(0);
+                sA[idx] = ok ? (Acc)load_f(Kh + rr * a.lk.sn + d) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Vh + rr * a.lv.sn + d) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Qh + rr * a.lq.sn + d) : Acc(0);
+                if (MODE == kFwdDelta) sX[idx] = ok ? (Acc)load_f(dOh + rr * a.ldo.sn + d) : Acc(0);
             } else if (MODE == kBwdDQ) {
-                sA[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
-                sB[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
-                sT[idx] = ok ? (Acc)load_f(dOh + o) : Acc(0);
-                sY[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
+                sA[idx] = ok ? (Acc)load_f(Vh + rr * a.lv.sn + d) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Kh + rr * a.lk.sn + d) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(dOh + rr * a.ldo.sn + d) : Acc(0);
+                sY[idx] = ok ? (Acc)load_f(Qh + rr * a.lq.sn + d) : Acc(0);
             } else if (MODE == kBwdDK) {
-                sA[idx] = ok ? (Acc)load_f(dOh + o) / sG[r] : Acc(0);
-                sB[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
-                sT[idx] = ok ? (Acc)load_f(Vh + o) : Acc(0);
+                sA[idx] = ok ? (Acc)load_f(dOh + rr * a.ldo.sn + d) / sG[r] : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(Qh + rr * a.lq.sn + d) : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Vh + rr * a.lv.sn + d) : Acc(0);
             } else {
-                sA[idx] = ok ? (Acc)load_f(Qh + o) : Acc(0);
-                sB[idx] = ok ? (Acc)load_f(dOh + o) / sG[r] : Acc(0);
-                sT[idx] = ok ? (Acc)load_f(Kh + o) : Acc(0);
+                sA[idx] = ok ? (Acc)load_f(Qh + rr * a.lq.sn + d) : Acc(0);
+                sB[idx] = ok ? (Acc)load_f(dOh + rr * a.ldo.sn + d) / sG[r] : Acc(0);
+                sT[idx] = ok ? (Acc)load_f(Kh + rr * a.lk.sn + d) : Acc(0);
             }
         }
         __syncthreads();
@@ -356,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
             if (MODE == kFwdDelta) {
                 sRun[r * C::EB + col] = v * sX[r * D + colg];  // sRun (z rows) is dead in phase 4
             } else {
-                store_f((T *)a.out + hoff + (b0 + r) * D + colg, v);
+                store_f((T *)a.out + hout + (b0 + r) * a.lout.sn + colg, v);
             }
         }
         if (MODE == kFwdDelta) {
@@ -399,6 +407,13 @@ Args make_args(const Plan &p, const void *Q, const void *K, const void *V, const
     a.rs_delta = ws + p.off_rowstats + (size_t)p.BH * p.N * p.acc_bytes;
     a.rs_dpart = ws + p.off_rowstats + 2 * (size_t)p.BH * p.N * p.acc_bytes;
     a.BHN = (long long)p.BH * p.N;
+    a.lq = p.lay[kOpQ];
+    a.lk = p.lay[kOpK];
+    a.lv = p.lay[kOpV];
+    a.lo = p.lay[kOpO];
+    a.ldo = p.lay[kOpdO];
+    a.lout = p.lay[kOpO];
+    a.H = p.H;
     a.N = p.N;
     a.stride = p.stride;
     a.nseg = p.nseg;
@@ -444,12 +459,15 @@ cudaError_t backward_impl(const Plan &p, Args a, void *dQ, void *dK, void *dV, c
     simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 0);
     simt_rows<T, Acc, D, kFwdDelta><<<grid, kThreads, sr, s>>>(a);
     a.out = dQ;
+    a.lout = p.lay[kOpdQ];
     simt_rows<T, Acc, D, kBwdDQ><<<grid, kThreads, sr, s>>>(a);
     simt_aggregate<T, Acc, D, kAggRev><<<grid, kThreads, sa, s>>>(a);
     simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 1);
     a.out = dK;
+    a.lout = p.lay[kOpdK];
     simt_rows<T, Acc, D, kBwdDK><<<grid, kThreads, sr, s>>>(a);
     a.out = dV;
+    a.lout = p.lay[kOpdV];
     simt_rows<T, Acc, D, kBwdDV><<<grid, kThreads, sr, s>>>(a);
     e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(8);

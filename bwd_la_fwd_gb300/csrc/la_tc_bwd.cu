@@ -251,9 +251,10 @@ __device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h,
 }
 
 // Issues the TMA stores of a two-box output tile from shared memory and commits them.  One thread.
-__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, int h) {
-    tma_store_3d(map, tile2, 0, row0, h);
-    tma_store_3d(map, tile2 + kBox, 64, row0, h);
+template <bool FLAT>
+__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, HeadCoord hc) {
+    tile_store<FLAT>(map, tile2, 0, row0, hc);
+    tile_store<FLAT>(map, tile2 + kBox, 64, row0, hc);
     bulk_commit();
 }
 
@@ -271,6 +272,7 @@ __device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigne
 // prefetched into L2 meanwhile, and dQ leaves through its own staging tile.
 // Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128.
 // ----------------------------------------------------------------------------------------------------
+template <bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr uint32_t TB = NB * kBox;
@@ -353,6 +355,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x301)) {
@@ -361,19 +364,20 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 }
                 mbar_arrive_expect_tx(full, STAGE);
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, hc);
                 }
                 const long long nx = pc.h * P.sl.nchunk + c + 1;  // the slice's next chunk, into L2
                 if (nx < hi) {
                     const int nh = (int)(nx / P.sl.nchunk), nrow = (int)(nx % P.sl.nchunk) * kC;
+                    const HeadCoord hn = head_coord<FLAT>(nh, P.H);
                     for (int nb = 0; nb < NB; ++nb) {
-                        tma_prefetch_3d(&P.tmQ, nb * 64, nrow, nh);
-                        tma_prefetch_3d(&P.tmdO, nb * 64, nrow, nh);
-                        tma_prefetch_3d(&P.tmK, nb * 64, nrow, nh);
-                        tma_prefetch_3d(&P.tmV, nb * 64, nrow, nh);
+                        tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
+                        tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
+                        tile_prefetch<FLAT>(&P.tmK, nb * 64, nrow, hn);
+                        tile_prefetch<FLAT>(&P.tmV, nb * 64, nrow, hn);
                     }
                 }
             }
@@ -541,7 +545,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
                 fence_proxy_async_smem();
                 epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
-                if (u == 0) store_tile(&P.tmdQ, dqt, (int)row0, (int)pc.h);
+                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, (int)row0, head_coord<FLAT>(pc.h, P.H));
                 if (c + 1 < pc.e) {
                     tmem_half_to_tile(R2 + lo, Sb, i, hf);
                     fence_proxy_async_smem();
@@ -592,6 +596,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
 // into R2) are issued one chunk behind, once the epilogue has rewritten dO as dO / g in place; dQ leaves
 // through its own staging tile.
 // ----------------------------------------------------------------------------------------------------
+template <bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64, NST = 2;
     constexpr uint32_t TB = NB * kBox;
@@ -678,6 +683,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
@@ -688,8 +694,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, hc);
+                    tile_load<FLAT>(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, hc);
                 }
             }
         }
@@ -793,7 +799,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 }
                 mbar_arrive(barDt);
                 epi_sync256();  // dQ of every row is staged
-                if (u == 0) store_tile(&P.tmdQ, dqt, c * kC, (int)pc.h);
+                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, c * kC, head_coord<FLAT>(pc.h, P.H));
             }
             if (!ok) break;
             ok = wait_or_abort(barPP, pno & 1, abort_flag, P.status, 0x32A);
@@ -831,6 +837,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
 // as soon as dK, the last MMA reading it, is done.  One TMA stage (Q, dO, K, V); the next chunk's tiles
 // are prefetched into L2 meanwhile.
 // ----------------------------------------------------------------------------------------------------
+template <bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr uint32_t TB = NB * kBox;
@@ -904,6 +911,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x401)) {
@@ -912,19 +920,20 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 }
                 mbar_arrive_expect_tx(full, STAGE);
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(stage + nb * kBox, &P.tmQ, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + TB + nb * kBox, &P.tmdO, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + 2 * TB + nb * kBox, &P.tmK, full, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(stage + 3 * TB + nb * kBox, &P.tmV, full, nb * 64, c * kC, hc);
                 }
                 long long nh;
                 int nc;
                 if (next_rev_chunk(pi, pc, c, &nh, &nc)) {  // the next chunk to be walked, into L2
+                    const HeadCoord hn = head_coord<FLAT>(nh, P.H);
                     for (int nb = 0; nb < NB; ++nb) {
-                        tma_prefetch_3d(&P.tmQ, nb * 64, nc * kC, (int)nh);
-                        tma_prefetch_3d(&P.tmdO, nb * 64, nc * kC, (int)nh);
-                        tma_prefetch_3d(&P.tmK, nb * 64, nc * kC, (int)nh);
-                        tma_prefetch_3d(&P.tmV, nb * 64, nc * kC, (int)nh);
+                        tile_prefetch<FLAT>(&P.tmQ, nb * 64, nc * kC, hn);
+                        tile_prefetch<FLAT>(&P.tmdO, nb * 64, nc * kC, hn);
+                        tile_prefetch<FLAT>(&P.tmK, nb * 64, nc * kC, hn);
+                        tile_prefetch<FLAT>(&P.tmV, nb * 64, nc * kC, hn);
                     }
                 }
             }
@@ -1068,7 +1077,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 tmem_half_to_out(R2 + lo, hf, ec, 1.f, dvt, j);
                 fence_proxy_async_smem();
                 epi_sync256();
-                if (u == 0) store_tile(&P.tmdV, dvt, (int)row0, (int)pc.h);
+                if (u == 0) store_tile<FLAT>(&P.tmdV, dvt, (int)row0, head_coord<FLAT>(pc.h, P.H));
                 // dK_j = [R1]_j - y
                 ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
                 if (!ok) break;
@@ -1076,7 +1085,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 tmem_half_to_out(R1 + lo, hf, yc, -1.f, dkt, j);
                 fence_proxy_async_smem();
                 epi_sync256();  // dK rows staged; every read of yc and ec for this chunk is done
-                if (u == 0) store_tile(&P.tmdK, dkt, (int)row0, (int)pc.h);
+                if (u == 0) store_tile<FLAT>(&P.tmdK, dkt, (int)row0, head_coord<FLAT>(pc.h, P.H));
                 // P (with this chunk's rows, for the earlier chunks) -> Pb: its update finished before dV
                 if (c > pc.a) {
                     tmem_half_to_tile(R3 + lo, Pb, j, hf);
@@ -1103,6 +1112,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
 // (the sum of all its pieces' slots), so only K and V are read.  Three TMA stages of (K, V); R2 accumulates dK,
 // then dV; dK leaves through the V tile and dV through the K tile.
 // ----------------------------------------------------------------------------------------------------
+template <bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64, NST = 3;
     constexpr uint32_t TB = NB * kBox;
@@ -1172,6 +1182,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
                 prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
@@ -1182,8 +1193,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(st + TB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(st + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, hc);
+                    tile_load<FLAT>(st + TB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, hc);
                 }
             }
         }
@@ -1256,7 +1267,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
                 tc_fence_before();
                 mbar_arrive(barKf);
                 epi_sync256();
-                if (u == 0) store_tile(&P.tmdK, st + TB, row0, (int)pc.h);
+                if (u == 0) store_tile<FLAT>(&P.tmdK, st + TB, row0, head_coord<FLAT>(pc.h, P.H));
                 // dV_j = [R2]_j + e, staged in the K tile (its last reader, dV = K Pb, is done)
                 ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x427);
                 if (!ok) break;
@@ -1267,7 +1278,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
                 mbar_arrive(barVf);
                 epi_sync256();
                 if (u == 0) {
-                    store_tile(&P.tmdV, st, row0, (int)pc.h);
+                    store_tile<FLAT>(&P.tmdV, st, row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_wait_read0();
                     mbar_arrive(&empty[s]);
                 }
@@ -1301,10 +1312,16 @@ bool set_bwd_attrs() {
     static int done = 0;
     if (done) return done > 0;
     const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    bool ok = cudaFuncSetAttribute(tc::tc_bwd_dq_kernel, A, (int)kSmemDq) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dq_nc_kernel, A, (int)kSmemDqNc) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_kernel, A, (int)kSmemDkdv) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_bwd_dkdv_nc_kernel, A, (int)kSmemDkdvNc) == cudaSuccess;
+    bool ok = true;
+    for (int f = 0; f < 2 && ok; ++f)
+        ok = cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, A, (int)kSmemDq) ==
+                 cudaSuccess &&
+             cudaFuncSetAttribute(f ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>, A,
+                                  (int)kSmemDqNc) == cudaSuccess &&
+             cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_kernel<true> : tc::tc_bwd_dkdv_kernel<false>, A,
+                                  (int)kSmemDkdv) == cudaSuccess &&
+             cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_nc_kernel<true> : tc::tc_bwd_dkdv_nc_kernel<false>, A,
+                                  (int)kSmemDkdvNc) == cudaSuccess;
     done = ok ? 1 : -1;
     return ok;
 }
@@ -1317,10 +1334,14 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
     if (!tc_host::fill_common(P, p, ws)) return cudaErrorInvalidDevice;
-    if (!tc_host::make_map(&P.tmQ, Q, p) || !tc_host::make_map(&P.tmK, K, p) || !tc_host::make_map(&P.tmV, V, p) ||
-        !tc_host::make_map(&P.tmdO, dO, p) || !tc_host::make_map(&P.tmdQ, dQ, p) ||
-        !tc_host::make_map(&P.tmdK, dK, p) || !tc_host::make_map(&P.tmdV, dV, p))
+    const int ops[7] = {kOpQ, kOpK, kOpV, kOpdO, kOpdQ, kOpdK, kOpdV};
+    const bool flat = tc_host::flat_heads(p, ops, 7);
+    if (!tc_host::make_map(&P.tmQ, Q, p, kOpQ, flat) || !tc_host::make_map(&P.tmK, K, p, kOpK, flat) ||
+        !tc_host::make_map(&P.tmV, V, p, kOpV, flat) || !tc_host::make_map(&P.tmdO, dO, p, kOpdO, flat) ||
+        !tc_host::make_map(&P.tmdQ, dQ, p, kOpdQ, flat) || !tc_host::make_map(&P.tmdK, dK, p, kOpdK, flat) ||
+        !tc_host::make_map(&P.tmdV, dV, p, kOpdV, flat))
         return cudaErrorInvalidValue;
+    P.flat = flat ? 1 : 0;
     P.slots_rev = (float *)(ws + p.off_states2);
     P.rs_g = (float *)(ws + p.off_rowstats);
     P.rs_dt = P.rs_g + (size_t)p.BH * p.N;
@@ -1345,8 +1366,10 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         }
     }
     if (e == cudaSuccess) {
-        e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dq_kernel, P.sl.G, nthr, kSmemDq, s, P)
-                     : tc_host::launch_tc(tc::tc_bwd_dq_nc_kernel, P.sl.G, nthr, kSmemDqNc, s, P);
+        e = p.causal ? tc_host::launch_tc(flat ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, P.sl.G,
+                                          nthr, kSmemDq, s, P)
+                     : tc_host::launch_tc(flat ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>,
+                                          P.sl.G, nthr, kSmemDqNc, s, P);
         ++launches;
     }
     if (e == cudaSuccess) {
@@ -1354,8 +1377,10 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         ++launches;
     }
     if (e == cudaSuccess) {
-        e = p.causal ? tc_host::launch_tc(tc::tc_bwd_dkdv_kernel, P.sl.G, nthr, kSmemDkdv, s, P)
-                     : tc_host::launch_tc(tc::tc_bwd_dkdv_nc_kernel, P.sl.G, nthr, kSmemDkdvNc, s, P);
+        e = p.causal ? tc_host::launch_tc(flat ? tc::tc_bwd_dkdv_kernel<true> : tc::tc_bwd_dkdv_kernel<false>,
+                                          P.sl.G, nthr, kSmemDkdv, s, P)
+                     : tc_host::launch_tc(flat ? tc::tc_bwd_dkdv_nc_kernel<true> : tc::tc_bwd_dkdv_nc_kernel<false>,
+                                          P.sl.G, nthr, kSmemDkdvNc, s, P);
         ++launches;
     }
     if (e == cudaSuccess) count_launches(launches);

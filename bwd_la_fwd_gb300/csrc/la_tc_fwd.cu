@@ -34,6 +34,7 @@ using namespace sm100;
 // MMAs, and two per-chunk z_c, a_c blocks (16 + 16 columns) from MMAs against a tile of ones (N = 16);
 // the epilogue drains z_c, a_c every chunk and adds them up for the piece in fp32 registers.
 // ----------------------------------------------------------------------------------------------------
+template <bool FLAT>
 __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64, NST = 3;
     constexpr uint32_t STAGE = 2 * NB * kBox;  // K and V boxes
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
         int it = 0;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && !*abort_flag; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x101))
@@ -97,8 +99,8 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
-                    tma_load_3d(st + (NB + nb) * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(st + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, hc);
+                    tile_load<FLAT>(st + (NB + nb) * kBox, &P.tmV, &full[s], nb * 64, c * kC, hc);
                 }
             }
         }
@@ -213,7 +215,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
 // TMEM: causal  T 0-127, O 128-255, S 256-383, exchange 416-419;
 //       non-causal  O 0-127 / 128-255, exchange 256-259.
 // ----------------------------------------------------------------------------------------------------
-template <bool CAUSAL>
+template <bool CAUSAL, bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr int NST = CAUSAL ? 2 : 4;
@@ -284,6 +286,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
+            const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
                 prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
                 const int s = it % NST;
@@ -294,10 +297,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
-                    tma_load_3d(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, (int)pc.h);
+                    tile_load<FLAT>(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, hc);
                     if (CAUSAL) {
-                        tma_load_3d(st + QB + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, (int)pc.h);
-                        tma_load_3d(st + 2 * QB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, (int)pc.h);
+                        tile_load<FLAT>(st + QB + nb * kBox, &P.tmK, &full[s], nb * 64, c * kC, hc);
+                        tile_load<FLAT>(st + 2 * QB + nb * kBox, &P.tmV, &full[s], nb * 64, c * kC, hc);
                     }
                 }
             }
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 tc_fence_before();
                 epi_sync256();  // the whole O tile is in shared memory
                 if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < NB; ++nb) tma_store_3d(&P.tmO, st + nb * kBox, nb * 64, (int)row0, (int)pc.h);
+                    for (int nb = 0; nb < NB; ++nb) tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_commit();
                     bulk_wait_read0();       // the tile has been read out of shared memory
                     mbar_arrive(&empty[s]);  // the stage may be refilled
@@ -504,8 +507,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     }
 }
 
-template __global__ void tc_fwd_kernel<true>(const __grid_constant__ TcParams P);
-template __global__ void tc_fwd_kernel<false>(const __grid_constant__ TcParams P);
+template __global__ void tc_fwd_kernel<true, true>(const __grid_constant__ TcParams P);
+template __global__ void tc_fwd_kernel<false, true>(const __grid_constant__ TcParams P);
+template __global__ void tc_fwd_kernel<true, false>(const __grid_constant__ TcParams P);
+template __global__ void tc_fwd_kernel<false, false>(const __grid_constant__ TcParams P);
 
 // ----------------------------------------------------------------------------------------------------
 // Carries: in place over the piece slots of each head, in piece order, so that a walk then reads exactly
@@ -583,17 +588,29 @@ int sm_count() {
     return cached[dev];
 }
 
-// [BH][N][D] bf16 tensor, boxes of 128 rows x 64 columns, 128-byte swizzle; rows past N read as zero.
-bool make_map(CUtensorMap *m, const void *ptr, const Plan &p) {
+// Operand `op` as a bf16 map with boxes of 128 rows x 64 columns of one head, 128-byte swizzle; rows
+// past N read as zero and are not written.  flat: 3-D over {D, N, B H} (the operand's batch stride is H
+// times its head stride); else 4-D over {D, N, H, B}.
+bool make_map(CUtensorMap *m, const void *ptr, const Plan &p, int op, bool flat) {
     auto enc = encode_fn();
     if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)p.D, (cuuint64_t)p.N, (cuuint64_t)p.BH};
-    cuuint64_t strides[2] = {(cuuint64_t)p.D * 2, (cuuint64_t)p.N * p.D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)tc::kC, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+    const Layout &l = p.lay[op];
+    cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.N, (cuuint64_t)(flat ? p.BH : p.H), (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)l.sn * 2, (cuuint64_t)l.sh * 2, (cuuint64_t)l.sb * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)tc::kC, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, flat ? 3 : 4, const_cast<void *>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Whether every listed operand's heads can be numbered flat (batch stride = H x head stride, or B = 1).
+bool flat_heads(const Plan &p, const int *ops, int n) {
+    for (int k = 0; k < n; ++k) {
+        const Layout &l = p.lay[ops[k]];
+        if (p.B > 1 && l.sb != (long long)p.H * l.sh) return false;
+    }
+    return true;
 }
 
 constexpr size_t kSmemAgg = 3 * 2 * 2 * (size_t)tc::kBox + 2048 + 256;
@@ -604,12 +621,13 @@ static_assert(kSmemFwdCausal <= 232448, "forward kernel exceeds the shared-memor
 bool set_smem_attrs() {
     static int done = 0;
     if (done) return done > 0;
-    bool ok = cudaFuncSetAttribute(tc::tc_agg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAgg) ==
-                  cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemFwdCausal) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemFwdNonCausal) == cudaSuccess;
+    const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    bool ok = cudaFuncSetAttribute(tc::tc_agg_kernel<true>, A, (int)kSmemAgg) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_agg_kernel<false>, A, (int)kSmemAgg) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_fwd_kernel<true, true>, A, (int)kSmemFwdCausal) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_fwd_kernel<false, true>, A, (int)kSmemFwdNonCausal) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_fwd_kernel<true, false>, A, (int)kSmemFwdCausal) == cudaSuccess &&
+              cudaFuncSetAttribute(tc::tc_fwd_kernel<false, false>, A, (int)kSmemFwdNonCausal) == cudaSuccess;
     done = ok ? 1 : -1;
     return ok;
 }
@@ -628,6 +646,11 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     }
     P.sl.G = (int)G;
     P.N = p.N;
+    P.H = p.H;
+    uint64_t hsh = 0xcbf29ce484222325ull;  // FNV-1a over K's and V's strides
+    for (int op : {kOpK, kOpV})
+        for (long long v : {p.lay[op].sb, p.lay[op].sh, p.lay[op].sn}) hsh = (hsh ^ (uint64_t)v) * 0x100000001b3ull;
+    P.kv_layout = hsh;
     P.slot_stride = p.stride;
     P.slots = (float *)(ws + p.off_states);
     P.chunk_za = (float *)(ws + p.off_chunkza);
@@ -662,7 +685,7 @@ cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cud
 
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
     if (!set_smem_attrs()) return cudaErrorInvalidValue;
-    return launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
+    return launch_tc(P.flat ? tc::tc_agg_kernel<true> : tc::tc_agg_kernel<false>, P.sl.G, 192, kSmemAgg, s, P);
 }
 
 }  // namespace tc_host
@@ -679,18 +702,24 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
     if (!fill_common(P, p, ws)) return cudaErrorInvalidDevice;
-    if (!make_map(&P.tmQ, Q, p) || !make_map(&P.tmK, K, p) || !make_map(&P.tmV, V, p) || !make_map(&P.tmO, O, p))
+    const int ops[4] = {kOpQ, kOpK, kOpV, kOpO};
+    const bool flat = flat_heads(p, ops, 4);
+    if (!make_map(&P.tmQ, Q, p, kOpQ, flat) || !make_map(&P.tmK, K, p, kOpK, flat) ||
+        !make_map(&P.tmV, V, p, kOpV, flat) || !make_map(&P.tmO, O, p, kOpO, flat))
         return cudaErrorInvalidValue;
+    P.flat = flat ? 1 : 0;
     P.O = O;
     P.g = g;
     P.Kp = K;
     P.Vp = V;
-    cudaError_t e = launch_tc(tc::tc_agg_kernel, P.sl.G, 192, kSmemAgg, s, P);
+    cudaError_t e = launch_agg(P, s);
     if (e == cudaSuccess)
         e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal, true, s);
     if (e == cudaSuccess)
-        e = p.causal ? launch_tc(tc::tc_fwd_kernel<true>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdCausal, s, P)
-                     : launch_tc(tc::tc_fwd_kernel<false>, P.sl.G, 64 + tc::kEpiThreads, kSmemFwdNonCausal, s, P);
+        e = p.causal ? launch_tc(flat ? tc::tc_fwd_kernel<true, true> : tc::tc_fwd_kernel<true, false>, P.sl.G,
+                                 64 + tc::kEpiThreads, kSmemFwdCausal, s, P)
+                     : launch_tc(flat ? tc::tc_fwd_kernel<false, true> : tc::tc_fwd_kernel<false, false>, P.sl.G,
+                                 64 + tc::kEpiThreads, kSmemFwdNonCausal, s, P);
     if (e == cudaSuccess) count_launches(3);
     return e;
 }

@@ -13,9 +13,13 @@ namespace tc {
 
 // Kernel parameters (passed as a __grid_constant__ struct; the tensor maps stay in parameter space).
 struct TcParams {
-    CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D maps over [BH][N][D] bf16, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tmQ, tmK, tmV, tmdO;  // bf16 maps with the operand's strides (see `flat`); box 64 columns x
+                                      // 128 rows of one head, 128-byte swizzle
     CUtensorMap tmO, tmdQ, tmdK, tmdV;  // the outputs, same form (tiles are staged in shared memory)
     Slices sl;
+    int H;                  // heads per batch entry: flat head bh = b H + h
+    int flat;               // the maps are 3-D over {D, N, B H} (kernels <FLAT = true>), else 4-D over {D, N, H, B}
+    uint64_t kv_layout;     // hash of K's and V's strides (part of the per-piece sums' identity)
     long long N;
     float *slots;           // per-piece state sums, slot stride `slot_stride` floats
     float *slots_rev;       // backward: per-piece reverse-direction sums
@@ -45,7 +49,7 @@ constexpr size_t kTagOffset = 128;  // bytes into the workspace header
 static_assert(kTagOffset == offsetof(WsHeader, state_tag), "tag offset");
 constexpr int kTagWords = 7;
 __host__ __device__ inline void state_tag(const TcParams &P, uint64_t form, uint64_t *t) {
-    t[0] = 0x4C415F5354415445ull;  // marker ("LA_STATE")
+    t[0] = 0x4C415F5354415445ull ^ P.kv_layout;  // marker ("LA_STATE"), folded with K's and V's strides
     t[1] = (uint64_t)(uintptr_t)P.Kp;
     t[2] = (uint64_t)(uintptr_t)P.Vp;
     t[3] = (uint64_t)P.sl.T;
@@ -74,7 +78,8 @@ __device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
 
 // Host helpers shared by the forward and backward launchers (la_tc_fwd.cu).
 namespace tc_host {
-bool make_map(CUtensorMap *m, const void *ptr, const Plan &p);
+bool make_map(CUtensorMap *m, const void *ptr, const Plan &p, int op, bool flat);
+bool flat_heads(const Plan &p, const int *ops, int n);
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
 cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T V sums into P.slots
 // Launches a tensor-core kernel as a programmatic dependent of the previous kernel in the stream (the

@@ -18,6 +18,35 @@ __device__ __forceinline__ unsigned char *smem_base(unsigned char *raw, uint32_t
     return raw;
 }
 
+// Tile (columns [x, x + 64), rows [row, row + 128)) of one head of an operand.  The kernels come in two
+// forms.  FLAT: every operand's batch stride is H times its head stride (contiguous [B,H,N,D] among
+// others), the maps are 3-D over {D, N, B H} and a head is its flat index bh = b H + h.  Otherwise the
+// maps are 4-D over {D, N, H, B} with the caller's strides ([B,N,H,D], a head slice of a fused QKV
+// tensor...).  head_coord turns bh into the coordinates of the form, once per piece.
+struct HeadCoord {
+    int h, b;
+};
+template <bool FLAT> __device__ __forceinline__ HeadCoord head_coord(long long bh, int H) {
+    if (FLAT) return HeadCoord{(int)bh, 0};
+    const unsigned u = (unsigned)bh;  // B H < 2^31
+    return HeadCoord{(int)(u % (unsigned)H), (int)(u / (unsigned)H)};
+}
+template <bool FLAT>
+__device__ __forceinline__ void tile_load(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int row,
+                                          HeadCoord hc) {
+    if constexpr (FLAT) tma_load_3d(dst, m, bar, x, row, hc.h);
+    else tma_load_4d(dst, m, bar, x, row, hc.h, hc.b);
+}
+template <bool FLAT> __device__ __forceinline__ void tile_prefetch(const CUtensorMap *m, int x, int row, HeadCoord hc) {
+    if constexpr (FLAT) tma_prefetch_3d(m, x, row, hc.h);
+    else tma_prefetch_4d(m, x, row, hc.h, hc.b);
+}
+template <bool FLAT>
+__device__ __forceinline__ void tile_store(const CUtensorMap *m, const void *src, int x, int row, HeadCoord hc) {
+    if constexpr (FLAT) tma_store_3d(m, src, x, row, hc.h);
+    else tma_store_4d(m, src, x, row, hc.h, hc.b);
+}
+
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane quarter

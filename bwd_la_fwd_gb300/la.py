@@ -58,6 +58,11 @@ def load_library():
         lib.la_backward.restype = i
         lib.la_backward_with_forward_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
         lib.la_backward_with_forward_state.restype = i
+        lp = ctypes.POINTER(ctypes.c_longlong)
+        lib.la_forward_strided.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, lp, vp, sz, vp]
+        lib.la_forward_strided.restype = i
+        lib.la_backward_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, i, vp, sz, vp]
+        lib.la_backward_strided.restype = i
         lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
         lib.la_decode_step.restype = i
         lib.la_state_append.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
@@ -100,13 +105,19 @@ def _shape(Q):
 
 
 def _check_like(Q, *others):
-    for t in others:
+    for t in (Q, *others):
         if t is None:
             continue
         if t.shape != Q.shape or t.dtype != Q.dtype or t.device != Q.device:
             raise ValueError("all [B,H,N,D] tensors must share shape, dtype and device")
-        if not t.is_contiguous():
-            raise ValueError("tensors must be contiguous [B,H,N,D]")
+        if t.stride(-1) != 1:
+            raise ValueError("the D elements of each row must be contiguous (stride(-1) == 1)")
+
+
+def _strides(*ts):
+    """(batch, head, row) element strides of each [B,H,N,D] view, as the strided entry points take them."""
+    vals = [int(x) for t in ts for x in t.stride()[:3]]
+    return (ctypes.c_longlong * len(vals))(*vals)
 
 
 def la_launch_count() -> int:
@@ -128,7 +139,10 @@ def new_workspace(B: int, H: int, N: int, D: int, causal: bool, dtype: int, back
 
 
 def la_forward(Q, K, V, causal: bool, O=None, normaliser=None, workspace=None, stream=None):
-    """O, g = la_forward(Q, K, V, causal): normalised linear attention forward on [B,H,N,D] tensors."""
+    """O, g = la_forward(Q, K, V, causal): normalised linear attention forward on [B,H,N,D] tensors.
+
+    The tensors may be strided views (a [B,N,H,D] tensor permuted to [B,H,N,D], a slice of a fused QKV
+    projection) as long as each row's D elements are contiguous; they go to the library as they are."""
     import torch
     B, H, N, D = _shape(Q)
     _check_like(Q, K, V, O)
@@ -139,9 +153,9 @@ def la_forward(Q, K, V, causal: bool, O=None, normaliser=None, workspace=None, s
         normaliser = torch.empty((B, H, N), dtype=torch.float32, device=Q.device)
     if workspace is None:
         workspace = new_workspace(B, H, N, D, causal, dt, False, Q.device)
-    st = load_library().la_forward(_ptr(Q), _ptr(K), _ptr(V), int(bool(causal)), _ptr(O), _ptr(normaliser), B, H, N,
-                                   D, dt, _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                   _stream_ptr(stream))
+    st = load_library().la_forward_strided(_ptr(Q), _ptr(K), _ptr(V), int(bool(causal)), _ptr(O), _ptr(normaliser),
+                                           B, H, N, D, dt, _strides(Q, K, V, O), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != 0:
         raise LAError(st, "la_forward")
     return O, normaliser
@@ -165,10 +179,10 @@ def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspa
         if reuse_forward_state:
             raise ValueError("reuse_forward_state needs the workspace the forward ran with")
         workspace = new_workspace(B, H, N, D, causal, dt, True, Q.device)
-    lib = load_library()
-    fn = lib.la_backward_with_forward_state if reuse_forward_state else lib.la_backward
-    st = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), int(bool(causal)), B, H, N, D,
-            dt, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    st = load_library().la_backward_strided(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV),
+                                            int(bool(causal)), B, H, N, D, dt, _strides(Q, K, V, O, dO, dQ, dK, dV),
+                                            int(bool(reuse_forward_state)), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     if st != 0:
         raise LAError(st, "la_backward_with_forward_state" if reuse_forward_state else "la_backward")
     return dQ, dK, dV

@@ -16,7 +16,8 @@
  * never formed: the kernels carry D x D running states, as the O(N D^2) / O(N D) claims require.
  *
  * Layout.  Q, K, V, O, dO, dQ, dK, dV are dense, contiguous [B, H, N, D] tensors of one element
- * type (LA_F32 = float, LA_BF16 = bfloat16), element (b, h, i, d) at ((b H + h) N + i) D + d.  The
+ * type (LA_F32 = float, LA_BF16 = bfloat16), element (b, h, i, d) at ((b H + h) N + i) D + d (the
+ * *_strided entry points take other layouts).  The
  * normaliser is float [B, H, N].  All accumulation is in fp32.  Supported: B, H >= 1 (B*H < 2^31),
  * N >= 1 (B*H*N*D < 2^40), D in {16, 32, 64, 128, 256}.
  *
@@ -117,6 +118,30 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
 int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                                    void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,
                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Strided operands: the same passes on tensors laid out other than [B,H,N,D], with no transpose copy --
+ * [B,N,H,D] as a projection writes it, or the Q, K and V slices of one fused [B,N,3,H,D] projection
+ * output (the LA layer's projections precede the head, shd-paper.top page, abstract).
+ *   strides  in : host array, three element strides per operand, in the operands' argument order --
+ *                 (batch, head, row) for Q, K, V, O (forward: 12 values) or Q, K, V, O, dO, dQ, dK, dV
+ *                 (backward: 24 values); NULL means every operand is contiguous [B,H,N,D].
+ * The D elements of a row are contiguous.  Every stride must be a multiple of 16 bytes, and an operand's
+ * rows must not overlap one another: ordered by stride, the dimensions of extent > 1 must nest (the
+ * smallest stride >= D, each larger one >= the previous stride times its extent).  Inputs may share
+ * memory (a fused QKV tensor); an output may not meet an input, another output or the workspace, which
+ * is checked element-exactly for operands of equal strides and by address range otherwise.  The
+ * normaliser stays contiguous float [B,H,N].  Violations return LA_ERR_INVALID_ARG before any work.
+ * la_backward_strided with reuse_forward_state != 0 is la_backward_with_forward_state; the record of the
+ * forward's sums then also covers K's and V's strides.  Results are those of the contiguous calls on the
+ * same values.
+ */
+int la_forward_strided(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B,
+                       int H, int N, int D, int dtype, const long long *strides, void *workspace,
+                       size_t workspace_bytes, void *stream);
+int la_backward_strided(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ,
+                        void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype, const long long *strides,
+                        int reuse_forward_state, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Forward pass without a caller-supplied workspace, for callers that cannot allocate device memory (a

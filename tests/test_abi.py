@@ -130,3 +130,37 @@ def test_decode_entries_reject_bad_arguments_on_host(lib):
     assert append(K=0) == 1
     assert append(s=[0x1000_0000] + st[1:]) == 1               # S overlaps K
     assert append(K=0, V=0, N=0) == 0                          # nothing to append: nothing launched
+
+
+def test_strided_entries_reject_bad_layouts_on_host(lib):
+    vp = ctypes.c_void_p
+    B, H, N, D = 2, 4, 64, 64
+    base = [0x1000_0000 * (i + 1) for i in range(8)]
+
+    def fwd(strides, ptrs=base[:4]):
+        arr = (ctypes.c_longlong * 12)(*strides)
+        return lib.la_forward_strided(*[vp(p) for p in ptrs[:3]], 1, vp(ptrs[3]), vp(0), B, H, N, D, 1, arr,
+                                      vp(0xA000_0000), 1 << 30, vp(0))
+
+    def bwd(strides, ptrs=base):
+        arr = (ctypes.c_longlong * 24)(*strides)
+        return lib.la_backward_strided(*[vp(p) for p in ptrs], 1, B, H, N, D, 1, arr, 0, vp(0xA000_0000), 1 << 30,
+                                       vp(0))
+
+    bhnd = [H * N * D, N * D, D]
+    assert fwd(bhnd[:2] + [D - 8] + bhnd * 3) == 1            # rows of Q overlap (row stride < D)
+    assert fwd([H * N * D, N * D, D + 4] + bhnd * 3) == 1     # row stride not a multiple of 16 bytes
+    assert fwd([H * N * D, D, 2 * D] + bhnd * 3) == 1         # heads inside rows, but H of them do not fit
+    assert fwd(bhnd * 3 + [0, N * D, D]) == 1                 # zero batch stride with B = 2
+    # fused [B,N,3,H,D]: Q, K, V interleave and may; an output interleaved with them must not meet them
+    fused = [N * 3 * H * D, D, 3 * H * D]
+    q0 = 0x2000_0000
+    ptrs = [q0, q0 + 2 * H * D, q0 + 4 * H * D, q0 + 2]      # O one element into Q's first row
+    assert fwd(fused * 4, ptrs) == 1
+    # backward: dK written over V's rows of the same fused tensor
+    bptrs = [q0, q0 + 2 * H * D, q0 + 4 * H * D] + base[3:5] + [0x6000_0000, q0 + 4 * H * D, 0x7000_0000]
+    assert bwd(fused * 3 + bhnd * 2 + [bhnd[0] * 2, bhnd[1], bhnd[2]] + fused + bhnd, bptrs) == 1
+    # dQ and dK in one fused gradient tensor, overlapping rows (same offset)
+    g0 = 0x6000_0000
+    bptrs = base[:5] + [g0, g0, g0 + 4 * H * D]
+    assert bwd(bhnd * 5 + fused * 3, bptrs) == 1

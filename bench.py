@@ -40,7 +40,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "roofline_traffic.json")
 
 
 def config_dict():
-    return {"workload": WORKLOAD, "B": B, "H": H, "N": N, "D": D, "passes_per_step": list(PASSES),
+    return {"workload": WORKLOAD.replace("N=4096", f"N={N}"), "B": B, "H": H, "N": N, "D": D,
+            "passes_per_step": list(PASSES),
             "tokens_per_step": 2 * B * N, "l2": "inputs larger than L2 (4 x 67 MB per step), no flush",
             "backward": "la_backward_with_forward_state: per-piece K^T V sums taken from the forward's workspace",
             "seed": 1}
@@ -218,6 +219,11 @@ def run_ours(args):
     ws = la.new_workspace(B, H, N, D, True, la.LA_BF16, True, dev)
     outs = {p: {"O": torch.empty_like(Q), "g": torch.empty(B, H, N, device=dev), "dQ": torch.empty_like(Q),
                 "dK": torch.empty_like(Q), "dV": torch.empty_like(Q)} for p in PASSES}
+    if args.layout == "bnhd":  # every [B,H,N,D] operand as a view of a [B,N,H,D] tensor (strided entry points)
+        def bnhd(t):
+            return t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3)
+        Q, K, V, dO = (bnhd(t) for t in (Q, K, V, dO))
+        outs = {p: {k: (bnhd(v) if v.dim() == 4 else v) for k, v in o.items()} for p, o in outs.items()}
     stream = torch.cuda.current_stream()
 
     def step(evs=None, Q=Q, K=K, V=V, dO=dO, outs=outs):
@@ -546,6 +552,7 @@ def run_decode(args):
 
 
 def main():
+    global N
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -553,11 +560,17 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-heads", type=int, default=0, help="heads per reference step (default: one per core)")
+    ap.add_argument("--seq-len", type=int, default=N, help="N of the attention workload (sweeps; default 4096)")
+    ap.add_argument("--layout", choices=("bhnd", "bnhd"), default="bhnd",
+                    help="attention operands contiguous [B,H,N,D] (default) or views of [B,N,H,D] tensors")
     ap.add_argument("--workload", choices=("attention", "decode"), default="attention",
                     help="attention: the fwd+bwd hot path (default); decode: the recurrent decode step")
     ap.add_argument("--profile", action="store_true",
                     help="run only warm-up + timed steps of the hot path (for ncu); prints a reduced line")
     args = ap.parse_args()
+    N = args.seq_len
+    if args.layout != "bhnd" and not args.profile:
+        ap.error("--layout bnhd times the hot path only: add --profile")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.workload == "decode":

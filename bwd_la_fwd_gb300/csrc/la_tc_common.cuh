@@ -31,12 +31,10 @@ struct Slices {
 
 __host__ __device__ __forceinline__ long long slice_lo(const Slices &s, int b) { return (long long)b * s.T / s.G; }
 
-// The CTA whose slice contains flat chunk x.
+// The CTA whose slice contains flat chunk x: the largest b with floor(b T / G) <= x, i.e. b T < (x + 1) G.
 __device__ __forceinline__ int cta_of(const Slices &s, long long x) {
-    int b = (int)((x * s.G) / s.T);
-    while (b > 0 && slice_lo(s, b) > x) --b;
-    while (b + 1 < s.G && slice_lo(s, b + 1) <= x) ++b;
-    return b;
+    const long long b = ((x + 1) * s.G - 1) / s.T;
+    return (int)(b < s.G - 1 ? b : s.G - 1);
 }
 
 // float4 elements of a slot's data: the D x D matrix and the two D-vectors (D = 128).

@@ -517,9 +517,11 @@ template __global__ void tc_fwd_kernel<false, false>(const __grid_constant__ TcP
 // one slot (its own) per piece: kCombinePrefix gives each piece the sum over the head's earlier pieces
 // (causal, chunk order), kCombineSuffix over the later ones (causal, reverse order), kCombineTotal the
 // head's total (non-causal).  grid = (ceil(kSlotF4 / 256), heads; heads beyond the grid's y extent loop);
-// thread x owns float4 x of every slot of its head, and reads each slot before it writes it.
+// thread x owns float4 x of every slot of its head, and reads each slot before it writes it.  At most 32
+// registers, so that eight CTAs fit on an SM and the whole grid (17 x 64 CTAs at the standard shape) runs
+// in one wave: the kernel is a single round of loads and stores.
 // ----------------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ TcParams P) {
+__global__ void __launch_bounds__(256, 8) tc_combine_kernel(const __grid_constant__ TcParams P) {
     griddep_wait();  // the slots come from the previous kernel of the stream
     griddep_launch_dependents();
     if (P.combine_tag && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
@@ -537,13 +539,13 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
             return base + slot_of(h, mode == kCombineSuffix ? b1 - k : b0 + k) * s4;
         };
         float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int g = 0; g < n; g += 8) {  // up to eight loads in flight; each slot read before it is written
-            float4 v[8];
+        for (int g = 0; g < n; g += 4) {  // up to four loads in flight; each slot read before it is written
+            float4 v[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < 4; ++k)
                 if (g + k < n) v[k] = *at(g + k);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < 4; ++k)
                 if (g + k < n) {
                     if (mode != kCombineTotal) *at(g + k) = run;  // exclusive: the sum before this piece
                     run.x += v[k].x;

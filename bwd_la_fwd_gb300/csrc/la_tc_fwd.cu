@@ -338,22 +338,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                         mma_ss(tT, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                                sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
                     mma_commit(barT);
-                    ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x204);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < kC / 16; ++k)  // O = P V, K steps over j (P in TMEM, 8 columns each)
-                        mma_ts(tO, tT + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, k > 0);
+                    // S += K^T V as soon as the epilogue has copied S into this chunk's Sb, so that the
+                    // update runs while the epilogue forms P
                     ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x205);
                     if (!ok) break;
                     tc_fence_after();
-                }
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k)  // O += Q Sb, K steps over d
-                    mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
-                mma_commit(&barO[ob]);
-                if (CAUSAL) {
                     if (c + 1 < pc.e) {
 #pragma unroll
                         for (int k = 0; k < kC / 16; ++k)  // S += K^T V
@@ -361,7 +350,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                                    idMM, 1u);
                     }
                     mma_commit(barS);
+                    ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x204);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kC / 16; ++k)  // O = P V, K steps over j (P in TMEM, 8 columns each)
+                        mma_ts(tO, tT + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, k > 0);
                 }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)  // O += Q Sb, K steps over d
+                    mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                           sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
+                mma_commit(&barO[ob]);
                 mma_commit(&empty[s]);
             }
         }
@@ -434,19 +434,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 // one chunk's pair before the other half's write of the same pair two chunks later
                 const uint32_t tXc = tX + lo + 2 * (it & 1);
                 tmem_st1(tXc + hf, __float_as_uint(part));
-                float vn = 0.f;          // z (half 0) or a (half 1) after this chunk, for row d = i
-                if (CAUSAL) {
-                    ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x208);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (c + 1 < pc.e) {
-                        tmem_half_to_tile(tS + lo, Sb, i, hf);
-                        vn = (hf == 0 ? zc : ac)[i] + zav;  // z_c, a_c of this chunk from the sums kernel
-                        fence_proxy_async_smem();
-                        tc_fence_before();
-                        mbar_arrive(barSb);
-                    }
-                }
                 // g_i from both halves' partial sums
                 tmem_st_wait();
                 tc_fence_before();
@@ -492,6 +479,18 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 }
                 if (!CAUSAL) mbar_arrive(&barOf[ob]);
                 if (CAUSAL) {
+                    // S after this chunk -> Sb for the next one: Q Sb, Sb's reader, is complete (barO above)
+                    ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x208);
+                    if (!ok) break;
+                    tc_fence_after();
+                    float vn = 0.f;  // z (half 0) or a (half 1) after this chunk, for row d = i
+                    if (c + 1 < pc.e) {
+                        tmem_half_to_tile(tS + lo, Sb, i, hf);
+                        vn = (hf == 0 ? zc : ac)[i] + zav;  // z_c, a_c of this chunk from the sums kernel
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        mbar_arrive(barSb);
+                    }
                     epi_sync256();  // everyone has read z and a of this chunk
                     if (c + 1 < pc.e) (hf == 0 ? zc : ac)[i] = vn;
                     epi_sync256();

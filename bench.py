@@ -12,7 +12,8 @@ than the 129 MB L2, so no flush is needed between steps.
 Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs resident in HBM; `e2e` is the
 same metric through the public API with pinned host buffers copied in and results copied out inside
 the timed region; `roofline` is for the call that takes the largest share of the step; `cpu_baseline`
-is the fp64 oracle on a bounded sample of heads on this host's cores.  `--impl reference` times that
+is the fp64 oracle on a bounded sample of heads on this host's cores; `cpu_prefix_baseline` is the oracle's
+O(N D^2) running-state form on the whole workload (the "CPU O(N D^2) baseline").  `--impl reference` times that
 oracle alone, on the same workload and metric.
 """
 from __future__ import annotations
@@ -180,6 +181,22 @@ def sample_heads(cores: int) -> int:
 def sample_tokens(n_heads: int) -> float:
     """Tokens covered by a sample of n_heads head-sequences over both passes (a token spans H heads)."""
     return 2.0 * n_heads * N / H
+
+
+def cpu_prefix_baseline(host):
+    """The oracle's O(N D^2) running-state form (fp64, C, all host cores), as it stands, on the whole
+    workload: causal and non-causal forward + backward of every head."""
+    import oracle
+    from bwd_la_fwd_gb300 import inputs
+    oracle.build()
+    f = {k: inputs.to_f64(v, "bf16") for k, v in host.items()}
+    t0 = time.perf_counter()
+    for causal in (True, False):
+        oracle.prefix_forward(f["Q"], f["K"], f["V"], causal)
+        oracle.prefix_backward(f["Q"], f["K"], f["V"], f["dO"], causal)
+    dt = time.perf_counter() - t0
+    return {"value": 2 * B * N / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle prefix form",
+            "sample": f"the whole step (all {B * H} heads, both passes, fwd+bwd) in fp64; {dt:.1f} s"}
 
 
 def cpu_baseline(host):
@@ -390,6 +407,7 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(host)
+        line["cpu_prefix_baseline"] = cpu_prefix_baseline(host)
     return line
 
 

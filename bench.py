@@ -548,7 +548,7 @@ def run_decode(args):
         "config": {"workload": f"LA decode step B={DEC_B} H={DEC_H} D={D} bf16 tokens, fp32 state after a "
                                f"{N}-token prompt", "l2": "state 268 MB > L2, no flush"},
         "roofline": {"bound": "hbm", "call": "la_decode_step", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None, "peak_source": peak_kind,
+                     "frac": achieved / hbm, "traffic": traffic_for("decode_step"), "peak_source": peak_kind,
                      "alg_bytes_per_launch": decode_alg_bytes(bh), "avg_us": ms * 1e3},
         "e2e": {"value": DEC_B / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": 3 * q.numel() * ELEM,
                 "d2h_bytes_per_step": o.numel() * ELEM + g.numel() * 4, "ms_per_step": e2e_ms},

@@ -302,9 +302,10 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after timed region: {la.la_status_string(st)}")
     ms = ev_start.elapsed_time(ev_end) / args.steps
-    for evs in evsets:
-        for c in calls:
-            per_call[c] += evs[c][0].elapsed_time(evs[c][1]) / args.steps
+    samples = {c: [evs[c][0].elapsed_time(evs[c][1]) for evs in evsets] for c in calls}
+    for c in calls:
+        per_call[c] = sum(samples[c]) / args.steps
+    per_call_median = {c: statistics.median(samples[c]) for c in calls}
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([ms], device=dev)
@@ -398,6 +399,7 @@ def run_ours(args):
         "tflops": flops / (ms * 1e-3) / 1e12,
         "roofline_frac_step": roof_time / (ms * 1e-3),
         "calls_us": {c: per_call[c] * 1e3 for c in calls},
+        "calls_us_median": {c: per_call_median[c] * 1e3 for c in calls},
         "roofline": roof,
         "e2e": {"value": world * 2 * B * N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -49,23 +49,6 @@ __device__ __forceinline__ void tmem_half_to_bf16(uint32_t taddr, int hf, F f, u
     }
 }
 
-// Sum over rows [64 rh, 64 rh + 64) of w[r] * X[r][2 cp .. 2 cp + 1] for a bf16 tile X (two 64-column
-// boxes, 128-byte swizzle); w == nullptr means weights of one.
-__device__ __forceinline__ float2 colsum_half(const unsigned char *tile2, int cp, int rh, const float *w) {
-    const int col = 2 * cp;
-    const unsigned char *tile = tile2 + (col / 64) * kBox;
-    const int cc = col % 64;
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-    for (int r = 64 * rh; r < 64 * rh + 64; ++r) {
-        const uint32_t v = *(const uint32_t *)(tile + sw128_off(r, cc / 8) + (cc % 8) * 2);
-        const float wr = w ? w[r] : 1.f;
-        s0 = fmaf(wr, bf16lo(v), s0);
-        s1 = fmaf(wr, bf16hi(v), s1);
-    }
-    return make_float2(s0, s1);
-}
-
 // Reads this half's 64 columns of an fp32 TMEM block, adds add_scale * add[c] (c = column), rounds to
 // bf16 and writes them into row `row`, box hf of a two-box 128B-swizzled tile (the layout of the output
 // TMA maps).
@@ -91,27 +74,6 @@ __device__ __forceinline__ void tmem_half_to_out(uint32_t taddr, int hf, const f
             *(uint4 *)(tile + sw128_off(row, 4 * half32 + g4)) = w;
         }
     }
-}
-
-// q_row . y over box hf of a bf16 tile, with y the 64 fp32 values (bit patterns) of this half.
-__device__ __forceinline__ float dot_half_regs(const unsigned char *tile2, int row, int hf, const uint32_t (&y0)[32],
-                                               const uint32_t (&y1)[32]) {
-    const unsigned char *tile = tile2 + hf * kBox;
-    float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-        const uint4 v = *(const uint4 *)(tile + sw128_off(row, g8));
-        const uint32_t *yy = g8 < 4 ? y0 + 8 * g8 : y1 + 8 * (g8 - 4);
-        acc0 = fmaf(bf16lo(v.x), __uint_as_float(yy[0]), acc0);
-        acc1 = fmaf(bf16hi(v.x), __uint_as_float(yy[1]), acc1);
-        acc0 = fmaf(bf16lo(v.y), __uint_as_float(yy[2]), acc0);
-        acc1 = fmaf(bf16hi(v.y), __uint_as_float(yy[3]), acc1);
-        acc0 = fmaf(bf16lo(v.z), __uint_as_float(yy[4]), acc0);
-        acc1 = fmaf(bf16hi(v.z), __uint_as_float(yy[5]), acc1);
-        acc0 = fmaf(bf16lo(v.w), __uint_as_float(yy[6]), acc0);
-        acc1 = fmaf(bf16hi(v.w), __uint_as_float(yy[7]), acc1);
-    }
-    return acc0 + acc1;
 }
 
 // Row `row` of dQ over columns [64 hf, 64 hf + 64): x * ig - dt * z, rounded to bf16 into box hf of the

@@ -47,7 +47,6 @@ __device__ __forceinline__ void tile_store(const CUtensorMap *m, const void *src
     else tma_store_4d(m, src, x, row, hc.h, hc.b);
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane quarter
 __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }

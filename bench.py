@@ -217,6 +217,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over the ranks of the job (its time is that of its slowest replica); x alone without
+    a process group."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(ms_max: float, world: int) -> float:
+    """Whole-job throughput: every replica processes one step of 2 B N tokens in the slowest one's time."""
+    return world * 2 * B * N / (ms_max * 1e-3)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -306,12 +323,8 @@ def run_ours(args):
     for c in calls:
         per_call[c] = sum(samples[c]) / args.steps
     per_call_median = {c: statistics.median(samples[c]) for c in calls}
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * 2 * B * N / (ms * 1e-3)
+    ms = max_over_ranks(ms, dev)
+    value = job_tokens_per_s(ms, world)
     clocks = sampler.summary(t_spin, t_wall1)
     clocks["window"] = "spin-up + warm-up + timed region"
     if args.profile:  # hot path only (for profilers): no end-to-end leg, memory probe or CPU baseline
@@ -367,11 +380,7 @@ def run_ours(args):
     st = la.la_get_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after the end-to-end leg: {la.la_status_string(st)}")
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     tb = B * H * N * D * ELEM
     h2d = 4 * tb
     d2h = sum(v.numel() * v.element_size() for p in PASSES for v in outs[p].values())
@@ -401,7 +410,7 @@ def run_ours(args):
         "calls_us": {c: per_call[c] * 1e3 for c in calls},
         "calls_us_median": {c: per_call_median[c] * 1e3 for c in calls},
         "roofline": roof,
-        "e2e": {"value": world * 2 * B * N / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens_per_s(e2e_ms, world), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": int(launches),
         "clocks": clocks,

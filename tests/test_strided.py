@@ -99,3 +99,20 @@ def test_reuse_with_other_key_strides_reports_state_error():
     K_other = torch.as_strided(Kb, Kb.shape, (Kb.stride(0), 300 * 128, 128, 1))  # the same buffer read as [B,H,N,D]
     la.la_backward(Q, K_other, V, O, dO, True, workspace=ws, reuse_forward_state=True)
     assert la.la_get_status(ws) == 7
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+def test_bnhd_views_at_the_standard_shape(causal):
+    """The 4-D tensor-map kernels at the benchmark's shape (B = 4, H = 16, N = 4096, D = 128, bf16): every
+    output equals the contiguous call's bit for bit, forward and the reusing backward."""
+    import torch
+    B, H, N, D = 4, 16, 4096, 128
+    g = torch.Generator(device="cuda").manual_seed(440 + causal)
+    Q, K = (torch.randn(B, H, N, D, device="cuda", generator=g) / D ** 0.5 for _ in range(2))
+    V, dO = (torch.randn(B, H, N, D, device="cuda", generator=g) for _ in range(2))
+    Q, K, V, dO = (t.to(torch.bfloat16) for t in (Q, K, V, dO))
+    ref = _run(Q, K, V, dO, causal, reuse=True)
+    outs = [_bnhd(torch.empty_like(Q)) for _ in range(4)]
+    got = _run(*(_bnhd(t) for t in (Q, K, V, dO)), causal, outs=outs, reuse=True)
+    for name, a, b in zip(("O", "g", "dQ", "dK", "dV"), got, ref):
+        assert torch.equal(a, b), name

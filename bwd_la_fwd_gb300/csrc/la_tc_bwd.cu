@@ -659,6 +659,16 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                     tile_load<FLAT>(st + nb * kBox, &P.tmQ, &full[s], nb * 64, c * kC, hc);
                     tile_load<FLAT>(st + TB + nb * kBox, &P.tmdO, &full[s], nb * 64, c * kC, hc);
                 }
+                // the chunk that will next refill this stage, into L2 (within the slice)
+                const long long nx = pc.h * P.sl.nchunk + c + NST;
+                if (nx < slice_lo(P.sl, blockIdx.x + 1)) {
+                    const int nrow = (int)(nx % P.sl.nchunk) * kC;
+                    const HeadCoord hn = head_coord<FLAT>(nx / P.sl.nchunk, P.H);
+                    for (int nb = 0; nb < NB; ++nb) {
+                        tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
+                        tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
+                    }
+                }
             }
         }
         if (!ok) {

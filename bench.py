@@ -486,6 +486,114 @@ def run_reference(args):
 DEC_B, DEC_H = 256, 16  # sequences decoded together, heads each (D as above, bf16 tokens, fp32 state)
 
 
+# ------------------------------------------------------------------------------ config sweep ---
+
+SWEEP_CASES = (
+    # (name, B, H, N, D, layers, seed): the head-size sweep, the sequence-length sweep and the
+    # 24-layer decoder training step, all causal bf16 (the standard shape is the default line's)
+    *[(f"head_size_D{d}", 4, 16, 4096, d, 1, 2) for d in (32, 64, 256)],
+    *[(f"seq_len_N{n}", 4, 16, n, 128, 1, 3) for n in (1024, 2048, 8192, 16384, 32768, 65536)],
+    ("decoder_24_layers", 8, 16, 2048, 128, 24, 4),
+)
+
+
+def shape_roofline_s(b, h, n, d, hbm, tfl):
+    """Roofline time (seconds) of one causal forward + backward of one layer at this shape: per call the
+    slower of its algorithmic bytes at the HBM peak and its algorithmic flops at the bf16 peak."""
+    t = b * h * n * d * ELEM
+    fwd = max((4 * t + 4 * b * h * n) / (hbm * 1e9), 4 * d * d * b * h * n / (tfl * 1e12))
+    bwd = max(8 * t / (hbm * 1e9), 10 * d * d * b * h * n / (tfl * 1e12))
+    return fwd, bwd
+
+
+def run_sweep(args):
+    """The other workloads of the method's measurements, one JSON line each (rank 0 only): causal
+    forward + backward per layer, timed with CUDA events (median over the timed steps), against the
+    roofline of the shape, with the peak device memory of the case against its I/O floor.  Inputs are
+    drawn on the device (torch's generator; Q, K ~ N(0, 1/D), V, dO ~ N(0, 1)); the 24-layer case draws
+    every layer's tensors separately and runs the 24 forwards, then the 24 backwards in reverse order,
+    each backward reusing its layer's forward sums from that layer's own workspace."""
+    import torch
+
+    from bwd_la_fwd_gb300 import la
+    rank, _, local = dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    la.load_library()
+    hbm, tfl, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream()
+    for name, b, h, n, d, layers, seed in SWEEP_CASES:
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        gen = torch.Generator(device=dev).manual_seed(seed)
+
+        def layer():
+            x = {}
+            for op in ("Q", "K", "V", "dO"):
+                t = torch.randn(b, h, n, d, device=dev, generator=gen)
+                x[op] = (t.div_(d ** 0.5) if op in ("Q", "K") else t).to(torch.bfloat16)
+            x.update({"O": torch.empty_like(x["Q"]), "g": torch.empty(b, h, n, device=dev),
+                      "dQ": torch.empty_like(x["Q"]), "dK": torch.empty_like(x["Q"]), "dV": torch.empty_like(x["Q"]),
+                      "ws": la.new_workspace(b, h, n, d, True, la.LA_BF16, True, dev)})
+            return x
+
+        L = [layer() for _ in range(layers)]
+
+        def step(evs=None):
+            for i, x in enumerate(L):
+                if evs is not None and i == 0:
+                    evs[0].record(stream)
+                la.la_forward(x["Q"], x["K"], x["V"], True, O=x["O"], normaliser=x["g"], workspace=x["ws"])
+            if evs is not None:
+                evs[1].record(stream)
+            for x in reversed(L):
+                la.la_backward(x["Q"], x["K"], x["V"], x["O"], x["dO"], True, dQ=x["dQ"], dK=x["dK"],
+                               dV=x["dV"], workspace=x["ws"], reuse_forward_state=True)
+            if evs is not None:
+                evs[2].record(stream)
+
+        # working sets below twice the 129 MB L2 are flushed between timed steps (outside the events)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if layers * 8 * b * h * n * d * ELEM < (256 << 20) else None
+        torch.cuda.reset_peak_memory_stats(dev)  # from here: the case's tensors, workspaces and what the calls add
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evsets = []
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            step(evs)
+            evsets.append(evs)
+        torch.cuda.synchronize()
+        st = [la.la_get_status(x["ws"]) for x in L]
+        if any(st):
+            raise RuntimeError(f"{name}: device status {[la.la_status_string(s) for s in st if s]}")
+        fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evsets)
+        bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evsets)
+        peak = torch.cuda.max_memory_allocated(dev) - base - (flush.numel() if flush is not None else 0)
+        floor = layers * (8 * b * h * n * d * ELEM + 4 * b * h * n)
+        rf, rb = shape_roofline_s(b, h, n, d, hbm, tfl)
+        step_ms = fwd_ms + bwd_ms
+        line = {"workload": "sweep", "case": name, "B": b, "H": h, "N": n, "D": d, "layers": layers,
+                "causal": True, "dtype": "bf16", "seed": seed, "steps": args.steps, "warmup": args.warmup,
+                "path": "tensor cores" if d in (32, 64, 128) else "CUDA cores",
+                "fwd_us": fwd_ms * 1e3, "bwd_us": bwd_ms * 1e3, "step_ms": step_ms,
+                "tokens_per_s": b * n / (step_ms * 1e-3),
+                "tflops": layers * 14 * d * d * b * h * n / (step_ms * 1e-3) / 1e12,
+                "roofline_us": layers * (rf + rb) * 1e6,
+                "roofline_frac": layers * (rf + rb) / (step_ms * 1e-3),
+                "roofline_frac_fwd": layers * rf / (fwd_ms * 1e-3), "roofline_frac_bwd": layers * rb / (bwd_ms * 1e-3),
+                "peak_source": peak_kind, "l2": "flushed between steps" if flush is not None else "inputs larger than L2",
+                "peak_memory": {"bytes": int(peak), "floor": int(floor), "ratio": peak / floor}}
+        print(json.dumps(line), flush=True)
+        del L, step, evsets, flush
+    return None
+
+
 def decode_alg_bytes(bh: int) -> int:
     """HBM bytes of one decode step: the fp32 state S read and written, z and a read and written, the
     counts, q, k, v read and o written (bf16), the fp32 normaliser written."""
@@ -592,8 +700,9 @@ def main():
     ap.add_argument("--seq-len", type=int, default=N, help="N of the attention workload (sweeps; default 4096)")
     ap.add_argument("--layout", choices=("bhnd", "bnhd"), default="bhnd",
                     help="attention operands contiguous [B,H,N,D] (default) or views of [B,N,H,D] tensors")
-    ap.add_argument("--workload", choices=("attention", "decode"), default="attention",
-                    help="attention: the fwd+bwd hot path (default); decode: the recurrent decode step")
+    ap.add_argument("--workload", choices=("attention", "decode", "sweep"), default="attention",
+                    help="attention: the fwd+bwd hot path (default); decode: the recurrent decode step; "
+                         "sweep: the head-size, sequence-length and 24-layer cases, one line each")
     ap.add_argument("--profile", action="store_true",
                     help="run only warm-up + timed steps of the hot path (for ncu); prints a reduced line")
     args = ap.parse_args()
@@ -604,6 +713,8 @@ def main():
         args.warmup = 3
     if args.workload == "decode":
         line = run_decode(args) if args.impl == "ours" and dist_env()[0] == 0 else None
+    elif args.workload == "sweep":
+        line = run_sweep(args) if args.impl == "ours" else None
     else:
         line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:

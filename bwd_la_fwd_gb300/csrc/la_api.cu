@@ -41,9 +41,12 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     p->seg_len = (int)seg;
     p->nseg = (int)(((long long)N + seg - 1) / seg);
     if (BH * p->nseg >= (1LL << 31)) return false;
-    p->stride = (long long)round_up((size_t)D * D + 2 * (size_t)D, 64);
     p->acc_bytes = dtype == LA_F32 ? 8 : 4;
     p->use_tc = tc_supported(*p);
+    // a state slot holds a D x D matrix and two D-vectors; the tensor-core kernels always work on D = 128
+    // (narrower heads are zero-extended), so their slots have that size
+    const size_t sd = p->use_tc ? 128 : (size_t)D;
+    p->stride = (long long)round_up(sd * sd + 2 * sd, 64);
     if (p->use_tc) {
         // forward-direction slots (forward and backward), reverse-direction slots and per-row g, dt
         // (backward only)

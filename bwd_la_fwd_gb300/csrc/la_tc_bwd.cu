@@ -212,11 +212,13 @@ __device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h,
     *ye = P.chunk_ye[((size_t)h * P.sl.nchunk + c) * 256 + hf * 128 + j];
 }
 
-// Issues the TMA stores of a two-box output tile from shared memory and commits them.  One thread.
+// Issues the TMA stores of a two-box output tile from shared memory (the boxes that hold the operand's
+// columns: nbox of them) and commits them.  One thread.
 template <bool FLAT>
-__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, HeadCoord hc) {
+__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, HeadCoord hc,
+                                           int nbox) {
     tile_store<FLAT>(map, tile2, 0, row0, hc);
-    tile_store<FLAT>(map, tile2 + kBox, 64, row0, hc);
+    if (nbox > 1) tile_store<FLAT>(map, tile2 + kBox, 64, row0, hc);
     bulk_commit();
 }
 
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 if (nx < hi) {
                     const int nh = (int)(nx / P.sl.nchunk), nrow = (int)(nx % P.sl.nchunk) * kC;
                     const HeadCoord hn = head_coord<FLAT>(nh, P.H);
-                    for (int nb = 0; nb < NB; ++nb) {
+                    for (int nb = 0; nb < P.nbox; ++nb) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmK, nb * 64, nrow, hn);
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
                 fence_proxy_async_smem();
                 epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
-                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, (int)row0, head_coord<FLAT>(pc.h, P.H));
+                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, (int)row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
                 if (c + 1 < pc.e) {
                     tmem_half_to_tile(R2 + lo, Sb, i, hf);
                     fence_proxy_async_smem();
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 if (nx < slice_lo(P.sl, blockIdx.x + 1)) {
                     const int nrow = (int)(nx % P.sl.nchunk) * kC;
                     const HeadCoord hn = head_coord<FLAT>(nx / P.sl.nchunk, P.H);
-                    for (int nb = 0; nb < NB; ++nb) {
+                    for (int nb = 0; nb < P.nbox; ++nb) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
                     }
@@ -771,7 +773,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 }
                 mbar_arrive(barDt);
                 epi_sync256();  // dQ of every row is staged
-                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, c * kC, head_coord<FLAT>(pc.h, P.H));
+                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, c * kC, head_coord<FLAT>(pc.h, P.H), P.nbox);
             }
             if (!ok) break;
             ok = wait_or_abort(barPP, pno & 1, abort_flag, P.status, 0x32A);
@@ -901,7 +903,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 int nc;
                 if (next_rev_chunk(pi, pc, c, &nh, &nc)) {  // the next chunk to be walked, into L2
                     const HeadCoord hn = head_coord<FLAT>(nh, P.H);
-                    for (int nb = 0; nb < NB; ++nb) {
+                    for (int nb = 0; nb < P.nbox; ++nb) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nc * kC, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nc * kC, hn);
                         tile_prefetch<FLAT>(&P.tmK, nb * 64, nc * kC, hn);
@@ -1049,7 +1051,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 tmem_half_to_out(R2 + lo, hf, ec, 1.f, dvt, j);
                 fence_proxy_async_smem();
                 epi_sync256();
-                if (u == 0) store_tile<FLAT>(&P.tmdV, dvt, (int)row0, head_coord<FLAT>(pc.h, P.H));
+                if (u == 0) store_tile<FLAT>(&P.tmdV, dvt, (int)row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
                 // dK_j = [R1]_j - y
                 ok = wait_or_abort(barK, ph, abort_flag, P.status, 0x40B);
                 if (!ok) break;
@@ -1057,7 +1059,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 tmem_half_to_out(R1 + lo, hf, yc, -1.f, dkt, j);
                 fence_proxy_async_smem();
                 epi_sync256();  // dK rows staged; every read of yc and ec for this chunk is done
-                if (u == 0) store_tile<FLAT>(&P.tmdK, dkt, (int)row0, head_coord<FLAT>(pc.h, P.H));
+                if (u == 0) store_tile<FLAT>(&P.tmdK, dkt, (int)row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
                 // P (with this chunk's rows, for the earlier chunks) -> Pb: its update finished before dV
                 if (c > pc.a) {
                     tmem_half_to_tile(R3 + lo, Pb, j, hf);
@@ -1239,7 +1241,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
                 tc_fence_before();
                 mbar_arrive(barKf);
                 epi_sync256();
-                if (u == 0) store_tile<FLAT>(&P.tmdK, st + TB, row0, head_coord<FLAT>(pc.h, P.H));
+                if (u == 0) store_tile<FLAT>(&P.tmdK, st + TB, row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
                 // dV_j = [R2]_j + e, staged in the K tile (its last reader, dV = K Pb, is done)
                 ok = wait_or_abort(barV, ph, abort_flag, P.status, 0x427);
                 if (!ok) break;
@@ -1250,7 +1252,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
                 mbar_arrive(barVf);
                 epi_sync256();
                 if (u == 0) {
-                    store_tile<FLAT>(&P.tmdV, st, row0, head_coord<FLAT>(pc.h, P.H));
+                    store_tile<FLAT>(&P.tmdV, st, row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
                     bulk_wait_read0();
                     mbar_arrive(&empty[s]);
                 }

@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 tc_fence_before();
                 epi_sync256();  // the whole O tile is in shared memory
                 if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < NB; ++nb) tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
+                    for (int nb = 0; nb < P.nbox; ++nb) tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_commit();
                     bulk_wait_read0();       // the tile has been read out of shared memory
                     mbar_arrive(&empty[s]);  // the stage may be refilled
@@ -590,7 +590,7 @@ int sm_count() {
 }
 
 // Operand `op` as a bf16 map with boxes of 128 rows x 64 columns of one head, 128-byte swizzle; rows
-// past N read as zero and are not written.  flat: 3-D over {D, N, B H} (the operand's batch stride is H
+// past N and columns past D (D = 32, 64: the kernels work on 128 columns) read as zero and are not written.  flat: 3-D over {D, N, B H} (the operand's batch stride is H
 // times its head stride); else 4-D over {D, N, H, B}.
 bool make_map(CUtensorMap *m, const void *ptr, const Plan &p, int op, bool flat) {
     auto enc = encode_fn();
@@ -651,7 +651,8 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     uint64_t hsh = 0xcbf29ce484222325ull;  // FNV-1a over K's and V's strides
     for (int op : {kOpK, kOpV})
         for (long long v : {p.lay[op].sb, p.lay[op].sh, p.lay[op].sn}) hsh = (hsh ^ (uint64_t)v) * 0x100000001b3ull;
-    P.kv_layout = hsh;
+    P.kv_layout = (hsh ^ (uint64_t)p.D) * 0x100000001b3ull;
+    P.nbox = (p.D + 63) / 64;
     P.slot_stride = p.stride;
     P.slots = (float *)(ws + p.off_states);
     P.chunk_za = (float *)(ws + p.off_chunkza);
@@ -693,7 +694,7 @@ cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s) {
 
 using namespace tc_host;
 
-bool tc_supported(const Plan &p) { return p.dtype == 1 && p.D == 128; }
+bool tc_supported(const Plan &p) { return p.dtype == 1 && (p.D == 32 || p.D == 64 || p.D == 128); }
 
 size_t tc_slot_bytes(const Plan &p) { return ((size_t)p.BH + tc::kMaxCtas) * (size_t)p.stride * sizeof(float); }
 

@@ -19,6 +19,8 @@ struct TcParams {
     Slices sl;
     int H;                  // heads per batch entry: flat head bh = b H + h
     int flat;               // the maps are 3-D over {D, N, B H} (kernels <FLAT = true>), else 4-D over {D, N, H, B}
+    int nbox;               // 64-column boxes holding the operands' D columns: 2 for D = 128, 1 for D = 32, 64
+                            // (the kernels compute with D = 128; columns past D load as zero and are not stored)
     uint64_t kv_layout;     // hash of K's and V's strides (part of the per-piece sums' identity)
     long long N;
     float *slots;           // per-piece state sums, slot stride `slot_stride` floats

@@ -21,7 +21,7 @@ def _tensors(B, H, N, D, dtype, seed):
 
 
 @pytest.mark.parametrize("causal", [1, 0])
-@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("f32", 64)])
 def test_reuse_is_bit_identical_to_la_backward(causal, dtype, D):
     import torch
     from bwd_la_fwd_gb300 import la

@@ -2,6 +2,8 @@
 library as they are (no transpose copy) and give exactly what the contiguous calls give on the same
 values, on both paths (tensor cores: bf16, D = 128; CUDA cores: fp32), causal and non-causal, forward,
 backward and the backward that reuses the forward's sums; one case is also checked against the oracle.
+bf16 with D = 32 or 64 runs on the tensor-core kernels with the columns past D zero-extended by the tensor
+maps: the fused cases check that no store reaches past an operand's D columns into its neighbour's.
 """
 import numpy as np
 import pytest
@@ -11,7 +13,7 @@ from bwd_la_fwd_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-CASES = [("bf16", 128), ("f32", 64)]
+CASES = [("bf16", 128), ("bf16", 64), ("bf16", 32), ("f32", 64)]
 
 
 def _bnhd(t):

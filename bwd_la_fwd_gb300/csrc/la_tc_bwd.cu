@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 if (nx < hi) {
                     const int nh = (int)(nx / P.sl.nchunk), nrow = (int)(nx % P.sl.nchunk) * kC;
                     const HeadCoord hn = head_coord<FLAT>(nh, P.H);
-                    for (int nb = 0; nb < P.nbox; ++nb) {
+                    for (int nb = 0; nb < NB; ++nb) if (nb == 0 || P.nbox > 1) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmK, nb * 64, nrow, hn);
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 if (nx < slice_lo(P.sl, blockIdx.x + 1)) {
                     const int nrow = (int)(nx % P.sl.nchunk) * kC;
                     const HeadCoord hn = head_coord<FLAT>(nx / P.sl.nchunk, P.H);
-                    for (int nb = 0; nb < P.nbox; ++nb) {
+                    for (int nb = 0; nb < NB; ++nb) if (nb == 0 || P.nbox > 1) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nrow, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nrow, hn);
                     }
@@ -903,7 +903,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
                 int nc;
                 if (next_rev_chunk(pi, pc, c, &nh, &nc)) {  // the next chunk to be walked, into L2
                     const HeadCoord hn = head_coord<FLAT>(nh, P.H);
-                    for (int nb = 0; nb < P.nbox; ++nb) {
+                    for (int nb = 0; nb < NB; ++nb) if (nb == 0 || P.nbox > 1) {
                         tile_prefetch<FLAT>(&P.tmQ, nb * 64, nc * kC, hn);
                         tile_prefetch<FLAT>(&P.tmdO, nb * 64, nc * kC, hn);
                         tile_prefetch<FLAT>(&P.tmK, nb * 64, nc * kC, hn);

@@ -472,7 +472,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 tc_fence_before();
                 epi_sync256();  // the whole O tile is in shared memory
                 if (threadIdx.x == 64) {
-                    for (int nb = 0; nb < P.nbox; ++nb) tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
+                    for (int nb = 0; nb < NB; ++nb)
+                        if (nb == 0 || P.nbox > 1)
+                            tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_commit();
                     bulk_wait_read0();       // the tile has been read out of shared memory
                     mbar_arrive(&empty[s]);  // the stage may be refilled

@@ -18,8 +18,10 @@
  * Layout.  Q, K, V, O, dO, dQ, dK, dV are dense, contiguous [B, H, N, D] tensors of one element
  * type (LA_F32 = float, LA_BF16 = bfloat16), element (b, h, i, d) at ((b H + h) N + i) D + d (the
  * *_strided entry points take other layouts).  The
- * normaliser is float [B, H, N].  All accumulation is in fp32.  Supported: B, H >= 1 (B*H < 2^31),
- * N >= 1 (B*H*N*D < 2^40), D in {16, 32, 64, 128, 256}.
+ * normaliser is float [B, H, N].  bf16 storage accumulates in fp32, fp32 storage in fp64.  Supported:
+ * B, H >= 1 (B*H < 2^31), N >= 1 (B*H*N*D < 2^40), D in {16, 32, 64, 128, 256}.  bf16 with D = 32, 64,
+ * 128 runs on the tensor-core kernels (D < 128 zero-extended to 128 columns); fp32 storage and bf16 with
+ * D = 16 or 256 run on the CUDA-core (SIMT) kernels.
  *
  * Memory.  Every pointer is a DEVICE pointer except where stated.  The caller owns every buffer; the
  * library never allocates device or host memory and never synchronises the stream (except
@@ -112,7 +114,7 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * have been la_forward or la_backward on the same K and V buffers (same pointers, unchanged contents) and
  * the same B, H, N, D and dtype.  The workspace records which K, V and shape its sums belong to; when the
  * record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.  Unchanged
- * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or D != 128)
+ * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or D = 16 or 256)
  * there are no such sums to reuse and this call is la_backward.
  */
 int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,

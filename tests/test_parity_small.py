@@ -86,11 +86,12 @@ def test_multi_chunk_slices_narrow_heads(oracle_lib, monkeypatch, D, causal):
     _check(oracle_lib, 2, 3, 549, D, "bf16", causal, seed=41 + D)
 
 
-@pytest.mark.parametrize("dtype,D,tc", [("bf16", 32, True), ("bf16", 64, True), ("bf16", 128, True),
-                                        ("bf16", 256, False), ("f32", 64, False), ("f32", 128, False)])
+@pytest.mark.parametrize("dtype,D,tc", [("bf16", 16, False), ("bf16", 32, True), ("bf16", 64, True),
+                                        ("bf16", 128, True), ("bf16", 256, False), ("f32", 64, False),
+                                        ("f32", 128, False)])
 def test_path_taken(dtype, D, tc):
-    """bf16 with D = 32, 64, 128 runs on the tensor-core kernels (backward: 5 launches), the rest on the
-    CUDA-core kernels (backward: 8 launches)."""
+    """bf16 with D = 32, 64, 128 runs on the tensor-core kernels (backward: 5 launches), the rest (bf16 with
+    D = 16 or 256, fp32) on the CUDA-core kernels (backward: 8 launches)."""
     import torch
     from bwd_la_fwd_gb300 import la
     x = inputs.generate(1, 2, 300, D, 3, dtype=dtype)

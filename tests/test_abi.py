@@ -63,6 +63,22 @@ def test_workspace_sizes(lib):
     assert ws(4, 16, 65536, 128, 1, 1, 1) <= 0.2 * 16 * (8 * 4 * 16 * 65536 * 128 * 2)
 
 
+def test_narrow_bf16_heads_take_the_tensor_core_workspace(lib):
+    """bf16 with D = 32, 64 runs on the D = 128 tensor-core kernels (columns past D zero-extended): its
+    workspace is the D = 128 one (state slots of 128 x 128 + 2 x 128 floats, per-row and per-chunk sums),
+    for any B, H, N and either mask; bf16 D = 16, 256 and fp32 are sized by their own D (CUDA-core path)."""
+    ws = lib.la_workspace_bytes
+    for B, H, N in ((1, 1, 1), (2, 3, 549), (4, 16, 4096)):
+        for causal in (0, 1):
+            for bw in (0, 1):
+                ref = ws(B, H, N, 128, causal, 1, bw)
+                assert ws(B, H, N, 64, causal, 1, bw) == ref
+                assert ws(B, H, N, 32, causal, 1, bw) == ref
+    assert ws(2, 3, 549, 256, 1, 1, 1) != ws(2, 3, 549, 128, 1, 1, 1)
+    assert ws(2, 3, 549, 16, 1, 1, 1) < ws(2, 3, 549, 32, 1, 1, 1)
+    assert ws(2, 3, 549, 64, 1, 0, 1) < ws(2, 3, 549, 128, 1, 0, 1)   # fp32: CUDA-core states of D x D
+
+
 def _fwd(lib, Q=0x1000, K=0x2000_0000, V=0x4000_0000, O=0x6000_0000, g=0, B=1, H=1, N=8, D=64, dt=1,
          ws=0x8000_0000, wsb=1 << 30):
     vp = ctypes.c_void_p

@@ -1,0 +1,47 @@
+"""bench.py's host arithmetic on CPU (no GPU): the roofline of a shape and the algorithmic figures the
+JSON line reports, against the roofline table worked out from the method's stated costs (forward: Q, K,
+V read, O and the fp32 normaliser written, 4 D^2 flops per row; backward: eight tensor volumes, 10 D^2
+flops per row) with a 6776.3 GB/s copy and a 1912.5 TFLOP/s bf16 rate: 39.8 us forward, 79.2 us
+backward at B = 4, H = 16, N = 4096, D = 128, every call HBM-bound."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_standard_shape_roofline():
+    fwd, bwd = bench.shape_roofline_s(4, 16, 4096, 128, 6776.3, 1912.5)
+    assert fwd * 1e6 == pytest.approx(39.8, abs=0.05)
+    assert bwd * 1e6 == pytest.approx(79.2, abs=0.05)
+    # the bench line's own figures for that shape agree with the sweep's helper
+    assert bench.alg_bytes("fwd") == 4 * 4 * 16 * 4096 * 128 * 2 + 4 * 4 * 16 * 4096
+    assert bench.alg_bytes("bwd") == 8 * 4 * 16 * 4096 * 128 * 2
+    assert bench.alg_bytes("fwd") / (6776.3e9) == pytest.approx(fwd)
+
+
+@pytest.mark.parametrize("D,fwd_us,bwd_us", [(32, 10.1, 19.8), (64, 20.0, 39.6), (256, 79.4, 158.5)])
+def test_head_size_rooflines(D, fwd_us, bwd_us):
+    fwd, bwd = bench.shape_roofline_s(4, 16, 4096, D, 6776.3, 1912.5)
+    assert fwd * 1e6 == pytest.approx(fwd_us, abs=0.1)
+    assert bwd * 1e6 == pytest.approx(bwd_us, abs=0.1)
+
+
+def test_intensity_stays_below_the_ridge():
+    """Flops per byte of every call of the sweep stay below the ridge (1912.5 TF / 6776.3 GB/s = 282):
+    the roofline of each is its bytes."""
+    for _, b, h, n, d, _, _ in bench.SWEEP_CASES:
+        t = b * h * n * d * 2
+        assert 4 * d * d * b * h * n / (4 * t + 4 * b * h * n) < 282
+        assert 10 * d * d * b * h * n / (8 * t) < 282
+
+
+def test_sweep_cases_are_the_measured_workloads():
+    names = [c[0] for c in bench.SWEEP_CASES]
+    assert names == ["head_size_D32", "head_size_D64", "head_size_D256", "seq_len_N1024", "seq_len_N2048",
+                     "seq_len_N8192", "seq_len_N16384", "seq_len_N32768", "seq_len_N65536", "decoder_24_layers"]
+    assert bench.SWEEP_CASES[-1][1:] == (8, 16, 2048, 128, 24, 4)

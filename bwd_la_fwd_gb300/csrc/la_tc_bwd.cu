@@ -1,4 +1,4 @@
-// la_tc_bwd.cu -- tcgen05 / TMA backward of the bf16 path (D = 128).
+// la_tc_bwd.cu -- tcgen05 / TMA backward of the bf16 path (kernels on 128 columns; D = 32, 64 zero-extended).
 //
 // Gradients of L = sum_i dO_i . O_i ("Transformer Based Linear Attention with Optimized GPU Kernel
 // Implementation", sciencestack.ai page, TL;DR: analytical gradients of the LA head).  With
@@ -807,7 +807,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
 //   next 32); dV = P^T dOt + K Pb (R2, then + e) while U^T is formed, then dK = U^T Q + V Pb^T (R1,
 //   over the consumed Wt^T, then - y); P += Q^T dOt (R3: the sum over later rows, for the earlier
 //   chunks); then y += y_c, e += e_c.
-// Pb is the bf16 copy of P.  dK and dV leave through staging tiles of their own, so the stage is released
+// Pb is the bf16 copy of P.  Wt^T takes dOt rounded to bf16, so U^T = Wt^T - dt carries ~2^-9 of
+// |dO . v| / g where the two terms cancel (a single row: dK is then 0 by the definition); the dQ walk
+// forms W' from dO itself.  dK and dV leave through staging tiles of their own, so the stage is released
 // as soon as dK, the last MMA reading it, is done.  One TMA stage (Q, dO, K, V); the next chunk's tiles
 // are prefetched into L2 meanwhile.
 // ----------------------------------------------------------------------------------------------------

@@ -1,4 +1,5 @@
-// la_tc_fwd.cu -- tcgen05 / TMA kernels of the bf16 path (D = 128): per-piece state sums and the forward.
+// la_tc_fwd.cu -- tcgen05 / TMA kernels of the bf16 path (kernels on 128 columns; D = 32, 64 zero-extended by the
+// tensor maps): per-piece state sums and the forward.
 //
 // Method ("Transformer Based Linear Attention with Optimized GPU Kernel Implementation", sciencestack.ai
 // page, TL;DR: O(N D^2) time, O(N D) memory, normalisation scheme), per head, rows i, chunk c of kC rows:

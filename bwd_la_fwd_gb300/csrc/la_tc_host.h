@@ -92,7 +92,8 @@ cudaError_t launch_tc(void (*kernel)(const tc::TcParams), dim3 grid, unsigned bl
 cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cudaStream_t s);
 }  // namespace tc_host
 
-// bf16 storage and D = 128: the tcgen05 kernels; everything else takes the SIMT path.
+// bf16 storage with D = 32, 64 or 128: the tcgen05 kernels (on 128 columns, narrower heads zero-extended by
+// the tensor maps); everything else takes the SIMT path.
 bool tc_supported(const Plan &p);
 // Workspace bytes the tensor-core path needs for its state slots (one direction).
 size_t tc_slot_bytes(const Plan &p);

@@ -11,7 +11,7 @@ causal mask, or a transposed operand (q_j . k_i).
   * central finite differences of L for every entry of Q, K, V (the "analytical gradients");
   * invariants: rows of the normalised weights sum to one; causal outputs ignore future tokens;
     shifting V by a constant row shifts O by it; O is linear in V;
-  * closed forms: K = 0 or Q = 0 gives (prefix) means of V, N = 1 gives O = V, c = 0 with D = 1
+  * closed forms: K = 0 or Q = 0 gives (prefix) means of V, N = 1 gives O = V, dQ = dK = 0, dV = dO, c = 0 with D = 1
     gives a q-independent ratio, and the matching gradients;
   * the recurrent (decode) form: token by token it reproduces the hand-worked causal values and the
     explicit causal rows, and a block append followed by decoding continues the forward.
@@ -72,16 +72,19 @@ def test_golden_d1_worked_example(oracle_lib, causal, form):
 
 # ---------------------------------------------------------------------- explicit vs prefix ---
 
+@pytest.mark.parametrize("c", [1.0, 2.0])
 @pytest.mark.parametrize("causal", [1, 0])
 @pytest.mark.parametrize("shape", [(1, 2, 64, 16), (1, 1, 1, 4), (2, 1, 7, 3), (1, 3, 33, 8), (1, 1, 40, 1)])
-def test_explicit_matches_prefix_form(oracle_lib, causal, shape):
+def test_explicit_matches_prefix_form(oracle_lib, causal, shape, c):
+    """Both forms at the library's c = 1 and at c = 2, so that every place c enters either form (the
+    weights, the normaliser, the a and e terms of O and dV) is compared."""
     B, H, N, D = shape
     x = _tiny(seed=11 + N, B=B, H=H, N=N, D=D)
-    O, g = oracle_lib.forward(x["Q"], x["K"], x["V"], causal)
-    Op, gp = oracle_lib.prefix_forward(x["Q"], x["K"], x["V"], causal)
+    O, g = oracle_lib.forward(x["Q"], x["K"], x["V"], causal, c=c)
+    Op, gp = oracle_lib.prefix_forward(x["Q"], x["K"], x["V"], causal, c=c)
     assert _rel(O, Op) < 1e-12 and _rel(g, gp) < 1e-12
-    gr = oracle_lib.backward(x["Q"], x["K"], x["V"], x["dO"], causal)
-    grp = oracle_lib.prefix_backward(x["Q"], x["K"], x["V"], x["dO"], causal)
+    gr = oracle_lib.backward(x["Q"], x["K"], x["V"], x["dO"], causal, c=c)
+    grp = oracle_lib.prefix_backward(x["Q"], x["K"], x["V"], x["dO"], causal, c=c)
     for a, b in zip(gr, grp):
         assert _rel(a, b) < 1e-12
 
@@ -202,6 +205,16 @@ def test_single_token_returns_v(oracle_lib):
         O, g = oracle_lib.forward(x["Q"], x["K"], x["V"], causal)
         assert np.max(np.abs(O - x["V"])) < 1e-15
         assert np.max(np.abs(g - (1.0 + np.sum(x["Q"] * x["K"], axis=-1)))) < 1e-15
+
+
+def test_single_token_gradients(oracle_lib):
+    """N = 1: O_0 = v_0, so delta_0 = dO_0 . v_0 and dW_00 = (dO_0 . v_0 - delta_0) / g_0 = 0: dQ = dK = 0,
+    and dV_0 = (W_00 / g_0) dO_0 = dO_0.  A sign error in the delta term would leave dW_00 = 2 dO.v / g."""
+    x = _tiny(seed=8, N=1)
+    for causal in (0, 1):
+        dQ, dK, dV = oracle_lib.backward(x["Q"], x["K"], x["V"], x["dO"], causal)
+        assert np.max(np.abs(dQ)) < 1e-14 and np.max(np.abs(dK)) < 1e-14
+        assert np.max(np.abs(dV - x["dO"])) < 1e-14
 
 
 def test_equal_keys_noncausal_give_mean(oracle_lib):

@@ -32,7 +32,7 @@ struct Slices {
 __host__ __device__ __forceinline__ long long slice_lo(const Slices &s, int b) { return (long long)b * s.T / s.G; }
 
 // The CTA whose slice contains flat chunk x: the largest b with floor(b T / G) <= x, i.e. b T < (x + 1) G.
-__device__ __forceinline__ int cta_of(const Slices &s, long long x) {
+__host__ __device__ __forceinline__ int cta_of(const Slices &s, long long x) {
     const long long b = ((x + 1) * s.G - 1) / s.T;
     return (int)(b < s.G - 1 ? b : s.G - 1);
 }
@@ -60,10 +60,10 @@ struct Piece {
 struct PieceIter {
     long long x, hi;
     int nchunk;
-    __device__ __forceinline__ PieceIter(const Slices &s, int b)
+    __host__ __device__ __forceinline__ PieceIter(const Slices &s, int b)
         : x(slice_lo(s, b)), hi(slice_lo(s, b + 1)), nchunk(s.nchunk) {}
-    __device__ __forceinline__ bool valid() const { return x < hi; }
-    __device__ __forceinline__ Piece get() const {
+    __host__ __device__ __forceinline__ bool valid() const { return x < hi; }
+    __host__ __device__ __forceinline__ Piece get() const {
         Piece p;
         p.h = x / nchunk;
         p.a = (int)(x - p.h * nchunk);
@@ -71,7 +71,7 @@ struct PieceIter {
         p.e = (int)((hi < hend ? hi : hend) - p.h * nchunk);
         return p;
     }
-    __device__ __forceinline__ void next() {
+    __host__ __device__ __forceinline__ void next() {
         const Piece p = get();
         x = p.h * nchunk + p.e;
     }

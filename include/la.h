@@ -53,7 +53,7 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (e.g. an unsupported D) */
     LA_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than la_workspace_bytes() */
     LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-    LA_ERR_TIMEOUT = 5,     /* device: a bounded inter-block wait gave up (reported by la_get_status) */
+    LA_ERR_TIMEOUT = 5,     /* device: a bounded barrier wait inside a kernel gave up (reported by la_get_status) */
     LA_ERR_BOUNDS = 6,      /* device: an internal index check failed (reported by la_get_status) */
     LA_ERR_STATE = 7        /* device: la_backward_with_forward_state found no matching forward state */
 } la_status;

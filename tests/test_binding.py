@@ -43,3 +43,31 @@ def test_decode_state_checks():
     K = torch.empty(1, 2, 5, 64, dtype=torch.float32)
     with pytest.raises(ValueError, match="match"):
         la.la_state_append(st, K, K)
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """Without the compiled CUDA library every entry raises: there is no CPU or torch fallback."""
+    import torch
+    from bwd_la_fwd_gb300 import la
+    monkeypatch.setattr(la, "_lib", None)
+    monkeypatch.setattr(la, "library_path", lambda: "/nonexistent/liblagb300.so")
+    Q = torch.empty(1, 2, 8, 64, dtype=torch.bfloat16)
+    for call in (lambda: la.la_forward(Q, Q, Q, True),
+                 lambda: la.la_backward(Q, Q, Q, Q, Q, True),
+                 lambda: la.la_workspace_bytes(1, 2, 8, 64, True, la.LA_BF16, True),
+                 lambda: la.la_launch_count()):
+        with pytest.raises(RuntimeError, match="no CPU fallback"):
+            call()
+
+
+def test_product_package_never_imports_the_oracle():
+    """The oracle is test infrastructure: no module of the product package imports or loads it."""
+    import os
+    import re
+    pkg = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bwd_la_fwd_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle\b)|liblaoracle", re.M)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                with open(os.path.join(root, f), encoding="utf-8") as fh:
+                    assert not pat.search(fh.read()), f

@@ -651,7 +651,7 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     P.sl.G = (int)G;
     P.N = p.N;
     P.H = p.H;
-    uint64_t hsh = 0xcbf29ce484222325ull;  // FNV-1a over K's and V's strides
+    uint64_t hsh = 0xcbf29ce484222325ull;  // FNV-1a over K's and V's strides, then D
     for (int op : {kOpK, kOpV})
         for (long long v : {p.lay[op].sb, p.lay[op].sh, p.lay[op].sn}) hsh = (hsh ^ (uint64_t)v) * 0x100000001b3ull;
     P.kv_layout = (hsh ^ (uint64_t)p.D) * 0x100000001b3ull;

@@ -21,7 +21,7 @@ struct TcParams {
     int flat;               // the maps are 3-D over {D, N, B H} (kernels <FLAT = true>), else 4-D over {D, N, H, B}
     int nbox;               // 64-column boxes holding the operands' D columns: 2 for D = 128, 1 for D = 32, 64
                             // (the kernels compute with D = 128; columns past D load as zero and are not stored)
-    uint64_t kv_layout;     // hash of K's and V's strides (part of the per-piece sums' identity)
+    uint64_t kv_layout;     // hash of K's and V's strides and of D (part of the per-piece sums' identity)
     long long N;
     float *slots;           // per-piece state sums, slot stride `slot_stride` floats
     float *slots_rev;       // backward: per-piece reverse-direction sums
@@ -51,7 +51,7 @@ constexpr size_t kTagOffset = 128;  // bytes into the workspace header
 static_assert(kTagOffset == offsetof(WsHeader, state_tag), "tag offset");
 constexpr int kTagWords = 7;
 __host__ __device__ inline void state_tag(const TcParams &P, uint64_t form, uint64_t *t) {
-    t[0] = 0x4C415F5354415445ull ^ P.kv_layout;  // marker ("LA_STATE"), folded with K's and V's strides
+    t[0] = 0x4C415F5354415445ull ^ P.kv_layout;  // marker ("LA_STATE"), folded with K's and V's strides and D
     t[1] = (uint64_t)(uintptr_t)P.Kp;
     t[2] = (uint64_t)(uintptr_t)P.Vp;
     t[3] = (uint64_t)P.sl.T;

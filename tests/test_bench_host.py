@@ -1,4 +1,5 @@
-"""bench.py's host arithmetic on CPU (no GPU): the roofline of a shape and the algorithmic figures the
+"""bench.py's host logic on CPU (no GPU): the clock and throttle summary of the timed window, and the
+roofline of a shape and the algorithmic figures the
 JSON line reports, against the roofline table worked out from the method's stated costs (forward: Q, K,
 V read, O and the fp32 normaliser written, 4 D^2 flops per row; backward: eight tensor volumes, 10 D^2
 flops per row) with a 6776.3 GB/s copy and a 1912.5 TFLOP/s bf16 rate: 39.8 us forward, 79.2 us
@@ -45,3 +46,32 @@ def test_sweep_cases_are_the_measured_workloads():
     assert names == ["head_size_D32", "head_size_D64", "head_size_D256", "seq_len_N1024", "seq_len_N2048",
                      "seq_len_N8192", "seq_len_N16384", "seq_len_N32768", "seq_len_N65536", "decoder_24_layers"]
     assert bench.SWEEP_CASES[-1][1:] == (8, 16, 2048, 128, 24, 4)
+
+
+def _row(sm, mx, pw, active, hw="Not Active", hwt="Not Active", swt="Not Active", cap="Not Active"):
+    return ["0", str(sm), str(mx), str(pw), active, hw, hwt, swt, cap]
+
+
+def test_clock_summary_takes_the_window_median_and_active_reasons():
+    s = bench.ClockSampler(0)
+    s.samples = [(0.5, _row(1200, 2070, 300, "0x0")),            # before the window: ignored
+                 (1.0, _row(2070, 2070, 700, "0x0")),
+                 (1.2, _row(2040, 2070, 720, "0x4", cap="Active")),
+                 (1.4, _row(2070, 2070, 710, "0x0")),
+                 (9.0, _row(120, 2070, 90, "0x0", hwt="Active"))]  # after the window: ignored
+    out = bench.ClockSampler.summary(s, 1.0, 2.0)
+    assert out["samples"] == 3
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w_max"] == 720
+
+
+def test_clock_summary_reports_thermal_and_hardware_slowdowns():
+    s = bench.ClockSampler(0)
+    s.samples = [(1.0, _row(1500, 2070, 900, "0x40", hw="Active")),
+                 (1.1, _row(1400, 2070, 900, "0x20", swt="Active")),
+                 (1.2, _row("[N/A]", 2070, "[N/A]", "0x0", hwt="Active"))]
+    out = bench.ClockSampler.summary(s, 0.0, 2.0)
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert out["sm_mhz"] == 1450  # unreadable samples are skipped
+    assert bench.ClockSampler.summary(bench.ClockSampler(0), 0.0, 1.0)["samples"] == 0

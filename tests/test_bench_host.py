@@ -1,9 +1,13 @@
-"""bench.py's host logic on CPU (no GPU): the clock and throttle summary of the timed window, and the
-roofline of a shape and the algorithmic figures the
-JSON line reports, against the roofline table worked out from the method's stated costs (forward: Q, K,
-V read, O and the fp32 normaliser written, 4 D^2 flops per row; backward: eight tensor volumes, 10 D^2
-flops per row) with a 6776.3 GB/s copy and a 1912.5 TFLOP/s bf16 rate: 39.8 us forward, 79.2 us
-backward at B = 4, H = 16, N = 4096, D = 128, every call HBM-bound."""
+"""bench.py's host logic on CPU (no GPU).
+
+* The clock and throttle summary of the timed window.
+* The roofline of a shape and the algorithmic figures the JSON line reports.  They are checked against
+  the roofline table worked out from the method's stated costs, with a 6776.3 GB/s copy and a
+  1912.5 TFLOP/s bf16 rate: 39.8 us forward and 79.2 us backward at B = 4, H = 16, N = 4096, D = 128,
+  every call HBM-bound.
+  * Forward: Q, K, V read, O and the fp32 normaliser written; 4 D^2 flops per row.
+  * Backward: eight tensor volumes; 10 D^2 flops per row.
+"""
 import os
 import sys
 

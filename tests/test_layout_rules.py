@@ -1,4 +1,4 @@
-"""The strided entry points' host-side layout rules against brute force, on CPU.
+"""The host-side memory rules of the strided and the decode entry points against brute force, on CPU.
 
 `la_forward_strided` takes (batch, head, row) element strides per operand; the D elements of a row are
 contiguous.  Its contract (include/la.h):
@@ -6,7 +6,10 @@ contiguous.  Its contract (include/la.h):
     nest, and every stride is a multiple of 16 bytes; rows that do overlap are always refused;
   * the output may not meet an input: with equal strides the two are compared element by element (so
     interleaved slices of one fused tensor pass), otherwise by address range.
-Each case below is a random small layout (seeded) whose element sets are enumerated in Python.  The call
+`la_decode_step` / `la_state_append`: the state arrays (S, z, a, n) meet neither each other nor a token
+or output buffer; the outputs meet no token input and not each other; token inputs may share memory.
+Each case below is a random small layout (seeded) whose element sets or address ranges are enumerated in
+Python.  The call
 returns LA_ERR_INVALID_ARG (1) when refused.  An accepted call reaches its first CUDA call, which fails
 here with LA_ERR_CUDA (4): there is no device, so nothing runs.  These tests are skipped wherever a CUDA
 device is present, so that no accepted call with made-up pointers can ever launch work.
@@ -160,3 +163,62 @@ def test_output_against_input_with_other_strides_compares_ranges(lib, dtype):
         assert rc == (1 if ranges_meet else 4), (ext, D, sq, so, o_base - q_base)
         seen[rc] += 1
     assert seen[1] > 20 and seen[4] > 20
+
+
+# ------------------------------------------------------------------ decode state and tokens ---
+
+def _decode_buffers(rng, B, H, D, dtype, arena_units):
+    """Random 16-byte-aligned placements (bytes from the arena) of q, k, v, o, g, S, z, a, n."""
+    tok = B * H * D * (2 if dtype == 1 else 4)
+    acc = 4 if dtype == 1 else 8
+    sizes = {"q": tok, "k": tok, "v": tok, "o": tok, "g": B * H * 4,
+             "S": B * H * D * D * acc, "z": B * H * D * acc, "a": B * H * D * acc, "n": B * H * 4}
+    place = {name: 16 * rng.randrange(0, arena_units) for name in sizes}
+    return place, sizes
+
+
+def _meet(place, sizes, x, y):
+    return place[x] < place[y] + sizes[y] and place[y] < place[x] + sizes[x]
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_decode_step_refuses_exactly_the_forbidden_overlaps(lib, dtype):
+    """The state arrays meet neither each other nor a token or output buffer; o and g meet no token input
+    and not each other; the token inputs q, k, v may share memory."""
+    rng = random.Random(4000 + dtype)
+    vp = ctypes.c_void_p
+    seen = {1: 0, 4: 0}
+    state = ("S", "z", "a", "n")
+    for _ in range(600):
+        B, H, D = rng.randrange(1, 3), rng.randrange(1, 3), rng.choice([16, 32])
+        place, sizes = _decode_buffers(rng, B, H, D, dtype, arena_units=rng.choice([64, 512, 4096, 1 << 16]))
+        bad = any(_meet(place, sizes, s, t) for i, s in enumerate(state) for t in state[i + 1:])
+        bad |= any(_meet(place, sizes, s, t) for s in state for t in ("q", "k", "v", "o", "g"))
+        bad |= any(_meet(place, sizes, "o", t) for t in ("q", "k", "v"))
+        bad |= any(_meet(place, sizes, "g", t) for t in ("q", "k", "v", "o"))
+        p = {name: vp(ARENA + off) for name, off in place.items()}
+        rc = lib.la_decode_step(p["q"], p["k"], p["v"], p["o"], p["g"], p["S"], p["z"], p["a"], p["n"],
+                                B, H, D, dtype, vp(0))
+        assert rc == (1 if bad else 4), (B, H, D, place)
+        seen[rc] += 1
+    assert seen[1] > 50 and seen[4] > 50
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_state_append_refuses_exactly_the_forbidden_overlaps(lib, dtype):
+    """The state arrays meet neither each other nor the appended K, V (which may share memory)."""
+    rng = random.Random(5000 + dtype)
+    vp = ctypes.c_void_p
+    seen = {1: 0, 4: 0}
+    state = ("S", "z", "a", "n")
+    for _ in range(600):
+        B, H, D, N = rng.randrange(1, 3), rng.randrange(1, 3), rng.choice([16, 32]), rng.randrange(1, 6)
+        place, sizes = _decode_buffers(rng, B, H, D, dtype, arena_units=rng.choice([64, 512, 4096, 1 << 16]))
+        sizes["k"] = sizes["v"] = B * H * N * D * (2 if dtype == 1 else 4)
+        bad = any(_meet(place, sizes, s, t) for i, s in enumerate(state) for t in state[i + 1:])
+        bad |= any(_meet(place, sizes, s, t) for s in state for t in ("k", "v"))
+        p = {name: vp(ARENA + off) for name, off in place.items()}
+        rc = lib.la_state_append(p["k"], p["v"], p["S"], p["z"], p["a"], p["n"], B, H, N, D, dtype, vp(0))
+        assert rc == (1 if bad else 4), (B, H, D, N, place)
+        seen[rc] += 1
+    assert seen[1] > 50 and seen[4] > 50

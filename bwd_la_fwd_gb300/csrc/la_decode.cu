@@ -63,8 +63,8 @@ template <typename Acc, int D> struct DecSplit {
 // One decode step.  grid = BH * R CTAs in clusters of R (one cluster per head).  CTA r bulk-copies rows
 // [r ROWS, (r + 1) ROWS) of the head's S into shared memory (one TMA transfer), updates them there
 // (S += k v^T), forms its partial column sums of S^T q, and bulk-copies the rows back; rank 0 adds the
-// R partials through distributed shared memory and writes o, g, z, a and n.  A copy that does not land
-// within the bounded wait leaves the state untouched and writes NaN to o.
+// R partials through distributed shared memory and writes o, g, z, a and n.  If any CTA's copy does not
+// land within the bounded wait, no CTA of the cluster changes the head's state and o is written as NaN.
 template <typename T, typename Acc, int D>
 __global__ void __launch_bounds__(kThreads) decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                                                                const T *__restrict__ v, T *__restrict__ o,
@@ -96,7 +96,14 @@ __global__ void __launch_bounds__(kThreads) decode_step_kernel(const T *__restri
     }
     if (t == 0) landed = sm100::mbar_wait(&bar, 0, 2000000000ull) ? 1 : 0;
     __syncthreads();  // q, k in shared memory; the slab has landed (or the wait gave up)
-    const bool ok = landed != 0;
+    bool ok = landed != 0;
+    if constexpr (C::R > 1) {
+        // the cluster updates the head's state only if every CTA's slab landed: one CTA's rows of S must not
+        // advance while another's, or z, a and n, stay behind
+        cluster.sync();
+#pragma unroll
+        for (int r = 0; r < C::R; ++r) ok = ok && *cluster.map_shared_rank(&landed, r) != 0;
+    }
     const int cgi = t % C::CG, p = t / C::CG;
     if (ok && p < C::RG) {
         Acc ve[C::VEC], acc[C::VEC];
@@ -232,13 +239,12 @@ cudaError_t launch_step(const void *q, const void *k, const void *v, void *o, fl
                         int *n, long long BH, cudaStream_t s) {
     using C = DecSplit<Acc, D>;
     constexpr int R = C::R;
-    static int attr_set = 0;  // the slab can exceed the 48 KB default window
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute(decode_step_kernel<T, Acc, D>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = 1;
-    }
+    static std::atomic<int> attr_state[kMaxDevices];  // the slab can exceed the 48 KB default window
+    if (!once_per_device(attr_state, [] {
+            return cudaFuncSetAttribute(decode_step_kernel<T, Acc, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)C::BYTES) == cudaSuccess;
+        }))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(BH * R));
     cfg.blockDim = dim3(kThreads);

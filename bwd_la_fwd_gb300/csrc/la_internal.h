@@ -5,7 +5,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace la {
+
+constexpr int kMaxDevices = 64;
+
+// Runs `set` once for the current device and remembers how it ended (state[dev]: 0 not yet, 1 done,
+// -1 failed).  Function attributes such as the dynamic shared-memory limit belong to the current
+// device's context, so a process that uses several devices sets them on each.  Two threads that race on
+// a device's first call both run `set`, which only repeats an idempotent setting.
+template <typename F> bool once_per_device(std::atomic<int> *state, F set) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    int s = state[dev].load(std::memory_order_acquire);
+    if (s == 0) {
+        s = set() ? 1 : -1;
+        state[dev].store(s, std::memory_order_release);
+    }
+    return s > 0;
+}
 
 // Device status codes written into the workspace's sticky status word (same values as la_status).
 enum : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBounds = 6, kDevState = 7 };

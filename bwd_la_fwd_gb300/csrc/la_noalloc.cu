@@ -6,9 +6,11 @@
 // memory budget is fixed when it loads.  For them this entry point runs the same forward kernels with a
 // workspace that lives in a fixed device array compiled into the library, so it allocates nothing.
 //
-// The first call on each device looks the array's device address up (cudaGetSymbolAddress); make that
-// first call before any stream capture begins.  Every call on a device shares the one array, so calls
-// whose work overlaps on the GPU (different streams, or different host threads) race with each other.
+// The first call on each device looks the array's device address up (cudaGetSymbolAddress) and clears the
+// array's status header (cudaMemset, then a wait for it); make that first call before any stream capture
+// begins.  Every call on a device shares the one array, so calls whose work overlaps on the GPU (different
+// streams, or different host threads) race with each other.  Device-side conditions (a bounded wait that
+// ran out) are recorded in the array's sticky status word, which la_noalloc_get_status reads and clears.
 //
 // The array below has static storage: every device on which this part of the library is loaded keeps
 // LA_NOALLOC_SCRATCH_BYTES reserved until the process exits.  In host code its name is only a host-side
@@ -29,14 +31,18 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void *g_scratch_ptr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (looked up on first use per device).
-int scratch_for_current_device(void **out) {
+// Device address of the scratch array on the current device, looked up (and its header cleared) on the
+// first use per device.  `create` false: report nullptr when the device has not been set up yet.
+int scratch_for_current_device(void **out, bool create) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] && create) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LA_ERR_CUDA;
+        // the header (status word, state record) must start at zero; the forward writes everything else
+        // it reads within the same call
+        if (cudaMemset(p, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
         g_scratch_ptr[dev] = p;
     }
     *out = g_scratch_ptr[dev];
@@ -54,10 +60,18 @@ extern "C" int la_forward_noalloc(const void *Q, const void *K, const void *V, i
     }
     if (need > (size_t)LA_NOALLOC_SCRATCH_BYTES) return LA_ERR_WORKSPACE;  // beyond the fixed scratch size
     void *ws = nullptr;
-    int rc = scratch_for_current_device(&ws);
+    const int rc = scratch_for_current_device(&ws, true);
     if (rc != LA_OK) return rc;
-    // The scratch keeps whatever the previous call left in it.  Everything the forward reads is written
-    // earlier in the same call except the status header, which must start at zero: clear it on the stream.
-    if (cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
+    // la_forward checks every argument on the host before it enqueues anything
     return la_forward(Q, K, V, causal, O, normaliser, B, H, N, D, dtype, ws, LA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int la_noalloc_get_status(void *stream) {
+    void *ws = nullptr;
+    const int rc = scratch_for_current_device(&ws, false);
+    if (rc != LA_OK) return rc;
+    if (!ws) {  // no call has used this device's scratch yet
+        return cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    }
+    return la_get_status(ws, stream);
 }

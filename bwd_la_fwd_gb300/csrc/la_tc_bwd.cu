@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barU = bar + 4, *barDt = bar + 5,
              *barX = bar + 6, *barR = bar + 7, *barPPf = bar + 8, *barC = bar + 9;
     uint32_t *tslot = (uint32_t *)(bar + 10);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         const uint32_t counts[10] = {1, E, E, 1, E, E, 1, E, E, 1};
         for (int k = 0; k < 10; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
@@ -584,7 +586,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     uint64_t *barYf = barY + 2;    // [2]: the epilogue has read Y out of R0 / R1
     uint64_t *barDt = barYf + 2, *barX = barDt + 1, *barSb = barDt + 2, *barPP = barDt + 3, *barPPf = barDt + 4;
     uint32_t *tslot = (uint32_t *)(barDt + 5);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -603,6 +606,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         mbar_init(barPP, 1);
         mbar_init(barPPf, E);
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     for (int k = threadIdx.x; k < 256; k += blockDim.x) ((uint32_t *)ones)[k] = 0x3F803F80u;
@@ -835,7 +839,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     uint64_t *barO = bar, *barT1 = bar + 1, *barT2 = bar + 2, *barP1 = bar + 3, *barP2 = bar + 4, *barPb = bar + 5,
              *barK = bar + 6, *barV = bar + 7, *barR = bar + 8;
     uint32_t *tslot = (uint32_t *)(bar + 9);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -845,6 +850,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         const uint32_t counts[9] = {E, 1, 1, E, E, E, 1, 1, E};
         for (int k = 0; k < 9; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1106,7 +1112,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
     uint64_t *bar = empty + NST;
     uint64_t *barPb = bar, *barK = bar + 1, *barKf = bar + 2, *barV = bar + 3, *barVf = bar + 4;
     uint32_t *tslot = (uint32_t *)(bar + 5);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1118,6 +1125,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         const uint32_t counts[5] = {E, 1, E, 1, E};
         for (int k = 0; k < 5; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -1285,21 +1293,21 @@ constexpr size_t kSmemDkdvNc = 3 * 2 * kTB + kTB + 2 * 128 * 4 + 512;         //
 static_assert(kSmemDkdvNc <= 232448 && kSmemDkdv <= 232448 && kSmemDq <= 232448 && kSmemDqNc <= 232448, "backward kernel exceeds the shared-memory limit");
 
 bool set_bwd_attrs() {
-    static int done = 0;
-    if (done) return done > 0;
-    const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    bool ok = true;
-    for (int f = 0; f < 2 && ok; ++f)
-        ok = cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, A, (int)kSmemDq) ==
-                 cudaSuccess &&
-             cudaFuncSetAttribute(f ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>, A,
-                                  (int)kSmemDqNc) == cudaSuccess &&
-             cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_kernel<true> : tc::tc_bwd_dkdv_kernel<false>, A,
-                                  (int)kSmemDkdv) == cudaSuccess &&
-             cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_nc_kernel<true> : tc::tc_bwd_dkdv_nc_kernel<false>, A,
-                                  (int)kSmemDkdvNc) == cudaSuccess;
-    done = ok ? 1 : -1;
-    return ok;
+    static std::atomic<int> state[kMaxDevices];
+    return once_per_device(state, [] {
+        const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        bool ok = true;
+        for (int f = 0; f < 2 && ok; ++f)
+            ok = cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, A,
+                                      (int)kSmemDq) == cudaSuccess &&
+                 cudaFuncSetAttribute(f ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>, A,
+                                      (int)kSmemDqNc) == cudaSuccess &&
+                 cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_kernel<true> : tc::tc_bwd_dkdv_kernel<false>, A,
+                                      (int)kSmemDkdv) == cudaSuccess &&
+                 cudaFuncSetAttribute(f ? tc::tc_bwd_dkdv_nc_kernel<true> : tc::tc_bwd_dkdv_nc_kernel<false>, A,
+                                      (int)kSmemDkdvNc) == cudaSuccess;
+        return ok;
+    });
 }
 
 }  // namespace

@@ -82,15 +82,25 @@ __device__ __forceinline__ void report(uint32_t *status, uint32_t code, uint32_t
     if (atomicCAS(status, 0u, code) == 0u) status[1] = where;
 }
 
+// Per-CTA abort state in shared memory: the flag that a role sets when it gives up, and the bound on any
+// single barrier wait of the launch (kWaitNs unless the launch asks for a shorter one).  `flag` is the
+// first member, so the kernels pass a pointer to it and the wait finds the bound beside it.
+struct AbortState {
+    int flag;
+    int pad;
+    uint64_t limit_ns;
+};
+
 // Barrier wait bounded in time and aborted early when another role of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                               uint32_t *status, uint32_t where) {
     if (sm100::mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = reinterpret_cast<volatile AbortState *>(abort_flag)->limit_ns;
     const uint64_t t0 = sm100::globaltimer_ns();
     while (true) {
         if (sm100::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (sm100::globaltimer_ns() - t0 > kWaitNs) {
+        if (sm100::globaltimer_ns() - t0 > limit) {
             *abort_flag = 1;
             report(status, 5u, where);
             return false;

@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     uint64_t *zafull = accfree + 2;  // [2] the chunk's z_c, a_c are in TMEM block it & 1
     uint64_t *zafree = zafull + 2;   // [2] the epilogue has read them
     uint32_t *tslot = (uint32_t *)(zafree + 2);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
             mbar_init(&zafree[b], 128);
         }
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     for (int i = threadIdx.x; i < 512; i += blockDim.x) ((uint32_t *)ones)[i] = 0x3F803F80u;
@@ -89,6 +91,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
         // ---- TMA producer
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
+        const int drop = blockIdx.x == 0 ? P.test_drop_load : -1;  // test hook (normally -1)
         int it = 0;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && !*abort_flag; pi.next()) {
             const Piece pc = pi.get();
@@ -97,6 +100,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x101))
                     break;
+                if (it == drop) continue;  // nothing issued: the MMA issuer's wait for this stage runs out
                 mbar_arrive_expect_tx(&full[s], STAGE);
                 unsigned char *st = stages + s * STAGE;
                 for (int nb = 0; nb < NB; ++nb) {
@@ -104,6 +108,10 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                     tile_load<FLAT>(st + (NB + nb) * kBox, &P.tmV, &full[s], nb * 64, c * kC, hc);
                 }
             }
+        }
+        if (*abort_flag) {  // let the copies already issued land before the CTA exits
+            for (int k = it > NST ? it - NST : 0; k < it; ++k)
+                if (k != drop) mbar_wait(&full[k % NST], (k / NST) & 1, 50000000ull);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
@@ -235,7 +243,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     uint64_t *barO = barS + 1;    // [2]
     uint64_t *barOf = barO + 2;   // [2] non-causal: accumulator drained
     uint32_t *tslot = (uint32_t *)(barOf + 2);
-    volatile int *abort_flag = (volatile int *)(tslot + 1);
+    AbortState *abst = (AbortState *)(tslot + 2);
+    volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -253,6 +262,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
             mbar_init(&barOf[b], kEpiThreads);
         }
         *abort_flag = 0;
+        abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -581,15 +591,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[kMaxDevices];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!cached[dev]) {
-        int n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (!n) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 // Operand `op` as a bf16 map with boxes of 128 rows x 64 columns of one head, 128-byte swizzle; rows
@@ -623,17 +633,16 @@ constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::
 static_assert(kSmemFwdCausal <= 232448, "forward kernel exceeds the shared-memory limit");
 
 bool set_smem_attrs() {
-    static int done = 0;
-    if (done) return done > 0;
-    const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    bool ok = cudaFuncSetAttribute(tc::tc_agg_kernel<true>, A, (int)kSmemAgg) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_agg_kernel<false>, A, (int)kSmemAgg) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<true, true>, A, (int)kSmemFwdCausal) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<false, true>, A, (int)kSmemFwdNonCausal) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<true, false>, A, (int)kSmemFwdCausal) == cudaSuccess &&
-              cudaFuncSetAttribute(tc::tc_fwd_kernel<false, false>, A, (int)kSmemFwdNonCausal) == cudaSuccess;
-    done = ok ? 1 : -1;
-    return ok;
+    static std::atomic<int> state[kMaxDevices];
+    return once_per_device(state, [] {
+        const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
+        return cudaFuncSetAttribute(tc::tc_agg_kernel<true>, A, (int)kSmemAgg) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::tc_agg_kernel<false>, A, (int)kSmemAgg) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::tc_fwd_kernel<true, true>, A, (int)kSmemFwdCausal) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::tc_fwd_kernel<false, true>, A, (int)kSmemFwdNonCausal) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::tc_fwd_kernel<true, false>, A, (int)kSmemFwdCausal) == cudaSuccess &&
+               cudaFuncSetAttribute(tc::tc_fwd_kernel<false, false>, A, (int)kSmemFwdNonCausal) == cudaSuccess;
+    });
 }
 
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
@@ -649,6 +658,18 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
         if (cap >= 1 && cap < G) G = cap;
     }
     P.sl.G = (int)G;
+    // Test hooks for the failure path: a shorter bound on barrier waits, and one load of the sums kernel
+    // that is never issued, so that a wait runs out and the kernels take their abort path.
+    P.wait_ns = 0;
+    if (const char *env = getenv("LA_TEST_WAIT_NS")) {
+        const long long ns = atoll(env);
+        if (ns >= 1000000) P.wait_ns = (uint64_t)ns;
+    }
+    P.test_drop_load = -1;
+    if (const char *env = getenv("LA_TEST_DROP_LOAD")) {
+        const long long it = atoll(env);
+        if (it >= 0 && it < (1LL << 30)) P.test_drop_load = (int)it;
+    }
     P.N = p.N;
     P.H = p.H;
     uint64_t hsh = 0xcbf29ce484222325ull;  // FNV-1a over K's and V's strides, then D

@@ -38,6 +38,8 @@ struct TcParams {
     float *combine_slots;   // tc_combine_kernel: the slot array it turns into carries
     int combine_mode;       // tc_combine_kernel: kCombinePrefix, kCombineSuffix or kCombineTotal
     int combine_tag;        // tc_combine_kernel: also record the new form in the workspace tag
+    uint64_t wait_ns;       // bound on a single barrier wait (0: the default, tc::kWaitNs)
+    int test_drop_load;     // test hook: CTA 0 of the sums kernel issues no load for this iteration (-1: none)
 };
 
 // Forms of the slot arrays (tc_combine_kernel).

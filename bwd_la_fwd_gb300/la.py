@@ -69,6 +69,10 @@ def load_library():
         lib.la_state_append.restype = i
         lib.la_get_status.argtypes = [vp, vp]
         lib.la_get_status.restype = i
+        lib.la_forward_noalloc.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp]
+        lib.la_forward_noalloc.restype = i
+        lib.la_noalloc_get_status.argtypes = [vp]
+        lib.la_noalloc_get_status.restype = i
         _lib = lib
         return lib
 
@@ -191,6 +195,28 @@ def la_backward(Q, K, V, O, dO, causal: bool, dQ=None, dK=None, dV=None, workspa
 def la_get_status(workspace, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status recorded in the workspace."""
     return int(load_library().la_get_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def la_forward_noalloc(Q, K, V, causal: bool, O=None, normaliser=None, stream=None):
+    """The forward without a workspace argument: the library's fixed scratch array on the current device
+    serves instead (for callers that cannot allocate device memory).  Returns (O, normaliser)."""
+    import torch
+    B, H, N, D = _shape(Q)
+    _check_like(Q, K, V)
+    if O is None:
+        O = torch.empty_like(Q)
+    if normaliser is None:
+        normaliser = torch.empty((B, H, N), device=Q.device, dtype=torch.float32)
+    st = load_library().la_forward_noalloc(_ptr(Q), _ptr(K), _ptr(V), int(bool(causal)), _ptr(O), _ptr(normaliser),
+                                           B, H, N, D, _dtype_code(Q), _stream_ptr(stream))
+    if st != 0:
+        raise LAError(st, "la_forward_noalloc")
+    return O, normaliser
+
+
+def la_noalloc_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status of the fixed scratch array."""
+    return int(load_library().la_noalloc_get_status(_stream_ptr(stream)))
 
 
 class DecodeState:

@@ -35,8 +35,9 @@
  *
  * Errors.  Every entry point returns an la_status.  Argument errors are found on the host before any
  * work is enqueued (nothing is launched).  A launch failure returns LA_ERR_CUDA.  Conditions found on
- * the device (a bounded wait that ran out, an index check) are recorded in a sticky status word inside
- * the workspace and reported by la_get_status().  Nothing is thrown across the ABI.
+ * the device (a bounded wait that ran out, a misaligned shared-memory window, a backward that found no
+ * matching forward state) are recorded in a sticky status word inside the workspace and reported by
+ * la_get_status().  Nothing is thrown across the ABI.
  */
 #ifndef LA_GB300_H
 #define LA_GB300_H
@@ -54,7 +55,8 @@ typedef enum {
     LA_ERR_WORKSPACE = 3,   /* workspace null, misaligned or smaller than la_workspace_bytes() */
     LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     LA_ERR_TIMEOUT = 5,     /* device: a bounded barrier wait inside a kernel gave up (reported by la_get_status) */
-    LA_ERR_BOUNDS = 6,      /* device: an internal index check failed (reported by la_get_status) */
+    LA_ERR_BOUNDS = 6,      /* device: an internal layout check failed -- a kernel's shared-memory window was not
+                               1024-byte aligned, so it computed nothing (reported by la_get_status) */
     LA_ERR_STATE = 7        /* device: la_backward_with_forward_state found no matching forward state */
 } la_status;
 
@@ -153,14 +155,24 @@ int la_backward_strided(const void *Q, const void *K, const void *V, const void 
  * is a fixed device array of LA_NOALLOC_SCRATCH_BYTES inside the library, held on every device that loads
  * it until the process exits.  Nothing is allocated.
  *   - Returns LA_ERR_WORKSPACE, before enqueuing anything, when la_workspace_bytes(B, H, N, D, causal,
- *     dtype, 0) exceeds LA_NOALLOC_SCRATCH_BYTES.
- *   - The first call on a device looks up the array's device address; make it before any stream capture.
- *   - Each call clears the array's status word on `stream`; device-side status is not reported back.
+ *     dtype, 0) exceeds LA_NOALLOC_SCRATCH_BYTES; every other argument error is found on the host before
+ *     anything is enqueued, as for la_forward.
+ *   - The first call on a device looks up the array's device address and clears its status header (a
+ *     cudaMemset and a device synchronisation); make it before any stream capture.
+ *   - Device-side conditions are recorded in the array's sticky status word: la_noalloc_get_status
+ *     reads and clears it.
  *   - All calls on a device share the array: calls whose work overlaps on the GPU race.
  */
 #define LA_NOALLOC_SCRATCH_BYTES (32u << 20)
 int la_forward_noalloc(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B,
                        int H, int N, int D, int dtype, void *stream);
+
+/*
+ * la_get_status for the fixed scratch array of la_forward_noalloc on the current device: synchronises
+ * `stream`, then returns and clears the sticky device status left by earlier la_forward_noalloc calls
+ * (LA_OK when no call has run on this device yet), or LA_ERR_CUDA if the stream failed.
+ */
+int la_noalloc_get_status(void *stream);
 
 /*
  * Recurrent (decode) form of the causal head.  The causal forward carries, per (b, h), the state of the

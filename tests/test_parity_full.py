@@ -1,11 +1,19 @@
 """GPU parity at the full workload sizes, on the launch configuration the benchmark times.
 
+The benchmark times la_forward followed by la_backward_with_forward_state on the forward's workspace (the
+backward takes the forward's per-piece K^T V sums instead of recomputing them).  Every case here runs
+exactly that sequence, then the plain la_backward on the same workspace, and requires the two backward
+results to be bit-identical; the outputs are then checked against the oracle.
+
 The explicit oracle costs O(N^2 D) per head, so at these sizes it checks sampled outputs it can compute
 one row at a time (O_i, g_i, dQ_i cost O(N D) each; dK_j, dV_j cost O((N - j) N D), so they are sampled
-near the end of causal heads).  Whole heads are also checked against the fp64 running-state form (itself
-pinned to the explicit oracle at small sizes).  Sizes: the paper's standalone shape (B=4 H=16 N=4096
-D=128, causal and non-causal), the head-size sweep (D = 32, 64, 256 at N = 4096), the sequence-length
-sweep (N = 1024 ... 65536 at D = 128) and two layers of the 1.4B-class step (B=8 H=16 N=2048 D=128).
+near the end of causal heads).  Whole heads are checked against the fp64 running-state form (itself
+pinned to the explicit oracle at small sizes): every head up to N = 8192, so that every piece of the
+work split -- including pieces that start or end inside an interior head -- is compared, and eight heads
+spread over the batch beyond that (the running-state form of all 64 heads of N = 65536 would take
+minutes of host time).  Sizes: the paper's standalone shape (B=4 H=16 N=4096 D=128, causal and
+non-causal), the head-size sweep (D = 32, 64, 256 at N = 4096), the sequence-length sweep (N = 1024 ...
+65536 at D = 128) and two layers of the 1.4B-class step (B=8 H=16 N=2048 D=128).
 """
 import numpy as np
 import pytest
@@ -25,6 +33,12 @@ def _sample_rows(N):
     return sorted({r for r in base if 0 <= r < N})
 
 
+def _compared_heads(BH, N):
+    if N <= 8192:
+        return list(range(BH))
+    return sorted({0, 1, BH // 4, BH // 2 - 1, BH // 2, 3 * BH // 4 + 1, BH - 2, BH - 1})
+
+
 def _check_full(oracle_lib, B, H, N, D, seed, causal, layer=0, layers=1):
     import torch
     from bwd_la_fwd_gb300 import la
@@ -34,11 +48,19 @@ def _check_full(oracle_lib, B, H, N, D, seed, causal, layer=0, layers=1):
     Q, K, V, dO = (U.to_device(x[n], "bf16") for n in ("Q", "K", "V", "dO"))
     ws = la.new_workspace(B, H, N, D, causal, la.LA_BF16, True)
     O, g = la.la_forward(Q, K, V, causal, workspace=ws)
-    dQ, dK, dV = la.la_backward(Q, K, V, O, dO, causal, workspace=ws)
+    # the benchmark's backward: the forward's state sums reused from the workspace
+    dQ, dK, dV = la.la_backward(Q, K, V, O, dO, causal, workspace=ws, reuse_forward_state=True)
     torch.cuda.synchronize()
     assert la.la_get_status(ws) == 0
+    # the plain backward recomputes those sums: bit-identical results
+    plain = la.la_backward(Q, K, V, O, dO, causal, workspace=ws)
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    for name, a, b in zip(("dQ", "dK", "dV"), (dQ, dK, dV), plain):
+        assert torch.equal(a, b), f"{name}: reused-state backward differs from the plain backward"
+    del plain
     out = {"O": O, "g": g, "dQ": dQ, "dK": dK, "dV": dV}
-    heads = [0, B * H - 1]
+    heads = _compared_heads(B * H, N)
     f = _heads_f64(x, heads, B, H, N, D)
     got = {k: v.reshape(B * H, N, -1)[heads].double().cpu().numpy().reshape(1, len(heads), N, -1)
            for k, v in out.items()}
@@ -50,19 +72,22 @@ def _check_full(oracle_lib, B, H, N, D, seed, causal, layer=0, layers=1):
     for name, ref in (("O", rO), ("g", rg), ("dQ", rdQ), ("dK", rdK), ("dV", rdV)):
         U.assert_close(name, got[name], ref, "bf16")
 
-    # sampled rows against the explicit definition
+    # sampled rows of the first and last compared heads against the explicit definition
+    ends = [0, len(heads) - 1]
+    fe = {k: v[:, ends] for k, v in f.items()}
+    ge = {k: v[:, ends] for k, v in got.items()}
     rows = _sample_rows(N)
-    flat = np.array([h * N + r for h in range(len(heads)) for r in rows])
-    sO, sg = oracle_lib.forward_rows(f["Q"], f["K"], f["V"], causal, flat)
-    sdQ = oracle_lib.dq_rows(f["Q"], f["K"], f["V"], f["dO"], causal, flat)
-    U.assert_close("O", got["O"].reshape(-1, D)[flat], sO, "bf16")
-    U.assert_close("g", got["g"].reshape(-1)[flat], sg, "bf16")
-    U.assert_close("dQ", got["dQ"].reshape(-1, D)[flat], sdQ, "bf16")
+    flat = np.array([k * N + r for k in range(2) for r in rows])
+    sO, sg = oracle_lib.forward_rows(fe["Q"], fe["K"], fe["V"], causal, flat)
+    sdQ = oracle_lib.dq_rows(fe["Q"], fe["K"], fe["V"], fe["dO"], causal, flat)
+    U.assert_close("O", ge["O"].reshape(-1, D)[flat], sO, "bf16")
+    U.assert_close("g", ge["g"].reshape(-1)[flat], sg, "bf16")
+    U.assert_close("dQ", ge["dQ"].reshape(-1, D)[flat], sdQ, "bf16")
     kv_rows = [N - 3, N - 2, N - 1] if causal else [0, N // 2, N - 1]
-    kflat = np.array([h * N + r for h in range(len(heads)) for r in kv_rows if r >= 0])
-    sdK, sdV = oracle_lib.dkdv_rows(f["Q"], f["K"], f["V"], f["dO"], causal, kflat)
-    U.assert_close("dK", got["dK"].reshape(-1, D)[kflat], sdK, "bf16")
-    U.assert_close("dV", got["dV"].reshape(-1, D)[kflat], sdV, "bf16")
+    kflat = np.array([k * N + r for k in range(2) for r in kv_rows if r >= 0])
+    sdK, sdV = oracle_lib.dkdv_rows(fe["Q"], fe["K"], fe["V"], fe["dO"], causal, kflat)
+    U.assert_close("dK", ge["dK"].reshape(-1, D)[kflat], sdK, "bf16")
+    U.assert_close("dV", ge["dV"].reshape(-1, D)[kflat], sdV, "bf16")
 
 
 @pytest.mark.parametrize("causal", [1, 0])

@@ -43,6 +43,7 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     if (BH * p->nseg >= (1LL << 31)) return false;
     p->acc_bytes = dtype == LA_F32 ? 8 : 4;
     p->use_tc = tc_supported(*p);
+    p->use_wide = wide_supported(*p);
     // a state slot holds a D x D matrix and two D-vectors; the tensor-core kernels always work on D = 128
     // (narrower heads are zero-extended), so their slots have that size
     const size_t sd = p->use_tc ? 128 : (size_t)D;
@@ -60,6 +61,15 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
         p->off_chunkye = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
         p->bytes_fwd = p->off_states2;
         p->bytes_bwd = round_up(p->off_chunkye + (size_t)BH * nchunk * 256 * sizeof(float), 256);
+        return true;
+    }
+    if (p->use_wide) {
+        // the forward needs only the header; the backward keeps dO / g (bf16) and the row terms g, dt
+        p->off_states = 256;
+        p->off_rowstats = round_up(p->off_states + (size_t)BH * N * D * 2, 256);
+        p->off_flags = p->off_rowstats;
+        p->bytes_fwd = 256;
+        p->bytes_bwd = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
         return true;
     }
     const size_t states = (size_t)BH * p->nseg * (size_t)p->stride * p->acc_bytes;
@@ -232,9 +242,10 @@ int la_forward_strided(const void *Q, const void *K, const void *V, int causal, 
             if (overlap(g_r, range_of(ins[k], (size_t)span_of(p, p.lay[ops[k]]) * elem))) return LA_ERR_INVALID_ARG;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s)
-                             : clear_state_tag(workspace, s);
-    if (e == cudaSuccess && !p.use_tc) e = la::simt_forward(p, Q, K, V, O, normaliser, (unsigned char *)workspace, s);
+    unsigned char *ws = (unsigned char *)workspace;
+    cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, ws, s) : clear_state_tag(workspace, s);
+    if (e == cudaSuccess && p.use_wide) e = la::wide_forward(p, Q, K, V, O, normaliser, ws, s);
+    else if (e == cudaSuccess && !p.use_tc) e = la::simt_forward(p, Q, K, V, O, normaliser, ws, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
@@ -270,11 +281,11 @@ static int backward_impl(const void *Q, const void *K, const void *V, const void
             if (k != o && operands_meet(p, ptrs[o], p.lay[o], ptrs[k], p.lay[k], elem)) return LA_ERR_INVALID_ARG;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = p.use_tc
-                        ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, (unsigned char *)workspace, s, reuse_fwd_state)
-                        : clear_state_tag(workspace, s);
-    if (e == cudaSuccess && !p.use_tc)
-        e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, (unsigned char *)workspace, s);
+    unsigned char *ws = (unsigned char *)workspace;
+    cudaError_t e = p.use_tc ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, ws, s, reuse_fwd_state)
+                             : clear_state_tag(workspace, s);
+    if (e == cudaSuccess && p.use_wide) e = la::wide_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s);
+    else if (e == cudaSuccess && !p.use_tc) e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

@@ -64,7 +64,8 @@ struct Plan {
     size_t off_chunkza; // tensor-core path: each chunk's column sums z_c = sum k_j, a_c = sum v_j
     size_t bytes_fwd;   // workspace bytes for the forward / for the backward
     size_t bytes_bwd;
-    bool use_tc;        // tcgen05 kernels (bf16) rather than the SIMT kernels
+    bool use_tc;        // tcgen05 kernels for bf16 with D <= 128 rather than the SIMT kernels
+    bool use_wide;      // tcgen05 kernels for bf16 with D = 256
     Layout lay[kNumOps]; // strides of each operand (make_plan: contiguous [B,H,N,D])
 };
 

@@ -82,6 +82,7 @@ __device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
 
 // Host helpers shared by the forward and backward launchers (la_tc_fwd.cu).
 namespace tc_host {
+int sm_count();  // multiprocessors of the current device (cached per device), 0 on error
 bool make_map(CUtensorMap *m, const void *ptr, const Plan &p, int op, bool flat);
 bool flat_heads(const Plan &p, const int *ops, int n);
 bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws);
@@ -105,5 +106,13 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
 // device, LA_ERR_STATE when it does not match) instead of recomputing them.
 cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
                         void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state);
+
+// bf16 with D = 256: the tcgen05 kernels of la_tc_wide.cu (one CTA per head and 128-column output half).
+bool wide_supported(const Plan &p);
+cudaError_t wide_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
+                         unsigned char *ws, cudaStream_t s);
+// Reads O (the forward's output) for dt_i = dO_i . O_i / g_i; the workspace holds g, dt and dO / g.
+cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
+                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s);
 
 }  // namespace la

@@ -20,8 +20,9 @@
  * *_strided entry points take other layouts).  The
  * normaliser is float [B, H, N].  bf16 storage accumulates in fp32, fp32 storage in fp64.  Supported:
  * B, H >= 1 (B*H < 2^31), N >= 1 (B*H*N*D < 2^40), D in {16, 32, 64, 128, 256}.  bf16 with D = 32, 64,
- * 128 runs on the tensor-core kernels (D < 128 zero-extended to 128 columns); fp32 storage and bf16 with
- * D = 16 or 256 run on the CUDA-core (SIMT) kernels.
+ * 128 runs on the tensor-core kernels of 128 columns (D < 128 zero-extended), bf16 with D = 256 on the wide
+ * tensor-core kernels (one CTA per head and 128-column output half); fp32 storage and bf16 with D = 16 run
+ * on the CUDA-core (SIMT) kernels.
  *
  * Memory.  Every pointer is a DEVICE pointer except where stated.  The caller owns every buffer; the
  * library never allocates device or host memory and never synchronises the stream (except
@@ -98,10 +99,11 @@ int la_forward(const void *Q, const void *K, const void *V, int causal, void *O,
  *   dQ, dK, dV      out: [B,H,N,D] of `dtype`, the gradients of L = sum dO . O
  *   causal          in : must match the forward call
  *   workspace       in/out: workspace_bytes >= la_workspace_bytes(..., backward = 1)
- * O must be a valid buffer but is not read: the backward recomputes the normaliser g_i and the row
- * terms delta_i = dO_i . O_i from Q, K and V in its accumulator precision, which is both exact to that
- * precision (the stored O is rounded to `dtype`) and one tensor read fewer.  Pointers must be 16-byte
- * aligned.
+ * For D <= 128, O must be a valid buffer but is not read: the backward recomputes the normaliser g_i and
+ * the row terms delta_i = dO_i . O_i from Q, K and V in its accumulator precision, which is both exact to
+ * that precision (the stored O is rounded to `dtype`) and one tensor read fewer.  For bf16 with D = 256
+ * the backward recomputes g_i and reads O for delta_i, so O must hold la_forward's output for these
+ * inputs.  Pointers must be 16-byte aligned.
  */
 int la_backward(const void *Q, const void *K, const void *V, const void *O, const void *dO, void *dQ, void *dK,
                 void *dV, int causal, int B, int H, int N, int D, int dtype, void *workspace,
@@ -116,8 +118,9 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * have been la_forward or la_backward on the same K and V buffers (same pointers, unchanged contents) and
  * the same B, H, N, D and dtype.  The workspace records which K, V and shape its sums belong to; when the
  * record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.  Unchanged
- * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or D = 16 or 256)
- * there are no such sums to reuse and this call is la_backward.
+ * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or bf16 with
+ * D = 16) and on the wide path (bf16 with D = 256) there are no such sums to reuse and this call is
+ * la_backward.
  */
 int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                                    void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,

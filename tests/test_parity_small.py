@@ -86,12 +86,12 @@ def test_multi_chunk_slices_narrow_heads(oracle_lib, monkeypatch, D, causal):
     _check(oracle_lib, 2, 3, 549, D, "bf16", causal, seed=41 + D)
 
 
-@pytest.mark.parametrize("dtype,D,tc", [("bf16", 16, False), ("bf16", 32, True), ("bf16", 64, True),
-                                        ("bf16", 128, True), ("bf16", 256, False), ("f32", 64, False),
-                                        ("f32", 128, False)])
-def test_path_taken(dtype, D, tc):
-    """bf16 with D = 32, 64, 128 runs on the tensor-core kernels (backward: 5 launches), the rest (bf16 with
-    D = 16 or 256, fp32) on the CUDA-core kernels (backward: 8 launches)."""
+@pytest.mark.parametrize("dtype,D,launches", [("bf16", 16, 8), ("bf16", 32, 5), ("bf16", 64, 5), ("bf16", 128, 5),
+                                              ("bf16", 256, 5), ("f32", 64, 8), ("f32", 128, 8)])
+def test_path_taken(dtype, D, launches):
+    """bf16 with D = 32, 64, 128 runs on the tensor-core kernels of 128 columns (backward: sums, combine, dQ
+    walk, combine, dK/dV walk), bf16 with D = 256 on the wide tensor-core kernels (backward: g, row terms,
+    dQ, dK, dV), the rest (bf16 with D = 16, fp32) on the CUDA-core kernels (backward: 8 launches)."""
     import torch
     from bwd_la_fwd_gb300 import la
     x = inputs.generate(1, 2, 300, D, 3, dtype=dtype)
@@ -102,7 +102,7 @@ def test_path_taken(dtype, D, tc):
     la.la_backward(Q, K, V, O, dO, True, workspace=ws)
     torch.cuda.synchronize()
     assert la.la_get_status(ws) == 0
-    assert la.la_launch_count() - n0 == (5 if tc else 8)
+    assert la.la_launch_count() - n0 == launches
 
 
 def test_repeatable_and_workspace_reusable():
@@ -142,3 +142,34 @@ def test_first_chunk_of_each_piece_waits_for_its_tiles(oracle_lib, monkeypatch, 
         assert la.la_get_status(ws) == 0
         U.assert_close("g", U.to_f64(g), g_ref, "bf16")
         U.assert_close("O", U.to_f64(O), O_ref, "bf16")
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 300])
+def test_wide_heads_edge_lengths(oracle_lib, N, causal):
+    """bf16 D = 256 (the wide tensor-core kernels: one CTA per head and 128-column output half) at lengths
+    around the 128-row chunk; at N = 1 dQ and dK vanish by the definition and are checked as in
+    test_single_row."""
+    if N > 1:
+        _check(oracle_lib, 1, 3, N, 256, "bf16", causal, seed=61 + N)
+        return
+    x = inputs.generate(1, 3, 1, 256, 61, dtype="bf16")
+    got = U.run_library(x, "bf16", causal)
+    f = U.stored_to_f64(x, "bf16")
+    O, g = oracle_lib.forward(f["Q"], f["K"], f["V"], causal)
+    dQ, dK, dV = oracle_lib.backward(f["Q"], f["K"], f["V"], f["dO"], causal)
+    for name, r in (("O", O), ("g", g), ("dV", dV)):
+        U.assert_close(name, got[name], r, "bf16")
+    dov = np.abs(np.sum(f["dO"] * f["V"], axis=-1, keepdims=True)) / np.abs(g[..., None])
+    for name, other in (("dQ", f["K"]), ("dK", f["Q"])):
+        scale = dov * np.max(np.abs(other), axis=-1, keepdims=True)
+        assert np.all(np.abs(got[name]) <= U.TOL["bf16"] * scale + 1e-30), name
+
+
+@pytest.mark.parametrize("causal", [1, 0])
+@pytest.mark.parametrize("ctas", [2, 4])
+def test_wide_heads_several_heads_per_cta(oracle_lib, monkeypatch, ctas, causal):
+    """bf16 D = 256 with the grid capped (LA_TC_MAX_CTAS): each CTA walks several heads in turn, each from a
+    zero state, and the g pass (one CTA per head) several heads too."""
+    monkeypatch.setenv("LA_TC_MAX_CTAS", str(ctas))
+    _check(oracle_lib, 2, 3, 300, 256, "bf16", causal, seed=71 + ctas)

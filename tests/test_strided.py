@@ -1,7 +1,8 @@
 """Strided operands on the GPU: [B,N,H,D] views and the slices of a fused [B,N,3,H,D] QKV tensor go to the
 library as they are (no transpose copy) and give exactly what the contiguous calls give on the same
-values, on both paths (tensor cores: bf16, D = 128; CUDA cores: fp32), causal and non-causal, forward,
-backward and the backward that reuses the forward's sums; one case is also checked against the oracle.
+values, on every path (tensor cores: bf16 with D = 32 ... 128 and, on the wide kernels, D = 256; CUDA cores:
+fp32), causal and non-causal, forward, backward and the backward that reuses the forward's sums; one case
+is also checked against the oracle.
 bf16 with D = 32 or 64 runs on the tensor-core kernels with the columns past D zero-extended by the tensor
 maps: the fused cases check that no store reaches past an operand's D columns into its neighbour's.
 """
@@ -13,7 +14,7 @@ from bwd_la_fwd_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 
-CASES = [("bf16", 128), ("bf16", 64), ("bf16", 32), ("f32", 64)]
+CASES = [("bf16", 128), ("bf16", 64), ("bf16", 32), ("bf16", 256), ("f32", 64)]
 
 
 def _bnhd(t):

@@ -233,7 +233,10 @@ int la_forward_strided(const void *Q, const void *K, const void *V, int causal, 
     const void *ins[3] = {Q, K, V};
     for (int k = 0; k < 3; ++k)
         if (operands_meet(p, O, p.lay[la::kOpO], ins[k], p.lay[ops[k]], elem)) return LA_ERR_INVALID_ARG;
-    const Range ws_r = range_of(workspace, p.bytes_fwd), o_r = range_of(O, (size_t)span_of(p, p.lay[la::kOpO]) * elem);
+    // the bytes of the workspace the forward writes: for D = 256 with a backward-sized workspace it also
+    // keeps g there for the backward
+    const size_t ws_used = p.use_wide && workspace_bytes >= p.bytes_bwd ? p.bytes_bwd : p.bytes_fwd;
+    const Range ws_r = range_of(workspace, ws_used), o_r = range_of(O, (size_t)span_of(p, p.lay[la::kOpO]) * elem);
     if (overlap(o_r, ws_r)) return LA_ERR_INVALID_ARG;
     if (normaliser) {
         const Range g_r = range_of(normaliser, (size_t)p.BH * N * 4);
@@ -244,7 +247,8 @@ int la_forward_strided(const void *Q, const void *K, const void *V, int causal, 
     cudaStream_t s = (cudaStream_t)stream;
     unsigned char *ws = (unsigned char *)workspace;
     cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, ws, s) : clear_state_tag(workspace, s);
-    if (e == cudaSuccess && p.use_wide) e = la::wide_forward(p, Q, K, V, O, normaliser, ws, s);
+    if (e == cudaSuccess && p.use_wide)
+        e = la::wide_forward(p, Q, K, V, O, normaliser, ws, s, workspace_bytes >= p.bytes_bwd);
     else if (e == cudaSuccess && !p.use_tc) e = la::simt_forward(p, Q, K, V, O, normaliser, ws, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
@@ -282,10 +286,18 @@ static int backward_impl(const void *Q, const void *K, const void *V, const void
     }
     cudaStream_t s = (cudaStream_t)stream;
     unsigned char *ws = (unsigned char *)workspace;
-    cudaError_t e = p.use_tc ? la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, ws, s, reuse_fwd_state)
-                             : clear_state_tag(workspace, s);
-    if (e == cudaSuccess && p.use_wide) e = la::wide_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s);
-    else if (e == cudaSuccess && !p.use_tc) e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s);
+    cudaError_t e = cudaSuccess;
+    if (p.use_tc) {
+        e = la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, ws, s, reuse_fwd_state);
+    } else if (p.use_wide) {
+        // D = 256: the reusing backward checks the forward's record of g; the plain one recomputes g over
+        // the region the forward keeps it in, so that record no longer holds
+        if (!reuse_fwd_state) e = clear_state_tag(workspace, s);
+        if (e == cudaSuccess) e = la::wide_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s, reuse_fwd_state);
+    } else {
+        e = clear_state_tag(workspace, s);
+        if (e == cudaSuccess) e = la::simt_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s);
+    }
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 

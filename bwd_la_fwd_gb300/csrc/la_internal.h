@@ -33,10 +33,9 @@ enum : uint32_t { kDevOk = 0, kDevTimeout = 5, kDevBounds = 6, kDevState = 7 };
 struct WsHeader {
     uint32_t status;      // sticky device status (first error wins); cleared by la_get_status
     uint32_t info[7];     // where the first error happened (kernel id, block, step), for debugging
-    uint32_t ticket[8];   // per-kernel ticket counters (reset by the last block of each launch)
-    uint32_t done[8];     // per-kernel completion counters
-    uint32_t epoch[8];    // per-kernel launch epochs (flags compare against these)
-    uint64_t state_tag[7]; // which K, V and slicing the per-piece state sums belong to, and their form
+    uint32_t wide_skip;   // D = 256 backward: its row kernel found no matching forward record, skip the rest
+    uint32_t reserved[23];
+    uint64_t state_tag[7]; // which operands and work split the saved sums (or g) belong to, and their form
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
 static_assert(offsetof(WsHeader, state_tag) == 128, "the state tag sits 128 bytes into the header");

@@ -109,10 +109,14 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
 
 // bf16 with D = 256: the tcgen05 kernels of la_tc_wide.cu (one CTA per head and 128-column output half).
 bool wide_supported(const Plan &p);
+// keep_g: the workspace is sized for the backward; g_i is also kept there, with a record of Q, K and shape.
 cudaError_t wide_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
-                         unsigned char *ws, cudaStream_t s);
+                         unsigned char *ws, cudaStream_t s, bool keep_g);
 // Reads O (the forward's output) for dt_i = dO_i . O_i / g_i; the workspace holds g, dt and dO / g.
+// reuse_g: take g from the forward (record checked on the device, LA_ERR_STATE when it does not match)
+// instead of recomputing it.
 cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
-                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s);
+                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s,
+                          bool reuse_g);
 
 }  // namespace la

@@ -51,9 +51,30 @@ struct WideParams {
     int nchunk;                        // chunks of kC rows per head
     uint32_t *status;                  // workspace status word
     float *g_out;                      // forward, g-only pass: g_i [BH, N] (forward: may be null)
+    float *g_ws;                       // forward: also keep g_i here for the backward (may be null)
     const float *rs_dt;                // dQ, dK passes: dt_i [BH, N]
+    const uint32_t *skip;              // dQ, dK, dV passes: skip everything when *skip (may be null)
+    uint64_t tag[7];                   // forward with g_ws: the record of what g belongs to
     uint64_t wait_ns;                  // bound on one barrier wait (0: kWaitNs)
 };
+
+// The record a forward that keeps g in the workspace writes into the header's tag words, and that a
+// reusing backward checks: Q's and K's addresses and strides, the shape and the mask.
+__host__ __device__ inline void wide_g_tag(const void *Q, const void *K, uint64_t qk_layout, long long BH,
+                                           long long N, int causal, uint64_t *t) {
+    t[0] = 0x4C415F5749444547ull ^ qk_layout;  // "LA_WIDEG"
+    t[1] = (uint64_t)(uintptr_t)Q;
+    t[2] = (uint64_t)(uintptr_t)K;
+    t[3] = (uint64_t)BH;
+    t[4] = (uint64_t)N;
+    t[5] = (uint64_t)causal;
+    t[6] = 4;  // form: g of the D = 256 forward
+}
+
+// Thread 0 of a walk: whether the backward's row kernel found no matching record (then nothing is done).
+__device__ __forceinline__ bool wide_skipped(const WideParams &P) {
+    return P.skip != nullptr && *(volatile const uint32_t *)P.skip != 0u;
+}
 
 // Key row j's weight in an N = 16 MMA operand (8-row boxes of 128-byte rows, 128-byte swizzle, rows
 // j < 64 in the first box): row 0 holds bf16(w), row 1 bf16(w - row 0); rows 2-7 stay zero.  An MMA of
@@ -99,6 +120,8 @@ template <int MODE> __device__ __forceinline__ float with_const(float v, float a
 // ----------------------------------------------------------------------------------------------------
 // Causal walk (forward or reverse chunk order).  TMEM: T 0-127 (P packed into 0-63 once read; the chunk's
 // column sums z 64-95 and a 96-111 after that; the row-sum exchange 112-115), out 128-255, S 256-511.
+// One stage of tiles, filled in three parts so that the next chunk's first T steps start while this
+// chunk's out tile is still leaving: the low and high 128 columns of X and Y, and W.
 // ----------------------------------------------------------------------------------------------------
 template <int MODE, bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __grid_constant__ WideParams P) {
@@ -108,7 +131,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
     constexpr bool KCONST = MODE == kWDk;
     constexpr uint32_t XB = 4 * kBox;  // an X or Y tile: 128 rows x 256 columns
     constexpr uint32_t WB = 2 * kBox;  // a W (or out) tile: 128 rows x 128 columns
-    constexpr uint32_t STAGE = 2 * XB + (HAS_W ? WB : 0);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     bool aligned;
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
@@ -119,18 +141,23 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
     unsigned char *ones = NORM ? area + 1024 : area;
     unsigned char *wtile = area;
     float *ac = (float *)(area + 2048);      // a (fp32, 128): the constant-weighted sum of the earlier w rows
-    uint64_t *full = (uint64_t *)(ac + 128);
-    uint64_t *empty = full + 1, *barT = full + 2, *barP = full + 3, *barSb = full + 4, *barO = full + 5,
-             *barS = full + 6;
-    uint32_t *tslot = (uint32_t *)(full + 7);
+    // The stage is filled and released in three parts: lo = columns 0-127 of X and Y, hi = columns 128-255
+    // of X and Y, and W.  lo and W are free once the state update has read them; hi also holds the out tile.
+    uint64_t *fullLo = (uint64_t *)(ac + 128);
+    uint64_t *fullHi = fullLo + 1, *fullW = fullLo + 2, *emptyLW = fullLo + 3, *emptyHi = fullLo + 4;
+    uint64_t *barT = fullLo + 5, *barP = fullLo + 6, *barSb = fullLo + 7, *barO = fullLo + 8, *barS = fullLo + 9;
+    uint32_t *tslot = (uint32_t *)(fullLo + 10);
     AbortState *abst = (AbortState *)(tslot + 2);
     volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        mbar_init(full, 1);
-        mbar_init(empty, 2);  // the chunk's last MMA commit + the epilogue once the out tile has left X
+        mbar_init(fullLo, 1);
+        mbar_init(fullHi, 1);
+        mbar_init(fullW, 1);
+        mbar_init(emptyLW, 1);  // the chunk's last MMA commit (the state update)
+        mbar_init(emptyHi, 2);  // the last MMA commit + the epilogue once the out tile has left X's high half
         mbar_init(barT, 1);
         mbar_init(barP, kEpiThreads);
         mbar_init(barSb, kEpiThreads);
@@ -155,6 +182,15 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
     tc_fence_after();
     griddep_wait();
     griddep_launch_dependents();
+    if (MODE == kWFwd && P.g_ws && blockIdx.x == 0 && threadIdx.x == 0) {  // g is kept: record for what
+        volatile uint64_t *w = (volatile uint64_t *)((unsigned char *)P.status + 128);
+        for (int k = 0; k < 7; ++k) w[k] = P.tag[k];
+    }
+    if (MODE >= kWDq) {  // the backward's row kernel may have found no forward state to use
+        if (threadIdx.x == 0 && wide_skipped(P)) *abort_flag = 1;
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t tT = tmem, tO = tmem + 128, tS0 = tmem + 256, tS1 = tmem + 384;
     const uint32_t tZ0 = tT + 64, tZ1 = tT + 80, tA = tT + 96, tX = tT + 112;
@@ -163,29 +199,45 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
     const int hstep = MODE == kWG ? (int)gridDim.x : (int)(gridDim.x >> 1);
     const int nch = P.nchunk;
 
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer: X, Y (256 columns) and W (this CTA's half) of each chunk, one stage
+    if (skip) {
+        // no forward state to use: nothing to compute
+    } else if (warp == 0 && lane == 0) {
+        // ---- TMA producer: X, Y (256 columns) and W (this CTA's half) of each chunk, one stage in three parts
         prefetch_tmap(&P.tmX);
         prefetch_tmap(&P.tmY);
         if (HAS_W) prefetch_tmap(&P.tmW);
-        int it = 0;
+        int it = 0, nlo = 0, nhi = 0, nw = 0;  // parts issued
         bool ok = true;
         for (int h = h0; h < P.BH && ok; h += hstep) {
             const HeadCoord hc = head_coord<FLAT>(h, P.H);
             for (int k = 0; k < nch; ++k, ++it) {
                 const int c = REV ? nch - 1 - k : k;
-                if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x501)) {
+                if (it > 0 && !wait_or_abort(emptyLW, (it - 1) & 1, abort_flag, P.status, 0x501)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(full, STAGE);
-                for (int nb = 0; nb < 4; ++nb) {
-                    tile_load<FLAT>(xt + nb * kBox, &P.tmX, full, nb * 64, c * kC, hc);
-                    tile_load<FLAT>(yt + nb * kBox, &P.tmY, full, nb * 64, c * kC, hc);
+                mbar_arrive_expect_tx(fullLo, 2 * WB);
+                for (int nb = 0; nb < 2; ++nb) {
+                    tile_load<FLAT>(xt + nb * kBox, &P.tmX, fullLo, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(yt + nb * kBox, &P.tmY, fullLo, nb * 64, c * kC, hc);
                 }
-                if (HAS_W)
+                ++nlo;
+                if (HAS_W) {
+                    mbar_arrive_expect_tx(fullW, WB);
                     for (int nb = 0; nb < 2; ++nb)
-                        tile_load<FLAT>(wt + nb * kBox, &P.tmW, full, 128 * half + 64 * nb, c * kC, hc);
+                        tile_load<FLAT>(wt + nb * kBox, &P.tmW, fullW, 128 * half + 64 * nb, c * kC, hc);
+                    ++nw;
+                }
+                if (it > 0 && !wait_or_abort(emptyHi, (it - 1) & 1, abort_flag, P.status, 0x505)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(fullHi, 2 * WB);
+                for (int nb = 2; nb < 4; ++nb) {
+                    tile_load<FLAT>(xt + nb * kBox, &P.tmX, fullHi, nb * 64, c * kC, hc);
+                    tile_load<FLAT>(yt + nb * kBox, &P.tmY, fullHi, nb * 64, c * kC, hc);
+                }
+                ++nhi;
                 // the CTA's next chunk into L2 while this one is processed
                 int nh = h, nk = k + 1;
                 if (nk == nch) {
@@ -204,7 +256,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                 }
             }
         }
-        if ((!ok || *abort_flag) && it > 0) mbar_wait(full, (it - 1) & 1, 50000000ull);  // issued copies land first
+        if (!ok || *abort_flag) {  // issued copies land before the CTA exits
+            if (nlo > 0) mbar_wait(fullLo, (nlo - 1) & 1, 50000000ull);
+            if (nhi > 0) mbar_wait(fullHi, (nhi - 1) & 1, 50000000ull);
+            if (nw > 0) mbar_wait(fullW, (nw - 1) & 1, 50000000ull);
+        }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
@@ -218,17 +274,26 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
         for (int h = h0; h < P.BH && ok; h += hstep) {
             for (int k = 0; k < nch && ok; ++k, ++it) {
                 const uint32_t ph = it & 1;
-                ok = wait_or_abort(full, ph, abort_flag, P.status, 0x502);
+                ok = wait_or_abort(fullLo, ph, abort_flag, P.status, 0x502);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {  // T = X Y^T over the 256 columns
+                for (int s = 0; s < 8; ++s) {  // T = X Y^T over columns 0-127 ...
                     const uint32_t o = (s >> 2) * kBox + 32 * (s & 3);
                     mma_ss(tT, sdesc_sw128(xb + o, 16, 1024), sdesc_sw128(yb + o, 16, 1024), idKK, s > 0);
+                }
+                ok = wait_or_abort(fullHi, ph, abort_flag, P.status, 0x506);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 8; s < 16; ++s) {  // ... and 128-255
+                    const uint32_t o = (s >> 2) * kBox + 32 * (s & 3);
+                    mma_ss(tT, sdesc_sw128(xb + o, 16, 1024), sdesc_sw128(yb + o, 16, 1024), idKK, 1u);
                 }
                 mma_commit(barT);
                 ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x503);  // T read out; P in TMEM
                 if (ok && HAS_W) ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x504);
+                if (ok && HAS_W) ok = wait_or_abort(fullW, ph, abort_flag, P.status, 0x507);
                 if (!ok) break;
                 tc_fence_after();
                 if (HAS_W) {
@@ -262,7 +327,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     }
                 }
                 mma_commit(barS);
-                mma_commit(empty);
+                mma_commit(emptyLW);
+                mma_commit(emptyHi);
             }
         }
     } else if (warp >= 2) {
@@ -344,7 +410,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     tmem_wait_ld(x0, x1);
                     gi = (float)row0 + __uint_as_float(x0) + __uint_as_float(x1);
                     inv = 1.f / gi;
-                    if (row_ok && hf == 0 && P.g_out) P.g_out[rix] = gi;
+                    if (row_ok && hf == 0) {
+                        if (P.g_out) P.g_out[rix] = gi;
+                        if (MODE == kWFwd && P.g_ws) P.g_ws[rix] = gi;
+                    }
                 }
                 ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x511);
                 if (!ok) break;
@@ -366,8 +435,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     an = ac[i] + __uint_as_float(v0) + (KCONST ? __uint_as_float(v1) : 0.f);
                 }
                 if (HAS_W) {
-                    // out_i = [P W + X Sb]_i + constant (forward: / g_i), staged in X (its readers are done)
-                    unsigned char *otile = xt + hf * kBox;
+                    // out_i = [P W + X Sb]_i + constant (forward: / g_i), staged in X's high half (its readers,
+                    // the MMAs and this row's q . z, are done)
+                    unsigned char *otile = xt + (2 + hf) * kBox;
 #pragma unroll 1
                     for (int half32 = 0; half32 < 2; ++half32) {
                         uint32_t v[32];
@@ -392,11 +462,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                 if (threadIdx.x == 64) {
                     if (HAS_W) {
                         for (int nb = 0; nb < 2; ++nb)
-                            tile_store<FLAT>(&P.tmOut, xt + nb * kBox, 128 * half + 64 * nb, (int)row0, hc);
+                            tile_store<FLAT>(&P.tmOut, xt + (2 + nb) * kBox, 128 * half + 64 * nb, (int)row0, hc);
                         bulk_commit();
                         bulk_wait_read0();
                     }
-                    mbar_arrive(empty);
+                    mbar_arrive(emptyHi);
                 }
                 if (NORM && hf == 0) {
                     zc[i] = zn0;
@@ -488,6 +558,15 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
     tc_fence_after();
     griddep_wait();
     griddep_launch_dependents();
+    if (MODE == kWFwd && P.g_ws && blockIdx.x == 0 && threadIdx.x == 0) {  // g is kept: record for what
+        volatile uint64_t *w = (volatile uint64_t *)((unsigned char *)P.status + 128);
+        for (int k = 0; k < 7; ++k) w[k] = P.tag[k];
+    }
+    if (MODE >= kWDq) {  // the backward's row kernel may have found no forward state to use
+        if (threadIdx.x == 0 && wide_skipped(P)) *abort_flag = 1;
+        __syncthreads();
+    }
+    const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t tS0 = tmem + 256, tS1 = tmem + 384;
     const uint32_t tZ0 = tmem, tZ1 = tmem + 16, tA = tmem + 32, tX = tS0;
@@ -496,7 +575,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
     const int hstep = MODE == kWG ? (int)gridDim.x : (int)(gridDim.x >> 1);
     const int nch = P.nchunk;
 
-    if (warp == 0 && lane == 0) {
+    if (skip) {
+        // no forward state to use: nothing to compute
+    } else if (warp == 0 && lane == 0) {
         // ---- TMA producer
         prefetch_tmap(&P.tmX);
         prefetch_tmap(&P.tmY);
@@ -669,7 +750,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
                     tmem_wait_ld(x0, x1);
                     const float gi = (float)P.N + __uint_as_float(x0) + __uint_as_float(x1);
                     inv = 1.f / gi;
-                    if (row_ok && hf == 0 && P.g_out) P.g_out[rix] = gi;
+                    if (row_ok && hf == 0) {
+                        if (P.g_out) P.g_out[rix] = gi;
+                        if (MODE == kWFwd && P.g_ws) P.g_ws[rix] = gi;
+                    }
                 }
                 if (HAS_W) {
                     ok = wait_or_abort(&barOB[s], phs, abort_flag, P.status, 0x544);
@@ -724,13 +808,35 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
 // Row terms of the backward: dt_i = (dO_i . O_i) / g_i and dOt_i = dO_i / g_i (bf16, contiguous
 // [B H, N, 256]).  One warp per row; a lane owns 8 consecutive columns.
 // ----------------------------------------------------------------------------------------------------
+struct WideTag {
+    uint64_t t[7];
+};
+
+// With `check`, g comes from the forward: every block first compares the workspace record with `expect`;
+// on a mismatch nothing is computed, block 0 reports LA_ERR_STATE and tells the walks to skip.
 __global__ void __launch_bounds__(256) wide_rowstats_kernel(const __nv_bfloat16 *__restrict__ dO, Layout ldo,
                                                             const __nv_bfloat16 *__restrict__ O, Layout lo,
                                                             const float *__restrict__ g, float *__restrict__ dt,
                                                             __nv_bfloat16 *__restrict__ dOt, int H, long long N,
-                                                            long long rows) {
+                                                            long long rows, uint32_t *status, int check,
+                                                            WideTag expect) {
+    __shared__ int bad;
     griddep_wait();
     griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        bool match = true;
+        if (check) {
+            const volatile uint64_t *w = (const volatile uint64_t *)((const unsigned char *)status + 128);
+            for (int k = 0; k < 7; ++k) match = match && w[k] == expect.t[k];
+        }
+        bad = match ? 0 : 1;
+        if (blockIdx.x == 0) {
+            ((WsHeader *)status)->wide_skip = match ? 0u : 1u;
+            if (!match) report(status, kDevState, 0x5A7Fu);
+        }
+    }
+    __syncthreads();
+    if (bad) return;
     const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= rows) return;
     const int lane = threadIdx.x & 31;
@@ -807,8 +913,7 @@ cudaError_t launch_wide(int mode, bool causal, bool flat, const WideParams &P, i
     }
     int G = mode == tc::kWG ? (P.BH < cap ? P.BH : cap) : 2 * (P.BH < cap / 2 ? P.BH : cap / 2);
     if (G < 1) G = 1;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)G);
     cfg.blockDim = dim3(64 + tc::kEpiThreads);
     cfg.dynamicSmemBytes = causal ? kSmemWide : kSmemWideNc;
@@ -839,8 +944,15 @@ bool wide_common(WideParams &P, const Plan &p) {
 
 bool wide_supported(const Plan &p) { return p.dtype == 1 && p.D == 256; }
 
+uint64_t qk_layout(const Plan &p) {  // FNV-1a over Q's and K's strides
+    uint64_t hsh = 0xcbf29ce484222325ull;
+    for (int op : {kOpQ, kOpK})
+        for (long long v : {p.lay[op].sb, p.lay[op].sh, p.lay[op].sn}) hsh = (hsh ^ (uint64_t)v) * 0x100000001b3ull;
+    return hsh;
+}
+
 cudaError_t wide_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
-                         unsigned char *ws, cudaStream_t s) {
+                         unsigned char *ws, cudaStream_t s, bool keep_g) {
     if (!set_wide_attrs()) return cudaErrorInvalidValue;
     const int nsm = tc_host::sm_count();
     if (nsm <= 1) return cudaErrorInvalidDevice;
@@ -853,13 +965,18 @@ cudaError_t wide_forward(const Plan &p, const void *Q, const void *K, const void
         return cudaErrorInvalidValue;
     P.status = (uint32_t *)ws;
     P.g_out = g;
+    if (keep_g) {  // the workspace has room for the backward's row terms: keep g there for it
+        P.g_ws = (float *)(ws + p.off_rowstats);
+        tc::wide_g_tag(Q, K, qk_layout(p), p.BH, p.N, p.causal, P.tag);
+    }
     const cudaError_t e = launch_wide(tc::kWFwd, p.causal != 0, flat, P, nsm, s);
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
 
 cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O,
-                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s) {
+                          const void *dO, void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s,
+                          bool reuse_g) {
     if (!set_wide_attrs()) return cudaErrorInvalidValue;
     const int nsm = tc_host::sm_count();
     if (nsm <= 1) return cudaErrorInvalidDevice;
@@ -876,18 +993,21 @@ cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const voi
     WideParams P;
     wide_common(P, p);
     P.status = (uint32_t *)ws;
-    // 1. g_i (the forward's normaliser) from Q and K
-    if (!tc_host::make_map(&P.tmX, Q, p, kOpQ, flat) || !tc_host::make_map(&P.tmY, K, p, kOpK, flat))
-        return cudaErrorInvalidValue;
-    P.g_out = rs_g;
-    cudaError_t e = launch_wide(tc::kWG, causal, flat, P, nsm, s);
-    if (e != cudaSuccess) return e;
-    ++launches;
-    // 2. dt_i and dOt = dO / g
+    // 1. g_i (the forward's normaliser) from Q and K, unless the forward kept it in the workspace
+    cudaError_t e = cudaSuccess;
+    if (!reuse_g) {
+        if (!tc_host::make_map(&P.tmX, Q, p, kOpQ, flat) || !tc_host::make_map(&P.tmY, K, p, kOpK, flat))
+            return cudaErrorInvalidValue;
+        P.g_out = rs_g;
+        if ((e = launch_wide(tc::kWG, causal, flat, P, nsm, s)) != cudaSuccess) return e;
+        ++launches;
+    }
+    // 2. dt_i and dOt = dO / g (checking, when g is reused, that it belongs to these Q, K and shape)
     {
+        tc::WideTag expect;
+        tc::wide_g_tag(Q, K, qk_layout(p), p.BH, p.N, p.causal, expect.t);
         const long long rows = (long long)p.BH * p.N;
-        cudaLaunchConfig_t cfg;
-        memset(&cfg, 0, sizeof(cfg));
+        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
         cfg.blockDim = dim3(256);
         cfg.stream = s;
@@ -898,12 +1018,13 @@ cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const voi
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, tc::wide_rowstats_kernel, (const __nv_bfloat16 *)dO, p.lay[kOpdO],
                                (const __nv_bfloat16 *)O, p.lay[kOpO], (const float *)rs_g, rs_dt, dOt, p.H,
-                               (long long)p.N, rows);
+                               (long long)p.N, rows, (uint32_t *)ws, reuse_g ? 1 : 0, expect);
         if (e != cudaSuccess) return e;
         ++launches;
     }
     P.g_out = nullptr;
     P.rs_dt = rs_dt;
+    P.skip = &((const WsHeader *)ws)->wide_skip;
     // 3. dQ: x = dOt, y = V, w = K
     if (!tc_host::make_map(&P.tmX, dOt, q, kOpdO, flat) || !tc_host::make_map(&P.tmY, V, p, kOpV, flat) ||
         !tc_host::make_map(&P.tmW, K, p, kOpK, flat) || !tc_host::make_map(&P.tmOut, dQ, p, kOpdQ, flat))

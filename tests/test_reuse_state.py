@@ -4,6 +4,8 @@ The forward's first kernel sums k_j v_j^T, k_j and v_j over each piece of rows; 
 same sums.  The reusing entry point must give exactly what la_backward gives (the sums are the same
 numbers, so the gradients are bit-identical), must refuse (LA_ERR_STATE, nothing computed) when the
 workspace holds sums of other K, V or of another work split, and is plain la_backward on the SIMT path.
+For bf16 with D = 256 what is reused is the normaliser g_i, which the forward keeps in a backward-sized
+workspace together with a record of Q, K, shape and mask: the same bit-identity and refusal rules hold.
 """
 import pytest
 
@@ -21,7 +23,7 @@ def _tensors(B, H, N, D, dtype, seed):
 
 
 @pytest.mark.parametrize("causal", [1, 0])
-@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("f32", 64)])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("bf16", 256), ("f32", 64)])
 def test_reuse_is_bit_identical_to_la_backward(causal, dtype, D):
     import torch
     from bwd_la_fwd_gb300 import la
@@ -122,3 +124,27 @@ def test_reuse_after_a_forward_with_the_other_mask_reports_state_error(fwd_causa
     O, _ = la.la_forward(t["Q"], t["K"], t["V"], bool(fwd_causal), workspace=ws)
     la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], not fwd_causal, workspace=ws, reuse_forward_state=True)
     assert la.la_get_status(ws) == LA_ERR_STATE
+
+
+@pytest.mark.parametrize("case", ["other_queries", "forward_sized_workspace", "other_mask"])
+def test_wide_reuse_without_matching_forward_reports_state_error(case):
+    """bf16 D = 256: the reusing backward checks the record of the forward's g (Q, K, strides, shape, mask)
+    on the device; when it does not match, the row kernel and the three walks compute nothing."""
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 1, 2, 300, 256
+    _, t = _tensors(B, H, N, D, "bf16", seed=81)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)
+    Q = t["Q"].clone() if case == "other_queries" else t["Q"]
+    fws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, False) if case == "forward_sized_workspace" else ws
+    O, _ = la.la_forward(Q, t["K"], t["V"], case != "other_mask", workspace=fws)
+    dQ, dK, dV = (torch.full_like(t["Q"], 7.0) for _ in range(3))
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, dQ=dQ, dK=dK, dV=dV, workspace=ws,
+                   reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+    for g in (dQ, dK, dV):
+        assert bool((g == 7.0).all())  # nothing was computed
+    # the plain backward on the same workspace then computes, and the record check is not sticky
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, dQ=dQ, workspace=ws)
+    assert la.la_get_status(ws) == 0
+    assert not bool((dQ == 7.0).any())

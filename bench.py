@@ -580,7 +580,9 @@ def run_sweep(args):
         step_ms = fwd_ms + bwd_ms
         line = {"workload": "sweep", "case": name, "B": b, "H": h, "N": n, "D": d, "layers": layers,
                 "causal": True, "dtype": "bf16", "seed": seed, "steps": args.steps, "warmup": args.warmup,
-                "path": "tensor cores" if d in (32, 64, 128) else "CUDA cores",
+                "path": ("tensor cores" if d in (32, 64, 128) else
+                         "tensor cores, wide kernels (one CTA per head and 128-column output half)" if d == 256
+                         else "CUDA cores"),
                 "fwd_us": fwd_ms * 1e3, "bwd_us": bwd_ms * 1e3, "step_ms": step_ms,
                 "tokens_per_s": b * n / (step_ms * 1e-3),
                 "tflops": layers * 14 * d * d * b * h * n / (step_ms * 1e-3) / 1e12,

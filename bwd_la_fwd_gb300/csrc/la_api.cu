@@ -49,17 +49,17 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
     const size_t sd = p->use_tc ? 128 : (size_t)D;
     p->stride = (long long)round_up(sd * sd + 2 * sd, 64);
     if (p->use_tc) {
-        // forward-direction slots (forward and backward), reverse-direction slots and per-row g, dt
-        // (backward only)
+        // state slots (the forward's sums; in the backward also its reverse sums, in the same slots), each
+        // chunk's column sums, and (backward only) per-row g, dt and each chunk's y_c, e_c
         const size_t slots = tc_slot_bytes(*p);
         const size_t nchunk = ((size_t)N + 127) / 128;
         p->off_states = 256;
+        p->off_states2 = p->off_states;
         p->off_chunkza = round_up(p->off_states + slots, 256);
-        p->off_states2 = round_up(p->off_chunkza + (size_t)BH * nchunk * 256 * sizeof(float), 256);
-        p->off_flags = round_up(p->off_states2 + slots, 256);
+        p->bytes_fwd = round_up(p->off_chunkza + (size_t)BH * nchunk * 256 * sizeof(float), 256);
+        p->off_flags = p->bytes_fwd;
         p->off_rowstats = p->off_flags;
         p->off_chunkye = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
-        p->bytes_fwd = p->off_states2;
         p->bytes_bwd = round_up(p->off_chunkye + (size_t)BH * nchunk * 256 * sizeof(float), 256);
         return true;
     }

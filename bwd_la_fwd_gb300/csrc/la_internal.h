@@ -34,7 +34,8 @@ struct WsHeader {
     uint32_t status;      // sticky device status (first error wins); cleared by la_get_status
     uint32_t info[7];     // where the first error happened (kernel id, block, step), for debugging
     uint32_t wide_skip;   // D = 256 backward: its row kernel found no matching forward record, skip the rest
-    uint32_t reserved[23];
+    uint32_t fwd_sums_used; // a backward has put its reverse sums where the recorded forward sums were
+    uint32_t reserved[22];
     uint64_t state_tag[7]; // which operands and work split the saved sums (or g) belong to, and their form
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");

@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace (and unused)?
+        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *fwd_sums_used(P))) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -623,8 +623,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace (and unused)?
+        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *fwd_sums_used(P))) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -871,6 +871,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         }
         __syncthreads();
     }
+    // this backward's reverse sums now fill the slots of the forward's sums (the dQ walk, which checked
+    // them, is complete)
+    if (blockIdx.x == 0 && threadIdx.x == 0) *fwd_sums_used(P) = 1u;
     const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
@@ -1146,6 +1149,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         }
         __syncthreads();
     }
+    // this backward's reverse sums now fill the slots of the forward's sums (the dQ walk, which checked
+    // them, is complete)
+    if (blockIdx.x == 0 && threadIdx.x == 0) *fwd_sums_used(P) = 1u;
     const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256;
@@ -1326,6 +1332,8 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         !tc_host::make_map(&P.tmdV, dV, p, kOpdV, flat))
         return cudaErrorInvalidValue;
     P.flat = flat ? 1 : 0;
+    // The reverse sums share the slot array with the forward sums: the dQ walk reads a piece's forward
+    // carry when the piece starts and writes that piece's reverse sums (same slot, same CTA) when it ends.
     P.slots_rev = (float *)(ws + p.off_states2);
     P.rs_g = (float *)(ws + p.off_rowstats);
     P.rs_dt = P.rs_g + (size_t)p.BH * p.N;
@@ -1345,7 +1353,8 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         e = tc_host::launch_agg(P, s);
         ++launches;
         if (e == cudaSuccess) {
-            e = tc_host::launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal, true, s);
+            e = tc_host::launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal,
+                                        p.causal ? tc::kTagPrefix : tc::kTagTotals, s);
             ++launches;
         }
     }
@@ -1357,7 +1366,7 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         ++launches;
     }
     if (e == cudaSuccess) {
-        e = tc_host::launch_combine(P, P.slots_rev, p.causal ? tc::kCombineSuffix : tc::kCombineTotal, false, s);
+        e = tc_host::launch_combine(P, P.slots_rev, p.causal ? tc::kCombineSuffix : tc::kCombineTotal, 0, s);
         ++launches;
     }
     if (e == cudaSuccess) {

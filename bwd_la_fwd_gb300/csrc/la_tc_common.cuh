@@ -20,7 +20,7 @@ namespace la {
 namespace tc {
 
 constexpr int kC = 128;               // rows per chunk
-constexpr int kMaxCtas = 256;         // upper bound on G used to size the workspace
+constexpr int kMaxCtas = 160;         // upper bound on G (>= the 152 SMs of a GB300) used to size the workspace
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on any single barrier wait
 
 struct Slices {

@@ -214,9 +214,10 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
 
 
 // ----------------------------------------------------------------------------------------------------
-// Forward output.  Per chunk (causal): T = Q K^T -> P = [j <= i](1 + T) (bf16, in place in TMEM) ->
-// O = P V + Q Sb (Sb = bf16 state before the chunk) -> S += K^T V (TMEM), from which the epilogue writes
-// the next Sb; the running fp32 z, a advance by each chunk's z_c, a_c from the sums kernel.  The epilogue
+// Forward output.  Per chunk (causal): T = Q K^T; O = Q Sb (Sb = bf16 state before the chunk) and
+// S += K^T V (TMEM) while the epilogue forms P = [j <= i](1 + T) (bf16, in place in TMEM); O += P V; the
+// epilogue then writes the next Sb from S; the running fp32 z, a advance by each chunk's z_c, a_c from the
+// sums kernel.  The epilogue
 // forms q_i . z and the normaliser.  Non-causal: O = Q Sb with the head's totals (no T, P or state update) into two
 // alternating TMEM accumulators, so the MMA of one chunk overlaps the epilogue of the previous one.
 // Eight epilogue warps: two per TMEM lane quarter, each owning half of the columns; the row sums they
@@ -349,29 +350,34 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                         mma_ss(tT, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                                sdesc_sw128(kb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024), idKK, k > 0);
                     mma_commit(barT);
-                    // S += K^T V as soon as the epilogue has copied S into this chunk's Sb, so that the
-                    // update runs while the epilogue forms P
+                    // once the epilogue has copied S into this chunk's Sb (and read the previous O out):
+                    // O = Q Sb, then S += K^T V, both while the epilogue forms P
                     ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x205);
                     if (!ok) break;
                     tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)  // O = Q Sb, K steps over d
+                        mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                               sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, k > 0);
                     if (c + 1 < pc.e) {
 #pragma unroll
                         for (int k = 0; k < kC / 16; ++k)  // S += K^T V
                             mma_ss(tS, sdesc_sw128(kb + 2048 * k, kBox, 1024), sdesc_sw128(vb + 2048 * k, kBox, 1024),
                                    idMM, 1u);
                     }
-                    mma_commit(barS);
+                    mma_commit(barS);  // also: Q Sb, Sb's reader, is complete
                     ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x204);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < kC / 16; ++k)  // O = P V, K steps over j (P in TMEM, 8 columns each)
-                        mma_ts(tO, tT + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, k > 0);
-                }
+                    for (int k = 0; k < kC / 16; ++k)  // O += P V, K steps over j (P in TMEM, 8 columns each)
+                        mma_ts(tO, tT + 8 * k, sdesc_sw128(vb + 2048 * k, kBox, 1024), idKM, 1u);
+                } else {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k)  // O += Q Sb, K steps over d
-                    mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
-                           sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, (CAUSAL || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < D / 16; ++k)  // O = Q Sb, K steps over d
+                        mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                               sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, k > 0);
+                }
                 mma_commit(&barO[ob]);
                 mma_commit(&empty[s]);
             }
@@ -487,12 +493,14 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                         if (nb == 0 || P.nbox > 1)
                             tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_commit();
-                    bulk_wait_read0();       // the tile has been read out of shared memory
-                    mbar_arrive(&empty[s]);  // the stage may be refilled
+                    if (!CAUSAL) {
+                        bulk_wait_read0();       // the tile has been read out of shared memory
+                        mbar_arrive(&empty[s]);  // the stage may be refilled
+                    }
                 }
                 if (!CAUSAL) mbar_arrive(&barOf[ob]);
                 if (CAUSAL) {
-                    // S after this chunk -> Sb for the next one: Q Sb, Sb's reader, is complete (barO above)
+                    // S after this chunk -> Sb for the next one (Q Sb, Sb's reader, is complete: barS)
                     ok = wait_or_abort(barS, ph, abort_flag, P.status, 0x208);
                     if (!ok) break;
                     tc_fence_after();
@@ -503,6 +511,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(barSb);
+                    }
+                    if (threadIdx.x == 64) {  // after the copy, which the next chunk's MMAs wait for
+                        bulk_wait_read0();       // the O tile has been read out of shared memory
+                        mbar_arrive(&empty[s]);  // the stage may be refilled
                     }
                     epi_sync256();  // everyone has read z and a of this chunk
                     if (c + 1 < pc.e) (hf == 0 ? zc : ac)[i] = vn;
@@ -536,8 +548,10 @@ template __global__ void tc_fwd_kernel<false, false>(const __grid_constant__ TcP
 __global__ void __launch_bounds__(256, 8) tc_combine_kernel(const __grid_constant__ TcParams P) {
     griddep_wait();  // the slots come from the previous kernel of the stream
     griddep_launch_dependents();
-    if (P.combine_tag && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-        write_state_tag(P, P.combine_mode == kCombineTotal ? kTagTotals : kTagPrefix);
+    if (P.combine_tag && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        write_state_tag(P, P.combine_tag);
+        *fwd_sums_used(P) = 0u;
+    }
     const int x = blockIdx.x * 256 + threadIdx.x;
     if (x >= kSlotF4) return;
     const long long BH = P.sl.T / P.sl.nchunk, s4 = P.slot_stride / 4;
@@ -700,10 +714,10 @@ cudaError_t launch_tc(void (*kernel)(const tc::TcParams), dim3 grid, unsigned bl
     return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
-cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cudaStream_t s) {
+cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, uint64_t tag_form, cudaStream_t s) {
     P.combine_slots = slots;
     P.combine_mode = mode;
-    P.combine_tag = tag ? 1 : 0;
+    P.combine_tag = tag_form;
     const long long BH = P.sl.T / P.sl.nchunk;
     const dim3 grid((tc::kSlotF4 + 255) / 256, (unsigned)(BH < 65535 ? BH : 65535));
     return launch_tc(tc::tc_combine_kernel, grid, 256, 0, s, P);
@@ -740,7 +754,8 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     P.Vp = V;
     cudaError_t e = launch_agg(P, s);
     if (e == cudaSuccess)
-        e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal, true, s);
+        e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal,
+                           p.causal ? tc::kTagPrefix : tc::kTagTotals, s);
     if (e == cudaSuccess)
         e = p.causal ? launch_tc(flat ? tc::tc_fwd_kernel<true, true> : tc::tc_fwd_kernel<true, false>, P.sl.G,
                                  64 + tc::kEpiThreads, kSmemFwdCausal, s, P)

@@ -37,7 +37,7 @@ struct TcParams {
     int check_tag;          // backward reusing the forward's sums: 0 no check, else the form expected + 1
     float *combine_slots;   // tc_combine_kernel: the slot array it turns into carries
     int combine_mode;       // tc_combine_kernel: kCombinePrefix, kCombineSuffix or kCombineTotal
-    int combine_tag;        // tc_combine_kernel: also record the new form in the workspace tag
+    uint64_t combine_tag;   // tc_combine_kernel: the form to record in the workspace tag (0: leave the tag)
     uint64_t wait_ns;       // bound on a single barrier wait (0: the default, tc::kWaitNs)
     int test_drop_load;     // test hook: CTA 0 of the sums kernel issues no load for this iteration (-1: none)
 };
@@ -76,6 +76,11 @@ __device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
     for (int k = 0; k < kTagWords; ++k) ok = ok && w[k] == t[k];
     return ok;
 }
+// The backward keeps its reverse sums in the slots of the forward's sums; its dK/dV walk marks them used,
+// and the combine that records new forward sums clears the mark.
+__device__ inline volatile uint32_t *fwd_sums_used(const TcParams &P) {
+    return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, fwd_sums_used));
+}
 #endif
 
 }  // namespace tc
@@ -91,8 +96,9 @@ cudaError_t launch_agg(const tc::TcParams &P, cudaStream_t s);  // per-piece K^T
 // kernels order their global accesses after griddepcontrol.wait, so stream order is kept).
 cudaError_t launch_tc(void (*kernel)(const tc::TcParams), dim3 grid, unsigned block, size_t smem,
                       cudaStream_t s, const tc::TcParams &P);
-// Turns the piece slots of `slots` into carries (mode: tc::kCombine*; tag: record the form).
-cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, bool tag, cudaStream_t s);
+// Turns the piece slots of `slots` into carries (mode: tc::kCombine*; tag_form: the form to record in the
+// workspace tag, 0 to leave it).
+cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, uint64_t tag_form, cudaStream_t s);
 }  // namespace tc_host
 
 // bf16 storage with D = 32, 64 or 128: the tcgen05 kernels (on 128 columns, narrower heads zero-extended by

@@ -114,11 +114,12 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * and v_j over each piece of rows (the tensor-core path's work split), and both passes need exactly those
  * sums; la_backward recomputes them, this entry point takes them from `workspace` instead, the way an
  * autograd backward takes tensors saved by its forward.  Arguments, checks and results are those of
- * la_backward, with one more condition: the last call that computed state sums in this workspace must
- * have been la_forward or la_backward on the same K and V buffers (same pointers, unchanged contents) and
- * the same B, H, N, D and dtype.  The workspace records which K, V and shape its sums belong to; when the
- * record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.  Unchanged
- * contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or bf16 with
+ * la_backward, with one more condition: the last call on this workspace must have been la_forward on the
+ * same K and V buffers (same pointers, unchanged contents) and the same B, H, N, D, dtype and mask.  A
+ * backward uses those sums up (it keeps its own reverse-direction sums in the same slots), so each reusing
+ * backward needs a forward of its own.  The workspace records which K, V and shape its sums belong to;
+ * when the record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.
+ * Unchanged contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or bf16 with
  * D = 16) and on the wide path (bf16 with D = 256) there are no such sums to reuse and this call is
  * la_backward.
  */

@@ -3,7 +3,8 @@
 The forward's first kernel sums k_j v_j^T, k_j and v_j over each piece of rows; the backward needs the
 same sums.  The reusing entry point must give exactly what la_backward gives (the sums are the same
 numbers, so the gradients are bit-identical), must refuse (LA_ERR_STATE, nothing computed) when the
-workspace holds sums of other K, V or of another work split, and is plain la_backward on the SIMT path.
+workspace holds sums of other K, V or of another work split -- or none, because a backward has since used
+them up -- and is plain la_backward on the SIMT path.
 For bf16 with D = 256 what is reused is the normaliser g_i, which the forward keeps in a backward-sized
 workspace together with a record of Q, K, shape and mask: the same bit-identity and refusal rules hold.
 """
@@ -148,3 +149,28 @@ def test_wide_reuse_without_matching_forward_reports_state_error(case):
     la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, dQ=dQ, workspace=ws)
     assert la.la_get_status(ws) == 0
     assert not bool((dQ == 7.0).any())
+
+
+def test_a_backward_uses_up_the_forward_sums():
+    """The backward keeps its reverse-direction sums in the slots that held the forward's sums: a second
+    reusing backward after one forward finds no forward sums (LA_ERR_STATE, nothing computed); a fresh
+    forward makes reuse possible again, with the same results."""
+    import torch
+    from bwd_la_fwd_gb300 import la
+    B, H, N, D = 2, 3, 777, 128
+    _, t = _tensors(B, H, N, D, "bf16", seed=78)
+    ws = la.new_workspace(B, H, N, D, 1, la.LA_BF16, True)
+    O, _ = la.la_forward(t["Q"], t["K"], t["V"], True, workspace=ws)
+    first = la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    dQ = torch.full_like(t["Q"], 7.0)
+    la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, dQ=dQ, workspace=ws, reuse_forward_state=True)
+    assert la.la_get_status(ws) == LA_ERR_STATE
+    assert bool((dQ == 7.0).all())
+    la.la_forward(t["Q"], t["K"], t["V"], True, O=O, workspace=ws)
+    again = la.la_backward(t["Q"], t["K"], t["V"], O, t["dO"], True, workspace=ws, reuse_forward_state=True)
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    for a, b in zip(first, again):
+        assert torch.equal(a, b)

@@ -16,9 +16,9 @@
 //     dK       x = v,   y = dOt, w = q,   c = -dt_j,   j >= i   (per key row)
 //     dV       x = k,   y = q,   w = dOt, c = 1,       j >= i
 // (dK_j = sum_{i >= j} dW_ij q_i and dV_j = sum_{i >= j} (W_ij / g_i) dO_i with dW_ij = dOt_i . v_j - dt_i).
-// Per 128-row chunk (causal): out = P W + X Sb + c a, P_ij = m_ij (c_ij + T_ij) (bf16 in TMEM), Sb the
-// bf16 state of the earlier chunks (later chunks, walking in reverse), a = sum c_j w_j over them; then
-// S += Y^T W.  Non-causal: S, a (and z) over the whole head first, then out = X Sb + c a for every chunk.
+// Per 128-row chunk (causal): out = X Sb + P W + c a, P_ij = m_ij (c_ij + T_ij) (bf16 in TMEM), Sb the
+// bf16 state of the earlier chunks (later chunks, walking in reverse), a = sum c_j w_j over them; X Sb and
+// S += Y^T W are issued while the epilogue forms P.  Non-causal: S, a (and z) over the whole head first, then out = X Sb + c a for every chunk.
 // The normaliser g_i = n_i + q_i . z + r_i (z = sum k_j, r_i = sum_j P_ij) is formed by the forward and by
 // a g-only pass of the same kernel that the backward runs first.
 //
@@ -291,19 +291,36 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     mma_ss(tT, sdesc_sw128(xb + o, 16, 1024), sdesc_sw128(yb + o, 16, 1024), idKK, 1u);
                 }
                 mma_commit(barT);
+                if (HAS_W) {
+                    // once the epilogue has copied the state into Sb (and read the previous out): out = X Sb
+                    // and S += Y^T W while the epilogue forms P
+                    ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x504);
+                    if (ok) ok = wait_or_abort(fullW, ph, abort_flag, P.status, 0x507);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int s = 0; s < 16; ++s)  // out = X Sb over the 256 rows d of the state
+                        mma_ss(tO, sdesc_sw128(xb + (s >> 2) * kBox + 32 * (s & 3), 16, 1024),
+                               sdesc_sw128(sb + (s >> 3) * 2 * kBox + 2048 * (s & 7), kBox, 1024), idKM, s > 0);
+                    if (k + 1 < nch) {
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {  // S += Y^T W, rows d of the two 128-column blocks of Y
+                            const uint32_t acc = (k > 0 || s > 0) ? 1u : 0u;
+                            mma_ss(tS0, sdesc_sw128(yb + 2048 * s, kBox, 1024), sdesc_sw128(wb + 2048 * s, kBox, 1024),
+                                   idMM, acc);
+                            mma_ss(tS1, sdesc_sw128(yb + 2 * kBox + 2048 * s, kBox, 1024),
+                                   sdesc_sw128(wb + 2048 * s, kBox, 1024), idMM, acc);
+                        }
+                    }
+                }
+                mma_commit(barS);  // also: X Sb, Sb's reader, is complete
                 ok = wait_or_abort(barP, ph, abort_flag, P.status, 0x503);  // T read out; P in TMEM
-                if (ok && HAS_W) ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x504);
-                if (ok && HAS_W) ok = wait_or_abort(fullW, ph, abort_flag, P.status, 0x507);
                 if (!ok) break;
                 tc_fence_after();
                 if (HAS_W) {
 #pragma unroll
-                    for (int s = 0; s < 8; ++s)  // out = P W (P in TMEM, 16 rows j per step)
-                        mma_ts(tO, tT + 8 * s, sdesc_sw128(wb + 2048 * s, kBox, 1024), idKM, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 16; ++s)  // out += X Sb over the 256 rows d of the state
-                        mma_ss(tO, sdesc_sw128(xb + (s >> 2) * kBox + 32 * (s & 3), 16, 1024),
-                               sdesc_sw128(sb + (s >> 3) * 2 * kBox + 2048 * (s & 7), kBox, 1024), idKM, 1u);
+                    for (int s = 0; s < 8; ++s)  // out += P W (P in TMEM, 16 rows j per step)
+                        mma_ts(tO, tT + 8 * s, sdesc_sw128(wb + 2048 * s, kBox, 1024), idKM, 1u);
                 }
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {  // the chunk's column sums: z = Y^T 1, a = W^T c
@@ -316,17 +333,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     if (HAS_W) mma_ss(tA, sdesc_sw128(wb + 2048 * s, kBox, 1024), cd, idZ, s > 0);
                 }
                 mma_commit(barO);
-                if (HAS_W && k + 1 < nch) {
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {  // S += Y^T W, rows d of the two 128-column blocks of Y
-                        const uint32_t acc = (k > 0 || s > 0) ? 1u : 0u;
-                        mma_ss(tS0, sdesc_sw128(yb + 2048 * s, kBox, 1024), sdesc_sw128(wb + 2048 * s, kBox, 1024),
-                               idMM, acc);
-                        mma_ss(tS1, sdesc_sw128(yb + 2 * kBox + 2048 * s, kBox, 1024),
-                               sdesc_sw128(wb + 2048 * s, kBox, 1024), idMM, acc);
-                    }
-                }
-                mma_commit(barS);
                 mma_commit(emptyLW);
                 mma_commit(emptyHi);
             }
@@ -459,14 +465,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                 }
                 tc_fence_before();
                 epi_sync256();  // the out tile is complete; every read of z, a and the exchange is done
-                if (threadIdx.x == 64) {
-                    if (HAS_W) {
-                        for (int nb = 0; nb < 2; ++nb)
-                            tile_store<FLAT>(&P.tmOut, xt + (2 + nb) * kBox, 128 * half + 64 * nb, (int)row0, hc);
-                        bulk_commit();
-                        bulk_wait_read0();
-                    }
-                    mbar_arrive(emptyHi);
+                if (threadIdx.x == 64 && HAS_W) {
+                    for (int nb = 0; nb < 2; ++nb)
+                        tile_store<FLAT>(&P.tmOut, xt + (2 + nb) * kBox, 128 * half + 64 * nb, (int)row0, hc);
+                    bulk_commit();
                 }
                 if (NORM && hf == 0) {
                     zc[i] = zn0;
@@ -482,6 +484,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(barSb);
+                }
+                if (threadIdx.x == 64) {  // after the copy the next chunk's MMAs wait for
+                    if (HAS_W) bulk_wait_read0();  // the out tile has left X's high half
+                    mbar_arrive(emptyHi);
                 }
                 epi_sync256();  // z, a of the next chunk are in place
             }
@@ -806,8 +812,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
 
 // ----------------------------------------------------------------------------------------------------
 // Row terms of the backward: dt_i = (dO_i . O_i) / g_i and dOt_i = dO_i / g_i (bf16, contiguous
-// [B H, N, 256]).  One warp per row; a lane owns 8 consecutive columns.
+// [B H, N, 256]).  A warp takes kRowsPerWarp rows, a lane 8 consecutive columns of each; every load of
+// the warp's rows is issued before the first is used, so that enough bytes are in flight.
 // ----------------------------------------------------------------------------------------------------
+constexpr int kRowsPerWarp = 4;
+
 struct WideTag {
     uint64_t t[7];
 };
@@ -837,29 +846,39 @@ __global__ void __launch_bounds__(256) wide_rowstats_kernel(const __nv_bfloat16 
     }
     __syncthreads();
     if (bad) return;
-    const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (r >= rows) return;
     const int lane = threadIdx.x & 31;
-    const long long bh = r / N, n = r - bh * N;
-    const long long b = bh / H, h = bh - b * H;
-    const uint4 a = *(const uint4 *)(dO + b * ldo.sb + h * ldo.sh + n * ldo.sn + 8 * lane);
-    const uint4 o = *(const uint4 *)(O + b * lo.sb + h * lo.sh + n * lo.sn + 8 * lane);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, ov[4] = {o.x, o.y, o.z, o.w};
-    float d = 0.f;
+    const long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kRowsPerWarp;
+    uint4 a[kRowsPerWarp], o[kRowsPerWarp];
+    float gi[kRowsPerWarp];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        d = fmaf(bf16lo(av[q]), bf16lo(ov[q]), d);
-        d = fmaf(bf16hi(av[q]), bf16hi(ov[q]), d);
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        const long long r = r0 + k < rows ? r0 + k : rows - 1;  // rows past the end repeat the last (not stored)
+        const long long bh = r / N, n = r - bh * N;
+        const long long b = bh / H, h = bh - b * H;
+        a[k] = *(const uint4 *)(dO + b * ldo.sb + h * ldo.sh + n * ldo.sn + 8 * lane);
+        o[k] = *(const uint4 *)(O + b * lo.sb + h * lo.sh + n * lo.sn + 8 * lane);
+        gi[k] = g[r];
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-    const float gi = g[r], ig = 1.f / gi;
-    if (lane == 0) dt[r] = d * ig;
-    uint4 s;
-    uint32_t *sv = (uint32_t *)&s;
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+        const uint32_t av[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, ov[4] = {o[k].x, o[k].y, o[k].z, o[k].w};
+        float d = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) sv[q] = pack_bf16(bf16lo(av[q]) * ig, bf16hi(av[q]) * ig);
-    *(uint4 *)(dOt + r * 256 + 8 * lane) = s;
+        for (int q = 0; q < 4; ++q) {
+            d = fmaf(bf16lo(av[q]), bf16lo(ov[q]), d);
+            d = fmaf(bf16hi(av[q]), bf16hi(ov[q]), d);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+        if (r0 + k >= rows) continue;
+        const float ig = 1.f / gi[k];
+        if (lane == 0) dt[r0 + k] = d * ig;
+        uint4 sc;
+        uint32_t *sv = (uint32_t *)&sc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sv[q] = pack_bf16(bf16lo(av[q]) * ig, bf16hi(av[q]) * ig);
+        *(uint4 *)(dOt + (r0 + k) * 256 + 8 * lane) = sc;
+    }
 }
 
 }  // namespace tc
@@ -1008,7 +1027,7 @@ cudaError_t wide_backward(const Plan &p, const void *Q, const void *K, const voi
         tc::wide_g_tag(Q, K, qk_layout(p), p.BH, p.N, p.causal, expect.t);
         const long long rows = (long long)p.BH * p.N;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((rows + 7) / 8));
+        cfg.gridDim = dim3((unsigned)((rows + 8 * tc::kRowsPerWarp - 1) / (8 * tc::kRowsPerWarp)));
         cfg.blockDim = dim3(256);
         cfg.stream = s;
         cudaLaunchAttribute at[1];

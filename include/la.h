@@ -88,7 +88,9 @@ size_t la_workspace_bytes(int B, int H, int N, int D, int causal, int dtype, int
  *   O           out: [B,H,N,D] of `dtype`, O_i = sum_j W_ij v_j / g_i, rounded once (nearest-even)
  *   normaliser  out: float [B,H,N] with g_i, or NULL to skip it
  *   workspace   in/out: device scratch of workspace_bytes >= la_workspace_bytes(..., backward = 0)
- * Pointers must be 16-byte aligned.
+ * Pointers must be 16-byte aligned.  On the tensor-core paths the forward leaves in the workspace what
+ * la_backward_with_forward_state reuses (the per-piece sums; for bf16 with D = 256 the normaliser, and
+ * only when the workspace is backward-sized).
  */
 int la_forward(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B, int H,
                int N, int D, int dtype, void *workspace, size_t workspace_bytes, void *stream);
@@ -120,8 +122,12 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * backward needs a forward of its own.  The workspace records which K, V and shape its sums belong to;
  * when the record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.
  * Unchanged contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or bf16 with
- * D = 16) and on the wide path (bf16 with D = 256) there are no such sums to reuse and this call is
- * la_backward.
+ * D = 16) there are no such sums to reuse and this call is la_backward.  On the wide path (bf16 with
+ * D = 256) the forward forms no piece sums; what is reused there is the normaliser g_i, which la_forward
+ * keeps in the workspace when that workspace is backward-sized (la_workspace_bytes(..., backward = 1)),
+ * under a record of Q's and K's addresses and strides, the shape and the mask.  A mismatch is
+ * LA_ERR_STATE with nothing computed, as above; g is not used up, so several backwards may follow one
+ * forward there.
  */
 int la_backward_with_forward_state(const void *Q, const void *K, const void *V, const void *O, const void *dO,
                                    void *dQ, void *dK, void *dV, int causal, int B, int H, int N, int D, int dtype,

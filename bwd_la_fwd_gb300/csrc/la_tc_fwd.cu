@@ -493,9 +493,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                         if (nb == 0 || P.nbox > 1)
                             tile_store<FLAT>(&P.tmO, st + nb * kBox, nb * 64, (int)row0, head_coord<FLAT>(pc.h, P.H));
                     bulk_commit();
-                    if (!CAUSAL) {
-                        bulk_wait_read0();       // the tile has been read out of shared memory
-                        mbar_arrive(&empty[s]);  // the stage may be refilled
+                    if (!CAUSAL && it > 0) {
+                        // the previous chunk's O tile has been read out of shared memory: its stage may be
+                        // refilled (four stages: the release can trail by a chunk, and this one's store runs on)
+                        bulk_wait_read1();
+                        mbar_arrive(&empty[(it - 1) % NST]);
                     }
                 }
                 if (!CAUSAL) mbar_arrive(&barOf[ob]);

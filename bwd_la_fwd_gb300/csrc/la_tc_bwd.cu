@@ -128,6 +128,7 @@ __device__ __forceinline__ void piece_rev_sums(const TcParams &P, const Piece &p
                                                float y, float e) {
     constexpr int D = 128;
     float *slot = P.slots_rev + slot_of(pc.h, blockIdx.x) * P.slot_stride;
+    const bool sok = slot_ok(P, pc.h, blockIdx.x, 0xB007);  // the same for the whole CTA
 #pragma unroll 1
     for (int half32 = 0; half32 < 2; ++half32) {
         uint32_t v[32];
@@ -136,10 +137,10 @@ __device__ __forceinline__ void piece_rev_sums(const TcParams &P, const Piece &p
         float4 *dst = (float4 *)slot;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            dst[slot_f4(i, hf, 8 * half32 + q)] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+            if (sok) dst[slot_f4(i, hf, 8 * half32 + q)] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                                               __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
     }
-    if (hf == 1) {
+    if (hf == 1 && sok) {
         slot[(size_t)D * D + i] = y;
         slot[(size_t)D * D + D + i] = e;
     }
@@ -205,11 +206,12 @@ __device__ __forceinline__ bool next_rev_chunk(const PieceIter &pi, const Piece 
 __device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h, int c, int j, int hf, float *g,
                                                  float *dt, float *ye) {
     const long long r = (long long)c * kC + j;
-    const bool in = r < P.N;
-    const size_t x = (size_t)h * P.N + (in ? r : 0);
+    const long long x = h * P.N + r;
+    const bool in = r < P.N && in_range(x, n_row_floats(P), P.status, 0xB008);
     *g = in ? P.rs_g[x] : 0.f;
     *dt = in ? P.rs_dt[x] : 0.f;
-    *ye = P.chunk_ye[((size_t)h * P.sl.nchunk + c) * 256 + hf * 128 + j];
+    const long long yi = (h * P.sl.nchunk + c) * 256 + hf * 128 + j;
+    *ye = in_range(yi, n_chunk_floats(P), P.status, 0xB008) ? P.chunk_ye[yi] : 0.f;
 }
 
 // Issues the TMA stores of a two-box output tile from shared memory (the boxes that hold the operand's
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
         const long long hi = slice_lo(P.sl, blockIdx.x + 1);
         {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
-            if (p0.valid())
+            if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x, n_slot_floats(P), P.status);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x301)) {
                     ok = false;
                     break;
@@ -427,7 +429,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
             const Piece pc = pi.get();
             // forward state carried into the piece, from the head's earlier pieces (the previous
             // piece's MMAs on R2 are complete: its last barX has been waited for)
-            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, R2 + lo, 0u, 0u,
+            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+                load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, R2 + lo, 0u, 0u,
                                 Sb, zc, ac, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -439,7 +442,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
                 // this chunk's z_c[i] (half 0) or a_c[i] (half 1), from the sums kernel; used at the chunk's end
-                const float zav = P.chunk_za[((size_t)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i];
+                const long long zi = ((long long)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i;
+                const float zav = in_range(zi, n_chunk_floats(P), P.status, 0xB009) ? P.chunk_za[zi] : 0.f;
                 float gpart = 0.f, dpart = 0.f;  // partial g_i and partial delta_i g_i over this half
                 {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
@@ -489,8 +493,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 const float delta = (xd[i] + xd[kC + i]) * ig;
                 const float dt = delta * ig;
                 if (hf == 0 && i < nvalid) {
-                    P.rs_g[(size_t)pc.h * P.N + row0 + i] = gi;
-                    P.rs_dt[(size_t)pc.h * P.N + row0 + i] = dt;
+                    const long long x = (long long)pc.h * P.N + row0 + i;
+                    if (in_range(x, n_row_floats(P), P.status, 0xB00A)) {
+                        P.rs_g[x] = gi;
+                        P.rs_dt[x] = dt;
+                    }
                 }
                 {  // U' = [j <= i](W' - delta), bf16, over the R1 columns this half has read: R1 + 64 hf + [0, 32)
                     uint32_t pk[32];
@@ -529,9 +536,12 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     tmem_wait_ld(s0, s1);
                     tmem_wait_ld(s2, s3);
                     const float yv = __uint_as_float(s0) + __uint_as_float(s1), ev = __uint_as_float(s2);
-                    float *cye = P.chunk_ye + ((size_t)pc.h * P.sl.nchunk + c) * 256;
-                    cye[i] = yv;
-                    cye[128 + i] = ev;
+                    const long long ci = ((long long)pc.h * P.sl.nchunk + c) * 256;
+                    if (in_range(ci + i, n_chunk_floats(P), P.status, 0xB00B) &&
+                        in_range(ci + 128 + i, n_chunk_floats(P), P.status, 0xB00B)) {
+                        P.chunk_ye[ci + i] = yv;
+                        P.chunk_ye[ci + 128 + i] = ev;
+                    }
                     yacc += yv;
                     eacc += ev;
                 }
@@ -643,7 +653,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         prefetch_tmap(&P.tmdO);
         {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
-            if (p0.valid())
+            if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
@@ -653,7 +663,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x, n_slot_floats(P), P.status);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x321)) {
                     ok = false;
@@ -738,7 +748,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         bool ok = true;
         for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next(), ++pno) {
             const Piece pc = pi.get();
-            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, 0u, 0u, 0u, Sb, zc,
+            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+                load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, 0u, 0u, 0u, Sb, zc,
                                 ac, false, false);
             fence_proxy_async_smem();
             epi_sync256();
@@ -888,7 +899,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         prefetch_tmap(&P.tmV);
         {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
-            if (p0.valid())
+            if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots_rev + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
@@ -898,7 +909,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
-                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x, n_slot_floats(P), P.status);
                 if (it > 0 && !wait_or_abort(empty, (it - 1) & 1, abort_flag, P.status, 0x401)) {
                     ok = false;
                     break;
@@ -1008,7 +1019,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
             const Piece pc = pi.get();
             // carried reverse sums (the later pieces of the head); the previous piece's MMAs on R3 and Pb are
             // complete (its last barV)
-            load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, R3 + lo, 0u,
+            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+                load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, R3 + lo, 0u,
                                 0u, Pb, yc, ec, true, false);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1164,7 +1176,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
         prefetch_tmap(&P.tmV);
         {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
-            if (p0.valid())
+            if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots_rev + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
@@ -1174,7 +1186,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
-                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x);
+                prefetch_next_carry(pi, c - pc.a, pc.e - pc.a, P.slots_rev, P.slot_stride, blockIdx.x, n_slot_floats(P), P.status);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x421)) {
                     ok = false;
@@ -1238,7 +1250,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
             const Piece pc = pi.get();
             // the head's totals (every piece of a head carries the same sums); the previous piece's MMAs
             // on Pb are complete (its last barV)
-            load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, 0u, 0u, 0u, Pb,
+            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+                load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, 0u, 0u, 0u, Pb,
                                 yc, ec, false, false);
             fence_proxy_async_smem();
             epi_sync256();

@@ -108,6 +108,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
+// Index check of the LA_CHECKED build, for every global-memory index a thread computes itself: an index
+// outside [0, n) records LA_ERR_BOUNDS (6) with the place `where` in the workspace status word, and the
+// caller skips the access (a load then reads 0).  Tensor-map (TMA) copies need no such check: the maps
+// clip them to the operand's extents.  In the normal build the check is the constant true.
+__device__ __forceinline__ bool in_range(long long i, long long n, uint32_t *status, uint32_t where) {
+#ifdef LA_CHECKED
+    if (i >= 0 && i < n) return true;
+    report(status, 6u, where);
+    return false;
+#else
+    (void)i;
+    (void)n;
+    (void)status;
+    (void)where;
+    return true;
+#endif
+}
+
 // Byte offset of the 16-byte group holding element column `col8 * 8` of row `row` in a tile written by
 // TMA with the 128-byte swizzle (rows of 128 bytes = 64 bf16; group index XOR row % 8).
 __device__ __forceinline__ uint32_t sw128_off(int row, int col8) {

@@ -176,9 +176,12 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                 tmem_wait_ld(a0, a1);
                 tc_fence_before();
                 mbar_arrive(&zafree[zb]);
-                float *cza = P.chunk_za + ((size_t)pc.h * P.sl.nchunk + c) * 256;
-                cza[d] = __uint_as_float(z0);
-                cza[128 + d] = __uint_as_float(a0);
+                const long long ci = ((long long)pc.h * P.sl.nchunk + c) * 256;
+                if (in_range(ci + d, n_chunk_floats(P), P.status, 0xB001) &&
+                    in_range(ci + 128 + d, n_chunk_floats(P), P.status, 0xB001)) {
+                    P.chunk_za[ci + d] = __uint_as_float(z0);
+                    P.chunk_za[ci + 128 + d] = __uint_as_float(a0);
+                }
                 zs += __uint_as_float(z0);
                 as += __uint_as_float(a0);
             }
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
             if (!wait_or_abort(&accfull[buf], (p >> 1) & 1, abort_flag, P.status, 0x104)) break;
             tc_fence_after();
             float *slot = P.slots + slot_of(pc.h, blockIdx.x) * P.slot_stride;
+            const bool sok = slot_ok(P, pc.h, blockIdx.x, 0xB002);  // the same for the whole CTA
             const uint32_t ta = tmem + ((uint32_t)lb << 16) + buf * 128;
 #pragma unroll 1
             for (int c16 = 0; c16 < D / 16; ++c16) {
@@ -195,12 +199,14 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
                 float4 *dst = (float4 *)slot;
 #pragma unroll
                 for (int q = 0; q < 4; ++q)  // columns 16 c16 + 4 q: half c16 / 4, float4 4 (c16 % 4) + q of the half
-                    dst[slot_f4(d, c16 >> 2, 4 * (c16 & 3) + q)] =
+                    if (sok) dst[slot_f4(d, c16 >> 2, 4 * (c16 & 3) + q)] =
                         make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                     __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
             }
-            slot[(size_t)D * D + d] = zs;
-            slot[(size_t)D * D + D + d] = as;
+            if (sok) {
+                slot[(size_t)D * D + d] = zs;
+                slot[(size_t)D * D + D + d] = as;
+            }
             tc_fence_before();
             mbar_arrive(&accfree[buf]);
         }
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         }
         {  // the first piece's carry slot
             PieceIter p0(P.sl, blockIdx.x);
-            if (p0.valid())
+            if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.a; c < pc.e; ++c, ++it) {
-                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x);
+                prefetch_next_carry(pi, pc.e - 1 - c, pc.e - pc.a, P.slots, P.slot_stride, blockIdx.x, n_slot_floats(P), P.status);
                 const int s = it % NST;
                 if (it >= NST && !wait_or_abort(&empty[s], ((it / NST) - 1) & 1, abort_flag, P.status, 0x201)) {
                     ok = false;
@@ -396,7 +402,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x206)) break;
                 tc_fence_after();
             }
-            load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
+            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+                load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
                                 hf, tS + lo, 0u, 0u, Sb, zc, ac, CAUSAL, false);
             fence_proxy_async_smem();
             tc_fence_before();
@@ -412,7 +419,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 const long long row0 = (long long)c * kC;
                 const int nvalid = (int)min((long long)kC, P.N - row0);
                 // this chunk's z_c[i] (half 0) or a_c[i] (half 1), from the sums kernel (causal)
-                const float zav = CAUSAL ? P.chunk_za[((size_t)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i] : 0.f;
+                const long long zi = ((long long)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i;
+                const float zav = CAUSAL && in_range(zi, n_chunk_floats(P), P.status, 0xB004) ? P.chunk_za[zi] : 0.f;
                 float part = 0.f;
                 if (CAUSAL) {
                     // P = [j <= i](1 + T) for this half's columns j; r_i partial sum in fp32
@@ -484,7 +492,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
 #pragma unroll
                     for (int q = 0; q < 4; ++q) *(uint4 *)(otile + sw128_off(i, 4 * half32 + q)) = w[q];
                 }
-                if (row_ok && hf == 0 && P.g) P.g[(size_t)pc.h * P.N + row0 + i] = gi;
+                if (row_ok && hf == 0 && P.g) {
+                    const long long gix = (long long)pc.h * P.N + row0 + i;
+                    if (in_range(gix, n_row_floats(P), P.status, 0xB005)) P.g[gix] = gi;
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 epi_sync256();  // the whole O tile is in shared memory
@@ -566,6 +577,11 @@ __global__ void __launch_bounds__(256, 8) tc_combine_kernel(const __grid_constan
         auto at = [&](int k) -> float4 * {  // k-th slot of the head in the order of the sums
             return base + slot_of(h, mode == kCombineSuffix ? b1 - k : b0 + k) * s4;
         };
+#ifdef LA_CHECKED
+        bool sok = true;  // every slot of the head inside the array (the same for all threads)
+        for (int k = 0; k < n; ++k) sok = sok && slot_ok(P, h, mode == kCombineSuffix ? b1 - k : b0 + k, 0xB006);
+        if (!sok) continue;
+#endif
         float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int g = 0; g < n; g += 4) {  // up to four loads in flight; each slot read before it is written
             float4 v[4];

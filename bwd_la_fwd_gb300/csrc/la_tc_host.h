@@ -42,6 +42,22 @@ struct TcParams {
     int test_drop_load;     // test hook: CTA 0 of the sums kernel issues no load for this iteration (-1: none)
 };
 
+// Extents, in floats, of the workspace arrays that the kernels index themselves (checked in the LA_CHECKED
+// build): a slot array (BH + kMaxCtas slots), the per-chunk column sums, the per-row statistics (and the
+// caller's normaliser, [B,H,N]).
+__host__ __device__ inline long long n_slot_floats(const TcParams &P) {
+    return (P.sl.T / P.sl.nchunk + kMaxCtas) * P.slot_stride;
+}
+__host__ __device__ inline long long n_chunk_floats(const TcParams &P) { return P.sl.T * 256; }
+__host__ __device__ inline long long n_row_floats(const TcParams &P) { return P.sl.T / P.sl.nchunk * P.N; }
+
+// Whether slot (h + b) lies wholly inside its array (and slots do not overlap); LA_CHECKED only.
+__device__ __forceinline__ bool slot_ok(const TcParams &P, long long h, int b, uint32_t where) {
+    const long long base = slot_of(h, b) * P.slot_stride, n = n_slot_floats(P);
+    return in_range(base, n, P.status, where) && in_range(base + kSlotF4 * 4 - 1, n, P.status, where) &&
+           in_range(kSlotF4 * 4 - 1, P.slot_stride, P.status, where);
+}
+
 // Forms of the slot arrays (tc_combine_kernel).
 enum : int { kCombinePrefix = 0, kCombineSuffix = 1, kCombineTotal = 2 };
 // The per-piece sums kernel records in the workspace header which K, V and slicing the slots hold, and

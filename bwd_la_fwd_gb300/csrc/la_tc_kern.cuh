@@ -96,13 +96,17 @@ static __device__ __noinline__ void load_carry_half(const float *slots, long lon
 // Brings into L2 the carry slot of the piece that follows `pi` in the slice, when `remaining` chunks of
 // the current piece are still to be issued (two, or all of a shorter piece).  The slots were written by
 // an earlier kernel and the walks stream far more than L2 holds.  One thread (the TMA producer).
+// `nfloats`: the slot array's extent (LA_CHECKED: a slot outside it is not prefetched).
 __device__ __forceinline__ void prefetch_next_carry(const PieceIter &pi, int remaining, int piece_len,
-                                                    const float *slots, long long stride, int b) {
+                                                    const float *slots, long long stride, int b, long long nfloats,
+                                                    uint32_t *status) {
     if (remaining != (piece_len > 2 ? 2 : piece_len - 1)) return;
     PieceIter pn = pi;
     pn.next();
-    if (pn.valid())
-        bulk_prefetch_l2(slots + slot_of(pn.get().h, b) * stride, (uint32_t)(kSlotF4 * sizeof(float4)));
+    if (!pn.valid()) return;
+    const long long base = slot_of(pn.get().h, b) * stride;
+    if (in_range(base, nfloats, status, 0xB0F1) && in_range(base + kSlotF4 * 4 - 1, nfloats, status, 0xB0F1))
+        bulk_prefetch_l2(slots + base, (uint32_t)(kSlotF4 * sizeof(float4)));
 }
 
 // Row d's 64 columns [64 hf, 64 hf + 64) of an fp32 TMEM block, rounded into box hf of a bf16 operand tile.

@@ -364,10 +364,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                 const long long row0 = (long long)c * kC;
                 const bool row_ok = row0 + i < P.N;
                 const size_t rix = (size_t)h * P.N + (row_ok ? row0 + i : 0);
+                const bool rix_ok = in_range((long long)rix, (long long)P.BH * P.N, P.status, 0xB010);
                 float u = 1.f;  // query-side constant of row i
-                if (MODE == kWDq) u = row_ok ? -P.rs_dt[rix] : 0.f;
+                if (MODE == kWDq) u = row_ok && rix_ok ? -P.rs_dt[rix] : 0.f;
                 if (KCONST) {  // key-side constants of the chunk's rows (the previous chunk's MMAs read theirs: barO)
-                    if (hf == 0) weight_put(wtile, i, row_ok ? -P.rs_dt[rix] : 0.f);
+                    if (hf == 0) weight_put(wtile, i, row_ok && rix_ok ? -P.rs_dt[rix] : 0.f);
                     fence_proxy_async_smem();
                     epi_sync256();
                 }
@@ -417,8 +418,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_kernel(const __gr
                     gi = (float)row0 + __uint_as_float(x0) + __uint_as_float(x1);
                     inv = 1.f / gi;
                     if (row_ok && hf == 0) {
-                        if (P.g_out) P.g_out[rix] = gi;
-                        if (MODE == kWFwd && P.g_ws) P.g_ws[rix] = gi;
+                        if (P.g_out && rix_ok) P.g_out[rix] = gi;
+                        if (MODE == kWFwd && P.g_ws && rix_ok) P.g_ws[rix] = gi;
                     }
                 }
                 ok = wait_or_abort(barO, ph, abort_flag, P.status, 0x511);
@@ -698,7 +699,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
                     if (nA > 0) ok = wait_or_abort(emptyA, (nA - 1) & 1, abort_flag, P.status, 0x541);
                     if (!ok) break;
                     const long long r = (long long)k * kC + i;
-                    if (hf == 0) weight_put(wtile, i, r < P.N ? -P.rs_dt[(size_t)h * P.N + r] : 0.f);
+                    if (hf == 0) {
+                        const long long x = (long long)h * P.N + r;
+                        weight_put(wtile, i, r < P.N && in_range(x, (long long)P.BH * P.N, P.status, 0xB011)
+                                                 ? -P.rs_dt[x] : 0.f);
+                    }
                     fence_proxy_async_smem();
                     mbar_arrive(barW);
                 }
@@ -737,9 +742,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
                 const long long row0 = (long long)k * kC;
                 const bool row_ok = row0 + i < P.N;
                 const size_t rix = (size_t)h * P.N + (row_ok ? row0 + i : 0);
+                const bool rix_ok = in_range((long long)rix, (long long)P.BH * P.N, P.status, 0xB010);
                 unsigned char *xs = region + s * XB;
                 float u = 1.f;
-                if (MODE == kWDq) u = row_ok ? -P.rs_dt[rix] : 0.f;
+                if (MODE == kWDq) u = row_ok && rix_ok ? -P.rs_dt[rix] : 0.f;
                 float inv = 1.f;
                 if (NORM) {  // g_i = N + q_i . z, halves exchanged through two TMEM columns
                     ok = wait_or_abort(&fullB[s], phs, abort_flag, P.status, 0x543);
@@ -757,8 +763,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_wide_nc_kernel(const _
                     const float gi = (float)P.N + __uint_as_float(x0) + __uint_as_float(x1);
                     inv = 1.f / gi;
                     if (row_ok && hf == 0) {
-                        if (P.g_out) P.g_out[rix] = gi;
-                        if (MODE == kWFwd && P.g_ws) P.g_ws[rix] = gi;
+                        if (P.g_out && rix_ok) P.g_out[rix] = gi;
+                        if (MODE == kWFwd && P.g_ws && rix_ok) P.g_ws[rix] = gi;
                     }
                 }
                 if (HAS_W) {
@@ -857,7 +863,7 @@ __global__ void __launch_bounds__(256) wide_rowstats_kernel(const __nv_bfloat16 
         const long long b = bh / H, h = bh - b * H;
         a[k] = *(const uint4 *)(dO + b * ldo.sb + h * ldo.sh + n * ldo.sn + 8 * lane);
         o[k] = *(const uint4 *)(O + b * lo.sb + h * lo.sh + n * lo.sn + 8 * lane);
-        gi[k] = g[r];
+        gi[k] = in_range(r, rows, status, 0xB012) ? g[r] : 1.f;
     }
 #pragma unroll
     for (int k = 0; k < kRowsPerWarp; ++k) {
@@ -870,7 +876,7 @@ __global__ void __launch_bounds__(256) wide_rowstats_kernel(const __nv_bfloat16 
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-        if (r0 + k >= rows) continue;
+        if (r0 + k >= rows || !in_range(r0 + k, rows, status, 0xB012)) continue;
         const float ig = 1.f / gi[k];
         if (lane == 0) dt[r0 + k] = d * ig;
         uint4 sc;

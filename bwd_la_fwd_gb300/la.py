@@ -42,39 +42,45 @@ def load_library():
         if not os.path.exists(path):
             raise RuntimeError(f"CUDA library {path} is missing: run `python -m bwd_la_fwd_gb300.build` "
                                "(or __graft_entry__.build()); there is no CPU fallback")
-        lib = ctypes.CDLL(path)
-        vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
-        lib.la_version.argtypes = []
-        lib.la_version.restype = i
-        lib.la_launch_count.argtypes = []
-        lib.la_launch_count.restype = ctypes.c_ulonglong
-        lib.la_status_string.argtypes = [i]
-        lib.la_status_string.restype = ctypes.c_char_p
-        lib.la_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
-        lib.la_workspace_bytes.restype = sz
-        lib.la_forward.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, sz, vp]
-        lib.la_forward.restype = i
-        lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
-        lib.la_backward.restype = i
-        lib.la_backward_with_forward_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
-        lib.la_backward_with_forward_state.restype = i
-        lp = ctypes.POINTER(ctypes.c_longlong)
-        lib.la_forward_strided.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, lp, vp, sz, vp]
-        lib.la_forward_strided.restype = i
-        lib.la_backward_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, i, vp, sz, vp]
-        lib.la_backward_strided.restype = i
-        lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
-        lib.la_decode_step.restype = i
-        lib.la_state_append.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
-        lib.la_state_append.restype = i
-        lib.la_get_status.argtypes = [vp, vp]
-        lib.la_get_status.restype = i
-        lib.la_forward_noalloc.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp]
-        lib.la_forward_noalloc.restype = i
-        lib.la_noalloc_get_status.argtypes = [vp]
-        lib.la_noalloc_get_status.restype = i
-        _lib = lib
-        return lib
+        _lib = open_library(path)
+        return _lib
+
+
+def open_library(path: str):
+    """A ctypes handle on a build of the library at `path`, with every entry point's C signature set
+    (load_library() opens the product build with it; the tests also open the index-checked build)."""
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.la_version.argtypes = []
+    lib.la_version.restype = i
+    lib.la_launch_count.argtypes = []
+    lib.la_launch_count.restype = ctypes.c_ulonglong
+    lib.la_status_string.argtypes = [i]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    lib.la_workspace_bytes.restype = sz
+    lib.la_forward.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp, sz, vp]
+    lib.la_forward.restype = i
+    lib.la_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+    lib.la_backward.restype = i
+    lib.la_backward_with_forward_state.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, sz, vp]
+    lib.la_backward_with_forward_state.restype = i
+    lp = ctypes.POINTER(ctypes.c_longlong)
+    lib.la_forward_strided.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, lp, vp, sz, vp]
+    lib.la_forward_strided.restype = i
+    lib.la_backward_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, lp, i, vp, sz, vp]
+    lib.la_backward_strided.restype = i
+    lib.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
+    lib.la_decode_step.restype = i
+    lib.la_state_append.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.la_state_append.restype = i
+    lib.la_get_status.argtypes = [vp, vp]
+    lib.la_get_status.restype = i
+    lib.la_forward_noalloc.argtypes = [vp, vp, vp, i, vp, vp, i, i, i, i, i, vp]
+    lib.la_forward_noalloc.restype = i
+    lib.la_noalloc_get_status.argtypes = [vp]
+    lib.la_noalloc_get_status.restype = i
+    return lib
 
 
 def la_status_string(status: int) -> str:

@@ -36,6 +36,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_index_checked_build_exports_the_same_symbols():
+    """The LA_CHECKED test build (index checks in the tensor-core kernels) is built from the same sources
+    and exposes the same boundary."""
+    from bwd_la_fwd_gb300 import build, la
+    checked = la.open_library(build.build(checked=True))
+    for name in declared_functions():
+        assert ctypes.cast(getattr(checked, name), ctypes.c_void_p).value, name
+    assert checked.la_version() == la.load_library().la_version()
+
+
 def test_version_and_status_strings(lib):
     assert lib.la_version() >= 100
     for code, name in [(0, "LA_OK"), (1, "LA_ERR_INVALID_ARG"), (2, "LA_ERR_UNSUPPORTED"),

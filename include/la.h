@@ -57,7 +57,9 @@ typedef enum {
     LA_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
     LA_ERR_TIMEOUT = 5,     /* device: a bounded barrier wait inside a kernel gave up (reported by la_get_status) */
     LA_ERR_BOUNDS = 6,      /* device: an internal layout check failed -- a kernel's shared-memory window was not
-                               1024-byte aligned, so it computed nothing (reported by la_get_status) */
+                               1024-byte aligned, so it computed nothing; or, in the index-checked test build
+                               (libla_gb300_checked.so), an index out of its array was skipped (reported by
+                               la_get_status) */
     LA_ERR_STATE = 7        /* device: la_backward_with_forward_state found no matching forward state */
 } la_status;
 

@@ -682,8 +682,7 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
     if (nsm <= 0) return false;
     P.sl.nchunk = (p.N + tc::kC - 1) / tc::kC;
     P.sl.T = (long long)p.BH * P.sl.nchunk;
-    long long G = P.sl.T < nsm ? P.sl.T : nsm;
-    if (G > tc::kMaxCtas) G = tc::kMaxCtas;
+    long long G = tc::choose_ctas(p.BH, P.sl.nchunk, nsm, p.causal != 0, p.D == 128);
     // Test hook: fewer CTAs, so that small problems also exercise multi-chunk, multi-head slices.
     if (const char *env = getenv("LA_TC_MAX_CTAS")) {
         const long long cap = atoll(env);

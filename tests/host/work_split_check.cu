@@ -1,7 +1,8 @@
 // Host-side brute force over the tensor-core kernels' work split (la_tc_common.cuh), run on the CPU:
 // slices tile the chunk list, cta_of inverts them, pieces stay within one head and cover each slice in
-// order, and the per-piece state slots never collide and fit the workspace's BH + kMaxCtas slots.
-// Prints "ok <cases>" and exits 0, or prints the first failing case and exits 1.
+// order, and the per-piece state slots never collide and fit the workspace's BH + kMaxCtas slots; the
+// grid that choose_ctas picks stays within bounds, and where it departs from the default every slice is
+// one piece of one head.  Prints "ok <cases>" and exits 0, or prints the first failing case and exits 1.
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -98,6 +99,38 @@ int main() {
             return 1;
         }
     }
+    // choose_ctas: within [1, min(T, nsm, kMaxCtas)]; narrow heads get the default; where it departs from
+    // the default, every slice is one piece (nchunk / k chunks of one head) and the split itself is valid
+    for (long long BH = 1; BH <= 300; BH += (BH < 40 ? 1 : 7))
+        for (int nchunk = 1; nchunk <= 600; nchunk += (nchunk < 40 ? 1 : 13))
+            for (int nsm : {152, 148, 132, 8})
+                for (int causal = 0; causal < 2; ++causal)
+                    for (int full = 0; full < 2; ++full, ++cases) {
+                        const long long T = BH * nchunk;
+                        long long def = T < nsm ? T : nsm;
+                        if (def > kMaxCtas) def = kMaxCtas;
+                        const long long G = choose_ctas(BH, nchunk, nsm, causal != 0, full != 0);
+                        bool bad = G < 1 || G > def || (!full && G != def);
+                        if (!bad && G != def) {
+                            Slices s;
+                            s.T = T;
+                            s.G = (int)G;
+                            s.nchunk = nchunk;
+                            bad = check(BH, nchunk, (int)G) != 0 || (T % G) != 0 || (nchunk % (T / G)) != 0;
+                            for (int b = 0; b < G && !bad; ++b) {
+                                int pieces = 0;
+                                for (PieceIter pi(s, b); pi.valid(); pi.next()) ++pieces;
+                                bad = pieces != 1;
+                            }
+                            // no more than one (causal) or two (non-causal) chunks per CTA above the default
+                            bad = bad || (T / G) - (T + def - 1) / def > (causal ? 1 : 2);
+                        }
+                        if (bad) {
+                            printf("choose_ctas fails: BH=%lld nchunk=%d nsm=%d causal=%d full=%d G=%lld\n", BH, nchunk,
+                                   nsm, causal, full, G);
+                            return 1;
+                        }
+                    }
     printf("ok %lld\n", cases);
     return 0;
 }

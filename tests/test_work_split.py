@@ -1,7 +1,7 @@
 """The tensor-core kernels' work split, checked on the CPU: `tests/host/work_split_check.cu` includes the
-kernels' own `la_tc_common.cuh` (slices, chunk owner, pieces, slot numbering and slot layout), is compiled
-by nvcc as a host program and brute-forces their invariants over every small shape and 3000 random large
-ones.  No GPU is used."""
+kernels' own `la_tc_common.cuh` (slices, chunk owner, pieces, slot numbering and slot layout, the grid
+size choice), is compiled by nvcc as a host program and brute-forces their invariants over every small
+shape and 3000 random large ones.  No GPU is used."""
 import os
 import shutil
 import subprocess

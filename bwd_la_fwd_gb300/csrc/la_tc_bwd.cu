@@ -184,14 +184,15 @@ __device__ __forceinline__ void dt_tile_put(unsigned char *dtt, int i, float dt)
 }
 
 // The chunk walked after chunk c of piece pc when each piece is walked in reverse: c - 1 in the piece,
-// else the last chunk of the slice's next piece.  False when c is the slice's last.
-__device__ __forceinline__ bool next_rev_chunk(const PieceIter &pi, const Piece &pc, int c, long long *h, int *cn) {
+// else the last chunk of the piece that `pi` yields next.  False when c is the last chunk walked.
+template <typename Iter>
+__device__ __forceinline__ bool next_rev_chunk(const Iter &pi, const Piece &pc, int c, long long *h, int *cn) {
     if (c > pc.a) {
         *h = pc.h;
         *cn = c - 1;
         return true;
     }
-    PieceIter pn = pi;
+    Iter pn = pi;
     pn.next();
     if (!pn.valid()) return false;
     const Piece q = pn.get();
@@ -429,7 +430,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
             const Piece pc = pi.get();
             // forward state carried into the piece, from the head's earlier pieces (the previous
             // piece's MMAs on R2 are complete: its last barX has been waited for)
-            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+            if (pc.a == 0)  // the head's first piece: nothing before it
+                zero_carry_half(i, hf, R2 + lo, Sb, zc, ac, true);
+            else if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
                 load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i, hf, R2 + lo, 0u, 0u,
                                 Sb, zc, ac, true, false);
             fence_proxy_async_smem();
@@ -814,7 +817,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
 }
 
 // ----------------------------------------------------------------------------------------------------
-// dK / dV walk (reverse chunk order), causal, with lane = key row j of the chunk.  Per chunk:
+// dK / dV walk (reverse chunk order: the slice's pieces last first, each piece's chunks last first),
+// causal, with lane = key row j of the chunk.  Per chunk:
 //   the epilogue first rewrites dO as dOt = dO / g in place (g_i, dt_i and the chunk's column sums
 //   y_c, e_c come from the dQ walk and are loaded one chunk ahead); T^T = K Q^T (R0) and
 //   Wt^T = V dOt^T (R1); P^T = [i >= j](1 + T^T) as soon as T^T is in, and U^T = [i >= j](Wt^T - dt_i)
@@ -898,14 +902,14 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         prefetch_tmap(&P.tmK);
         prefetch_tmap(&P.tmV);
         {  // the first piece's carry slot
-            PieceIter p0(P.sl, blockIdx.x);
+            RevPieceIter p0(P.sl, blockIdx.x);
             if (p0.valid() && slot_ok(P, p0.get().h, blockIdx.x, 0xB0F0))
                 bulk_prefetch_l2(P.slots_rev + slot_of(p0.get().h, blockIdx.x) * P.slot_stride,
                                  (uint32_t)(kSlotF4 * sizeof(float4)));
         }
         int it = 0;
         bool ok = true;
-        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+        for (RevPieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             const HeadCoord hc = head_coord<FLAT>(pc.h, P.H);
             for (int c = pc.e - 1; c >= pc.a; --c, ++it) {
@@ -944,7 +948,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         const uint32_t qb = smem_u32(stage), ob = qb + TB, kb = qb + 2 * TB, vb = qb + 3 * TB;
         int it = 0;
         bool ok = true;
-        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+        for (RevPieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             for (int c = pc.e - 1; c >= pc.a && ok; --c, ++it) {
                 const uint32_t ph = it & 1;
@@ -1007,7 +1011,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         // g_j, dt_j and component j of y_c (half 0) or e_c (half 1) for the next chunk to be walked
         float ng = 0.f, ndt = 0.f, nye = 0.f;
         {
-            PieceIter p0(P.sl, blockIdx.x);
+            RevPieceIter p0(P.sl, blockIdx.x);
             if (p0.valid()) {
                 const Piece q = p0.get();
                 load_chunk_stats(P, q.h, q.e - 1, j, hf, &ng, &ndt, &nye);
@@ -1015,11 +1019,15 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
         }
         int it = 0;
         bool ok = true;
-        for (PieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
+        for (RevPieceIter pi(P.sl, blockIdx.x); pi.valid() && ok; pi.next()) {
             const Piece pc = pi.get();
             // carried reverse sums (the later pieces of the head); the previous piece's MMAs on R3 and Pb are
-            // complete (its last barV)
-            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+            // complete (its last barV).  The slice's pieces are walked last first, so that where a slice
+            // straddles two heads the piece change leads into the earlier head's last piece, whose carry is
+            // zero and needs no load.
+            if (pc.e == P.sl.nchunk)
+                zero_carry_half(j, hf, R3 + lo, Pb, yc, ec, true);
+            else if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
                 load_carry_half(P.slots_rev, P.slot_stride, pc.h, blockIdx.x, j, hf, R3 + lo, 0u,
                                 0u, Pb, yc, ec, true, false);
             fence_proxy_async_smem();

@@ -101,6 +101,27 @@ struct PieceIter {
     }
 };
 
+// The same pieces in reverse: the slice's last piece first (its chunks [a, e) as above).
+struct RevPieceIter {
+    long long lo, x;
+    int nchunk;
+    __host__ __device__ __forceinline__ RevPieceIter(const Slices &s, int b)
+        : lo(slice_lo(s, b)), x(slice_lo(s, b + 1)), nchunk(s.nchunk) {}
+    __host__ __device__ __forceinline__ bool valid() const { return x > lo; }
+    __host__ __device__ __forceinline__ Piece get() const {
+        Piece p;
+        p.h = (x - 1) / nchunk;
+        const long long hs = p.h * nchunk;
+        p.a = (int)((lo > hs ? lo : hs) - hs);
+        p.e = (int)(x - hs);
+        return p;
+    }
+    __host__ __device__ __forceinline__ void next() {
+        const Piece p = get();
+        x = p.h * nchunk + p.a;
+    }
+};
+
 // Records the first device-side error in the workspace status word (first error wins).
 __device__ __forceinline__ void report(uint32_t *status, uint32_t code, uint32_t where) {
     if (atomicCAS(status, 0u, code) == 0u) status[1] = where;

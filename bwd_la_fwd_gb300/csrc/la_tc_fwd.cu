@@ -402,7 +402,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                 if (!wait_or_abort(barS, (it - 1) & 1, abort_flag, P.status, 0x206)) break;
                 tc_fence_after();
             }
-            if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
+            if (CAUSAL && pc.a == 0)  // the head's first piece: nothing before it
+                zero_carry_half(i, hf, tS + lo, Sb, zc, ac, true);
+            else if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
                 load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
                                 hf, tS + lo, 0u, 0u, Sb, zc, ac, CAUSAL, false);
             fence_proxy_async_smem();

@@ -93,15 +93,34 @@ static __device__ __noinline__ void load_carry_half(const float *slots, long lon
     if (to_tmem) tmem_st_wait();
 }
 
+// The same for a piece whose carried state is zero by definition (a causal piece that starts its head
+// walking forward, or ends it walking in reverse): zeros instead of a slot read.
+static __device__ __noinline__ void zero_carry_half(int d, int hf, uint32_t tS, unsigned char *Sb, float *zc,
+                                                float *ac, bool to_tmem) {
+    if (to_tmem) {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0u;
+        tmem_st32(tS + 64 * hf, r);
+        tmem_st32(tS + 64 * hf + 32, r);
+    }
+    unsigned char *tile = Sb + hf * kBox;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) *(uint4 *)(tile + sw128_off(d, g8)) = make_uint4(0u, 0u, 0u, 0u);
+    (hf == 0 ? zc : ac)[d] = 0.f;
+    if (to_tmem) tmem_st_wait();
+}
+
 // Brings into L2 the carry slot of the piece that follows `pi` in the slice, when `remaining` chunks of
 // the current piece are still to be issued (two, or all of a shorter piece).  The slots were written by
 // an earlier kernel and the walks stream far more than L2 holds.  One thread (the TMA producer).
 // `nfloats`: the slot array's extent (LA_CHECKED: a slot outside it is not prefetched).
-__device__ __forceinline__ void prefetch_next_carry(const PieceIter &pi, int remaining, int piece_len,
+template <typename Iter>
+__device__ __forceinline__ void prefetch_next_carry(const Iter &pi, int remaining, int piece_len,
                                                     const float *slots, long long stride, int b, long long nfloats,
                                                     uint32_t *status) {
     if (remaining != (piece_len > 2 ? 2 : piece_len - 1)) return;
-    PieceIter pn = pi;
+    Iter pn = pi;
     pn.next();
     if (!pn.valid()) return;
     const long long base = slot_of(pn.get().h, b) * stride;

@@ -1,6 +1,6 @@
 // Host-side brute force over the tensor-core kernels' work split (la_tc_common.cuh), run on the CPU:
 // slices tile the chunk list, cta_of inverts them, pieces stay within one head and cover each slice in
-// order, and the per-piece state slots never collide and fit the workspace's BH + kMaxCtas slots; the
+// order (RevPieceIter gives them back last first), and the per-piece state slots never collide and fit the workspace's BH + kMaxCtas slots; the
 // grid that choose_ctas picks stays within bounds, and where it departs from the default every slice is
 // one piece of one head.  Prints "ok <cases>" and exits 0, or prints the first failing case and exits 1.
 #include <stdio.h>
@@ -47,6 +47,15 @@ static int check(long long BH, int nchunk, int G) {
             slot_used[(size_t)slot] = 1;
         }
         if (expect != slice_lo(s, b + 1)) return 8;
+        // RevPieceIter yields the same pieces, last first
+        std::vector<Piece> fwd, rev;
+        for (PieceIter pi(s, b); pi.valid(); pi.next()) fwd.push_back(pi.get());
+        for (RevPieceIter pi(s, b); pi.valid(); pi.next()) rev.push_back(pi.get());
+        if (fwd.size() != rev.size()) return 12;
+        for (size_t k = 0; k < fwd.size(); ++k) {
+            const Piece &f = fwd[fwd.size() - 1 - k], &r = rev[k];
+            if (f.h != r.h || f.a != r.a || f.e != r.e) return 13;
+        }
     }
     if (covered != s.T) return 9;
     // the CTAs that cover a head are contiguous, from cta_of(first chunk) to cta_of(last chunk)

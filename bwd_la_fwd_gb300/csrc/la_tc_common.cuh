@@ -33,11 +33,12 @@ __host__ __device__ __forceinline__ long long slice_lo(const Slices &s, int b) {
 
 // CTAs for BH heads of nchunk chunks on nsm SMs.  By default every SM gets a slice, G = min(T, nsm)
 // (at most kMaxCtas); slices then straddle head boundaries, and a CTA whose slice does pays a fixed cost
-// where its pieces change (the carried state loaded, the pipeline drained and refilled), measured at
-// about one chunk of a causal walk and two of a non-causal walk.  When BH k CTAs fit for a divisor k of
-// nchunk, every slice is nchunk / k chunks of one head; for full-width heads (D = 128, whose walks share
-// the HBM bandwidth, so that fewer CTAs lose little) that split is taken when it gives a CTA at most
-// that many chunks more than the default.  Narrow heads (D = 32, 64: a half or a quarter of the bytes per
+// where its pieces change (the pipeline drained and refilled, the carried state loaded), measured at
+// less than one chunk of a causal walk (whose piece changes lead into a zero carry, with no load) and
+// about two of a non-causal walk.  When BH k CTAs fit for a divisor k of nchunk, every slice is
+// nchunk / k chunks of one head; for full-width heads (D = 128, whose walks share the HBM bandwidth, so
+// that fewer CTAs lose little) that split is taken when it gives a CTA no more chunks than the default
+// (causal) or at most two more (non-causal).  Narrow heads (D = 32, 64: a half or a quarter of the bytes per
 // chunk) measured slower with fewer CTAs and keep the default.  The forward and the backward of one
 // mask choose alike.
 __host__ __device__ inline long long choose_ctas(long long BH, int nchunk, int nsm, bool causal, bool full_width) {
@@ -49,7 +50,7 @@ __host__ __device__ inline long long choose_ctas(long long BH, int nchunk, int n
     for (long long k = nchunk; k >= 1; --k) {  // the largest k that divides nchunk with BH k <= G
         if (nchunk % k != 0 || BH * k > G) continue;
         const long long extra = nchunk / k - (T + G - 1) / G;
-        if (BH * k != G && extra <= (causal ? 1 : 2)) G = BH * k;
+        if (BH * k != G && extra <= (causal ? 0 : 2)) G = BH * k;
         break;
     }
     return G;

@@ -131,8 +131,8 @@ int main() {
                                 for (PieceIter pi(s, b); pi.valid(); pi.next()) ++pieces;
                                 bad = pieces != 1;
                             }
-                            // no more than one (causal) or two (non-causal) chunks per CTA above the default
-                            bad = bad || (T / G) - (T + def - 1) / def > (causal ? 1 : 2);
+                            // no more chunks per CTA than the default (causal), at most two more (non-causal)
+                            bad = bad || (T / G) - (T + def - 1) / def > (causal ? 0 : 2);
                         }
                         if (bad) {
                             printf("choose_ctas fails: BH=%lld nchunk=%d nsm=%d causal=%d full=%d G=%lld\n", BH, nchunk,

@@ -76,7 +76,8 @@ def test_workspace_sizes(lib):
 def test_narrow_bf16_heads_take_the_tensor_core_workspace(lib):
     """bf16 with D = 32, 64 runs on the D = 128 tensor-core kernels (columns past D zero-extended): its
     workspace is the D = 128 one (state slots of 128 x 128 + 2 x 128 floats, per-row and per-chunk sums),
-    for any B, H, N and either mask; bf16 D = 16, 256 and fp32 are sized by their own D (CUDA-core path)."""
+    for any B, H, N and either mask; bf16 D = 256 takes the wide kernels' layout, bf16 D = 16 and fp32 are
+    sized by their own D (CUDA-core path)."""
     ws = lib.la_workspace_bytes
     for B, H, N in ((1, 1, 1), (2, 3, 549), (4, 16, 4096)):
         for causal in (0, 1):

@@ -1373,7 +1373,7 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     if (!reuse_fwd_state) {
         e = tc_host::launch_agg(P, s);
         ++launches;
-        if (e == cudaSuccess) {
+        if (e == cudaSuccess && !P.whole_heads) {
             e = tc_host::launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal,
                                         p.causal ? tc::kTagPrefix : tc::kTagTotals, s);
             ++launches;
@@ -1386,7 +1386,7 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
                                           P.sl.G, nthr, kSmemDqNc, s, P);
         ++launches;
     }
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && !P.whole_heads) {  // whole heads: each piece's reverse sums are its head's totals
         e = tc_host::launch_combine(P, P.slots_rev, p.causal ? tc::kCombineSuffix : tc::kCombineTotal, 0, s);
         ++launches;
     }

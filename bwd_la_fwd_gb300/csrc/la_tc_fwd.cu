@@ -84,7 +84,12 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0) write_state_tag(P, kTagRaw);  // the slots below belong to P.Kp, P.Vp (until combined)
+    // the slots below belong to P.Kp, P.Vp: each piece's own sums (until combined), or with whole_heads the
+    // heads' totals; they are new, so no backward has used them
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        write_state_tag(P, P.whole_heads ? kTagTotals : kTagRaw);
+        *fwd_sums_used(P) = 0u;
+    }
     const uint32_t tmem = *tslot;
 
     if (warp == 0 && lane == 0) {
@@ -691,6 +696,8 @@ bool fill_common(tc::TcParams &P, const Plan &p, unsigned char *ws) {
         if (cap >= 1 && cap < G) G = cap;
     }
     P.sl.G = (int)G;
+    // non-causal, every slice one whole head: the sums kernel's piece sums are already the heads' totals
+    P.whole_heads = !p.causal && G == p.BH && P.sl.T % G == 0 && P.sl.T / G == P.sl.nchunk ? 1 : 0;
     // Test hooks for the failure path: a shorter bound on barrier waits, and one load of the sums kernel
     // that is never issued, so that a wait runs out and the kernels take their abort path.
     P.wait_ns = 0;
@@ -772,7 +779,7 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     P.Kp = K;
     P.Vp = V;
     cudaError_t e = launch_agg(P, s);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !P.whole_heads)  // whole heads: the sums kernel has written the totals
         e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal,
                            p.causal ? tc::kTagPrefix : tc::kTagTotals, s);
     if (e == cudaSuccess)
@@ -780,7 +787,7 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
                                  64 + tc::kEpiThreads, kSmemFwdCausal, s, P)
                      : launch_tc(flat ? tc::tc_fwd_kernel<false, true> : tc::tc_fwd_kernel<false, false>, P.sl.G,
                                  64 + tc::kEpiThreads, kSmemFwdNonCausal, s, P);
-    if (e == cudaSuccess) count_launches(3);
+    if (e == cudaSuccess) count_launches(P.whole_heads ? 2 : 3);
     return e;
 }
 

@@ -40,6 +40,8 @@ struct TcParams {
     uint64_t combine_tag;   // tc_combine_kernel: the form to record in the workspace tag (0: leave the tag)
     uint64_t wait_ns;       // bound on a single barrier wait (0: the default, tc::kWaitNs)
     int test_drop_load;     // test hook: CTA 0 of the sums kernel issues no load for this iteration (-1: none)
+    int whole_heads;        // non-causal, every slice exactly one head: its piece sums are the head's totals,
+                            // and no tc_combine_kernel runs
 };
 
 // Extents, in floats, of the workspace arrays that the kernels index themselves (checked in the LA_CHECKED

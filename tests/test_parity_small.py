@@ -105,6 +105,34 @@ def test_path_taken(dtype, D, launches):
     assert la.la_launch_count() - n0 == launches
 
 
+@pytest.mark.parametrize("N,whole", [(128, True), (256, False)])
+def test_noncausal_whole_heads_need_no_combine(oracle_lib, N, whole):
+    """Non-causal, bf16 D = 128, B = 1, H = 2: with one chunk per CTA, a head of one chunk is one CTA's
+    whole slice, so its piece sums are the head's totals and no combine kernel runs (forward 2 launches,
+    backward 3, reusing backward 2); a head of two chunks spans two CTAs and takes the combine (3, 5, 3).
+    Both agree with the oracle, and the reusing backward with the plain one bit for bit."""
+    import torch
+    from bwd_la_fwd_gb300 import la
+    x = inputs.generate(1, 2, N, 128, 5, dtype="bf16")
+    Q, K, V, dO = (U.to_device(x[n], "bf16") for n in ("Q", "K", "V", "dO"))
+    ws = la.new_workspace(1, 2, N, 128, False, la.LA_BF16, True)
+    n0 = la.la_launch_count()
+    O, g = la.la_forward(Q, K, V, False, workspace=ws)
+    n1 = la.la_launch_count()
+    plain = la.la_backward(Q, K, V, O, dO, False, workspace=ws)
+    n2 = la.la_launch_count()
+    la.la_forward(Q, K, V, False, O=O, workspace=ws)
+    n3 = la.la_launch_count()
+    reuse = la.la_backward(Q, K, V, O, dO, False, workspace=ws, reuse_forward_state=True)
+    n4 = la.la_launch_count()
+    torch.cuda.synchronize()
+    assert la.la_get_status(ws) == 0
+    assert (n1 - n0, n2 - n1, n4 - n3) == ((2, 3, 2) if whole else (3, 5, 3))
+    for a, b in zip(plain, reuse):
+        assert torch.equal(a, b)
+    _check(oracle_lib, 1, 2, N, 128, "bf16", False, seed=5)
+
+
 def test_repeatable_and_workspace_reusable():
     """Two calls on one workspace give bit-identical results (no state leaks between calls)."""
     import torch

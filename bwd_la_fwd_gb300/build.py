@@ -4,10 +4,10 @@ Every ``csrc/*.cu`` file is compiled for sm_103a only (``-gencode arch=compute_1
 parallel, then linked into ``bwd_la_fwd_gb300/libla_gb300.so``.  No CMake, no torch extension
 machinery: the library is a plain C-ABI shared object.
 
-``checked=True`` builds the same sources with ``-DLA_CHECKED`` into ``libla_gb300_checked.so``: in the
-tensor-core kernels every global-memory index that a thread computes itself is checked against its
-array's extent, and a violation is recorded as LA_ERR_BOUNDS in the workspace status word instead of
-being performed.  It is a test build (the product loads ``libla_gb300.so``).
+``checked=True`` builds the same sources with ``-DLA_CHECKED`` into ``libla_gb300_checked.so``: every
+global-memory index that a kernel computes itself for a workspace array or the normaliser is checked
+against the array's extent, and a violation is recorded as LA_ERR_BOUNDS in the workspace status word
+instead of being performed.  It is a test build (the product loads ``libla_gb300.so``).
 """
 from __future__ import annotations
 

@@ -65,7 +65,29 @@ struct Args {
     long long BHN;
     long long stride;
     int nseg, seg_len, causal;
+    uint32_t *status;        // workspace status word
+    long long n_states;      // extents of the workspace arrays, in accumulator elements (checked in the
+    long long n_rows;        // LA_CHECKED build): states, rs_g / rs_delta, rs_dpart
+    long long n_dpart;
 };
+
+// Index check of the LA_CHECKED build for the workspace arrays these kernels index themselves: an index
+// outside [0, n) records LA_ERR_BOUNDS (6) with the place `where` in the status word, and the caller skips
+// the access (a load reads a neutral value).  The operands' element offsets come from layouts that the host
+// checked against their extents.  In the normal build the check is the constant true.
+__device__ __forceinline__ bool ws_ok(uint32_t *status, long long i, long long n, uint32_t where) {
+#ifdef LA_CHECKED
+    if (i >= 0 && i < n) return true;
+    if (atomicCAS(status, 0u, 6u) == 0u) status[1] = where;
+    return false;
+#else
+    (void)status;
+    (void)i;
+    (void)n;
+    (void)where;
+    return true;
+#endif
+}
 
 // Element offset of flat head bh = b H + h of an operand with layout l.
 __device__ __forceinline__ long long head_off(const Layout &l, long long bh, long long H) {
@@ -106,9 +128,11 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
     for (long long b0 = r0; b0 < r1; b0 += C::RB) {
         const int nb = (int)min((long long)C::RB, r1 - b0);
         if (AM == kAggRev && t < nb) {
-            const Acc gi = rs_g[bh * a.N + b0 + t];
+            const long long x = bh * a.N + b0 + t;
+            const bool in = ws_ok(a.status, x, a.n_rows, 0xC001);
+            const Acc gi = in ? rs_g[x] : Acc(1);
             sSc[t] = Acc(1) / gi;
-            sDt[t] = rs_delta[bh * a.N + b0 + t] / gi;
+            sDt[t] = in ? rs_delta[x] / gi : Acc(0);
         }
         if (AM == kAggRev) __syncthreads();
         for (int idx = t; idx < C::RB * D; idx += kThreads) {
@@ -140,7 +164,11 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
         }
         __syncthreads();
     }
-    Acc *st = (Acc *)a.states + (bh * a.nseg + s) * a.stride;
+    const long long sbase = (bh * a.nseg + s) * a.stride;
+    if (!ws_ok(a.status, sbase, a.n_states, 0xC002) ||
+        !ws_ok(a.status, sbase + (long long)D * D + 2 * D - 1, a.n_states, 0xC002))
+        return;
+    Acc *st = (Acc *)a.states + sbase;
 #pragma unroll
     for (int m = 0; m < C::RPT; ++m) st[(long long)(p + C::NP * m) * D + colg] = X[m];
     if (blockIdx.y == 0 && t < D) {
@@ -158,10 +186,14 @@ __global__ void __launch_bounds__(kThreads) simt_aggregate(Args a) {
 // ------------------------------------------------------------------------------------------------
 template <typename Acc>
 __global__ void __launch_bounds__(kThreads) simt_scan(Acc *states, int nseg, long long stride, long long used,
-                                                      int causal, int reverse) {
+                                                      int causal, int reverse, uint32_t *status,
+                                                      long long n_states) {
     const long long x = (long long)blockIdx.x * kThreads + threadIdx.x;
     if (x >= used) return;
-    Acc *base = states + (long long)blockIdx.y * nseg * stride + x;
+    const long long b0 = (long long)blockIdx.y * nseg * stride + x;
+    if (!ws_ok(status, b0, n_states, 0xC003) || !ws_ok(status, b0 + (long long)(nseg - 1) * stride, n_states, 0xC003))
+        return;
+    Acc *base = states + b0;
     if (!causal) {
         Acc tot = Acc(0);
         for (int s = 0; s < nseg; ++s) tot += base[s * stride];
@@ -227,7 +259,10 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
     const T *Qh = (const T *)a.Q + head_off(a.lq, bh, a.H), *Kh = (const T *)a.K + head_off(a.lk, bh, a.H);
     const T *Vh = (const T *)a.V + head_off(a.lv, bh, a.H), *dOh = (const T *)a.dO + head_off(a.ldo, bh, a.H);
     const long long hout = head_off(a.lout, bh, a.H);
-    const Acc *st = (const Acc *)a.states + (bh * a.nseg + s) * a.stride;
+    const long long sbase = (bh * a.nseg + s) * a.stride;
+    const bool sok = ws_ok(a.status, sbase, a.n_states, 0xC004) &&
+                     ws_ok(a.status, sbase + (long long)D * D + 2 * D - 1, a.n_states, 0xC004);
+    const Acc *st = (const Acc *)a.states + sbase;
     Acc *rs_g = (Acc *)a.rs_g, *rs_delta = (Acc *)a.rs_delta, *rs_dpart = (Acc *)a.rs_dpart;
     constexpr bool FWD = (MODE == kFwdO || MODE == kFwdDelta);
 
@@ -235,10 +270,10 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
 #pragma unroll
     for (int m = 0; m < C::RPT; ++m) {
         const int r = p + C::NP * m;
-        X[m] = (FWD || MODE == kBwdDV) ? st[(long long)r * D + colg] : st[(long long)colg * D + r];
+        X[m] = !sok ? Acc(0) : (FWD || MODE == kBwdDV) ? st[(long long)r * D + colg] : st[(long long)colg * D + r];
     }
     Acc run1 = Acc(0), run2 = Acc(0);
-    if (t < D) {
+    if (t < D && sok) {
         run1 = (MODE == kBwdDV) ? st[(long long)D * D + D + t] : st[(long long)D * D + t];
         if (FWD) run2 = st[(long long)D * D + D + t];
     }
@@ -249,9 +284,11 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
         const int nb = (int)(REV ? (r1 - (long long)bi * RB) - b0 : min((long long)RB, r1 - b0));
         if (REV) {
             if (t < nb) {
-                const Acc gi = rs_g[bh * N + b0 + t];
+                const long long x = bh * N + b0 + t;
+                const bool in = ws_ok(a.status, x, a.n_rows, 0xC005);
+                const Acc gi = in ? rs_g[x] : Acc(1);
                 sG[t] = gi;
-                sDt[t] = rs_delta[bh * N + b0 + t] / gi;
+                sDt[t] = in ? rs_delta[x] / gi : Acc(0);
             }
             __syncthreads();
         }
@@ -310,16 +347,21 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
                     const Acc gi = n + warp_dot(sT + r * D, sRun + r * D, D, lane);
                     if (lane == 0) {
                         sG[r] = gi;
-                        if (MODE == kFwdO && a.g_out && blockIdx.y == 0) a.g_out[bh * N + b0 + r] = (float)gi;
+                        if (MODE == kFwdO && a.g_out && blockIdx.y == 0 &&
+                            ws_ok(a.status, bh * N + b0 + r, a.n_rows, 0xC006))
+                            a.g_out[bh * N + b0 + r] = (float)gi;
                     }
                 } else {
                     const Acc gi = n + warp_dot(sY + r * D, sRun + r * D, D, lane);
                     Acc delta = Acc(0);
-                    for (int q = 0; q < C::NBLK; ++q) delta += rs_dpart[(long long)q * a.BHN + bh * N + b0 + r];
+                    for (int q = 0; q < C::NBLK; ++q) {
+                        const long long x = (long long)q * a.BHN + bh * N + b0 + r;
+                        if (ws_ok(a.status, x, a.n_dpart, 0xC007)) delta += rs_dpart[x];
+                    }
                     if (lane == 0) {
                         sG[r] = gi;
                         sDt[r] = delta / gi;
-                        if (blockIdx.y == 0) {
+                        if (blockIdx.y == 0 && ws_ok(a.status, bh * N + b0 + r, a.n_rows, 0xC008)) {
                             rs_g[bh * N + b0 + r] = gi;
                             rs_delta[bh * N + b0 + r] = delta;
                         }
@@ -372,7 +414,8 @@ __global__ void __launch_bounds__(kThreads) simt_rows(Args a) {
             if (t < nb) {
                 Acc dsum = Acc(0);
                 for (int c = 0; c < C::EB; ++c) dsum += sRun[t * C::EB + c];
-                rs_dpart[(long long)blockIdx.y * a.BHN + bh * N + b0 + t] = dsum;
+                const long long x = (long long)blockIdx.y * a.BHN + bh * N + b0 + t;
+                if (ws_ok(a.status, x, a.n_dpart, 0xC009)) rs_dpart[x] = dsum;
             }
         }
         __syncthreads();
@@ -419,6 +462,10 @@ Args make_args(const Plan &p, const void *Q, const void *K, const void *V, const
     a.nseg = p.nseg;
     a.seg_len = p.seg_len;
     a.causal = p.causal;
+    a.status = (uint32_t *)ws;
+    a.n_states = (long long)p.BH * p.nseg * p.stride;
+    a.n_rows = a.BHN;
+    a.n_dpart = (long long)(p.D > 64 ? p.D / 64 : 1) * a.BHN;
     return a;
 }
 
@@ -432,7 +479,7 @@ cudaError_t forward_impl(const Plan &p, Args a, void *O, float *g, cudaStream_t 
     if ((e = allow_smem(simt_rows<T, Acc, D, kFwdO>, rows_smem<D, Acc>())) != cudaSuccess) return e;
     simt_aggregate<T, Acc, D, kAggFwd><<<grid, kThreads, agg_smem<D, Acc>(), s>>>(a);
     simt_scan<Acc><<<dim3((unsigned)((used + kThreads - 1) / kThreads), p.BH), kThreads, 0, s>>>(
-        (Acc *)a.states, p.nseg, p.stride, used, p.causal, 0);
+        (Acc *)a.states, p.nseg, p.stride, used, p.causal, 0, a.status, a.n_states);
     a.out = O;
     a.g_out = g;
     simt_rows<T, Acc, D, kFwdO><<<grid, kThreads, rows_smem<D, Acc>(), s>>>(a);
@@ -456,13 +503,13 @@ cudaError_t backward_impl(const Plan &p, Args a, void *dQ, void *dK, void *dV, c
     if ((e = allow_smem(simt_rows<T, Acc, D, kBwdDK>, sr)) != cudaSuccess) return e;
     if ((e = allow_smem(simt_rows<T, Acc, D, kBwdDV>, sr)) != cudaSuccess) return e;
     simt_aggregate<T, Acc, D, kAggFwd><<<grid, kThreads, sa, s>>>(a);
-    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 0);
+    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 0, a.status, a.n_states);
     simt_rows<T, Acc, D, kFwdDelta><<<grid, kThreads, sr, s>>>(a);
     a.out = dQ;
     a.lout = p.lay[kOpdQ];
     simt_rows<T, Acc, D, kBwdDQ><<<grid, kThreads, sr, s>>>(a);
     simt_aggregate<T, Acc, D, kAggRev><<<grid, kThreads, sa, s>>>(a);
-    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 1);
+    simt_scan<Acc><<<sgrid, kThreads, 0, s>>>((Acc *)a.states, p.nseg, p.stride, used, p.causal, 1, a.status, a.n_states);
     a.out = dK;
     a.lout = p.lay[kOpdK];
     simt_rows<T, Acc, D, kBwdDK><<<grid, kThreads, sr, s>>>(a);

@@ -57,7 +57,7 @@ __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" 
 // later pieces or all of them.  Row d, columns [64 hf, 64 hf + 64) of S go into TMEM (if to_tmem) and,
 // as bf16, into box hf of the operand tile Sb.  Half 0 also writes z[d] to zc (and TMEM column tZ if
 // to_tmem && vec_to_tmem), half 1 writes a[d] to ac (and column tA).
-static __device__ __noinline__ void load_carry_half(const float *slots, long long stride, long long h, int b, int d,
+static __device__ __forceinline__ void load_carry_half(const float *slots, long long stride, long long h, int b, int d,
                                                 int hf, uint32_t tS, uint32_t tZ, uint32_t tA, unsigned char *Sb,
                                                 float *zc, float *ac, bool to_tmem, bool vec_to_tmem) {
     constexpr int D = 128;
@@ -95,7 +95,7 @@ static __device__ __noinline__ void load_carry_half(const float *slots, long lon
 
 // The same for a piece whose carried state is zero by definition (a causal piece that starts its head
 // walking forward, or ends it walking in reverse): zeros instead of a slot read.
-static __device__ __noinline__ void zero_carry_half(int d, int hf, uint32_t tS, unsigned char *Sb, float *zc,
+static __device__ __forceinline__ void zero_carry_half(int d, int hf, uint32_t tS, unsigned char *Sb, float *zc,
                                                 float *ac, bool to_tmem) {
     if (to_tmem) {
         uint32_t r[32];

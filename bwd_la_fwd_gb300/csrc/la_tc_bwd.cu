@@ -171,17 +171,6 @@ __device__ __forceinline__ float2 dot2_half(const unsigned char *tile2, int row,
     return make_float2(az + bz, ay + by);
 }
 
-// dt_i (row i of the chunk) into an N = 16 MMA operand: two 8-row boxes of 128-byte rows in the 128-byte
-// swizzle (rows i < 64 in the first box), row 0 = bf16(dt_i), row 1 = bf16(dt_i - row 0), rows 2-7 zero.
-// An MMA of Q^T against it puts sum_i dt_i q_i, in two parts, into output columns 0 and 1.
-__device__ __forceinline__ void dt_tile_put(unsigned char *dtt, int i, float dt) {
-    unsigned char *bx = dtt + (i >> 6) * 1024;
-    const int e = i & 63;
-    const __nv_bfloat16 h = __float2bfloat16_rn(dt);
-    const __nv_bfloat16 l = __float2bfloat16_rn(dt - __bfloat162float(h));
-    *(__nv_bfloat16 *)(bx + ((e >> 3) << 4) + (e & 7) * 2) = h;              // row 0: 16-byte group e / 8
-    *(__nv_bfloat16 *)(bx + 128 + (((e >> 3) ^ 1) << 4) + (e & 7) * 2) = l;  // row 1: group index XOR 1
-}
 
 // The chunk walked after chunk c of piece pc when each piece is walked in reverse: c - 1 in the piece,
 // else the last chunk of the piece that `pi` yields next.  False when c is the last chunk walked.
@@ -252,7 +241,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     unsigned char *Sb = sm + STAGE;
     unsigned char *dqt = Sb + TB;        // dQ staging tile
     unsigned char *ones = dqt + TB;      // 8 rows x 128 B of bf16 1.0 (N = 16 operand, rows repeated)
-    unsigned char *dtt = ones + 1024;    // dt_i of the chunk's rows, as an N = 16 operand (dt_tile_put)
+    unsigned char *dtt = ones + 1024;    // dt_i of the chunk's rows, as an N = 16 operand (split_tile_put)
     float *zc = (float *)(dtt + 2048);   // z before the chunk (fp32, D)
     float *ac = zc + D;                  // a before the chunk
     float *xg = ac + D;                  // [2][128] row partials of g (per column half)
@@ -511,7 +500,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                     mbar_arrive(barU);
                 }
                 scale_row_half(ot, i, hf, ig);  // dO -> dO / g in place (W' and Y, its unscaled readers, are done)
-                if (hf == 0) dt_tile_put(dtt, i, dt);
+                if (hf == 0) split_tile_put(dtt, i, dt);
                 fence_proxy_async_smem();
                 mbar_arrive(barDt);
                 // dQ_i = X_i / g_i - dt_i z (X = Y + U' K), and the chunk's column sums
@@ -588,7 +577,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
     unsigned char *Sb = sm + NST * STAGE;
     unsigned char *dqt = Sb + TB;      // dQ staging tile
     unsigned char *ones = dqt + TB;    // 8 rows x 128 B of bf16 1.0
-    unsigned char *dtt = ones + 1024;  // [2 chunk parities] dt_i as an N = 16 operand (dt_tile_put)
+    unsigned char *dtt = ones + 1024;  // [2 chunk parities] dt_i as an N = 16 operand (split_tile_put)
     float *zc = (float *)(dtt + 4096); // the head's z
     float *ac = zc + D;                // the head's a
     float *xg = ac + D;                // [2][128] row partials of g
@@ -783,7 +772,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
                 const float dt = (xd[i] + xd[kC + i]) * ig * ig;
                 regs_half_to_dq(y0, y1, hf, ig, dt, zc, dqt, i);
                 scale_row_half(ot, i, hf, ig);  // dO -> dO / g in place (Y, its unscaled reader, is done)
-                if (hf == 0) dt_tile_put(dtt + (it & 1) * 2048, i, dt);
+                if (hf == 0) split_tile_put(dtt + (it & 1) * 2048, i, dt);
                 fence_proxy_async_smem();
                 if (it > 0) {  // keeps barDt one phase ahead of the MMA issuer at most
                     ok = wait_or_abort(barX, (it - 1) & 1, abort_flag, P.status, 0x329);

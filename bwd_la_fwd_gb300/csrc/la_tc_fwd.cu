@@ -230,11 +230,12 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
 // epilogue then writes the next Sb from S; the running fp32 z, a advance by each chunk's z_c, a_c from the
 // sums kernel.  The epilogue
 // forms q_i . z and the normaliser.  Non-causal: O = Q Sb with the head's totals (no T, P or state update) into two
-// alternating TMEM accumulators, so the MMA of one chunk overlaps the epilogue of the previous one.
-// Eight epilogue warps: two per TMEM lane quarter, each owning half of the columns; the row sums they
-// share (r_i and q_i . z) are exchanged through two TMEM columns.
+// alternating TMEM accumulators, so the MMA of one chunk overlaps the epilogue of the previous one, and
+// q_i . z by an N = 16 MMA of Q against z (split into two bf16 parts, ~16 significant bits) beside each.
+// Eight epilogue warps: two per TMEM lane quarter, each owning half of the columns; the causal row sums
+// they share (r_i and q_i . z) are exchanged through two TMEM columns.
 // TMEM: causal  T 0-127, O 128-255, S 256-383, exchange 416-419;
-//       non-causal  O 0-127 / 128-255, exchange 256-259.
+//       non-causal  O 0-127 / 128-255, q . z 288-303 / 304-319.
 // ----------------------------------------------------------------------------------------------------
 template <bool CAUSAL, bool FLAT>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __grid_constant__ TcParams P) {
@@ -247,7 +248,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     unsigned char *sm = smem_base(smem_raw, P.status, &aligned);
     unsigned char *stages = sm;
     unsigned char *Sb = sm + NST * STAGE;               // bf16 state, [d][e], two 64-column boxes
-    float *zc = (float *)(Sb + QB);                     // running z (fp32, D)
+    unsigned char *ztile = Sb + QB;                     // non-causal: z as an N = 16 operand (split_tile_put)
+    float *zc = (float *)(ztile + (CAUSAL ? 0 : 2048));  // running z (fp32, D)
     float *ac = zc + D;                                 // running a (fp32, D)
     uint64_t *full = (uint64_t *)(ac + D);
     uint64_t *empty = full + NST;
@@ -277,6 +279,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
     }
+    if (!CAUSAL) {
+        for (int k = threadIdx.x; k < 512; k += blockDim.x) ((uint32_t *)ztile)[k] = 0u;
+        fence_proxy_async_smem();
+    }
     if (warp == 1) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
@@ -290,6 +296,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
     griddep_launch_dependents();
     const uint32_t tmem = *tslot;
     const uint32_t tT = tmem, tS = tmem + 256;
+    const uint32_t tQZ = tmem + 288;  // non-causal: q_i . z in two parts, per accumulator buffer (16 columns each)
     const uint32_t tX = tmem + (CAUSAL ? 416 : 256);
 
     if (warp == 0 && lane == 0) {
@@ -336,6 +343,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
         const uint32_t idKK = idesc_bf16(128, 128, false, false);
         const uint32_t idKM = idesc_bf16(128, 128, false, true);
         const uint32_t idMM = idesc_bf16(128, 128, true, true);
+        const uint32_t idQZ = idesc_bf16(128, 16, false, false);
         const uint32_t sb = smem_u32(Sb);
         int it = 0, pno = 0;
         bool ok = true;
@@ -388,6 +396,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                     for (int k = 0; k < D / 16; ++k)  // O = Q Sb, K steps over d
                         mma_ss(tO, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
                                sdesc_sw128(sb + 2048 * k, kBox, 1024), idKM, k > 0);
+                    const uint32_t zb = smem_u32(ztile);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)  // q_i . z (columns 0 and 1: two parts), K steps over d
+                        mma_ss(tQZ + 16 * ob, sdesc_sw128(qb + (k >> 2) * kBox + 32 * (k & 3), 16, 1024),
+                               sdesc_sw128(zb + (k >> 2) * 1024 + 32 * (k & 3), 16, 0), idQZ, k > 0);
                 }
                 mma_commit(&barO[ob]);
                 mma_commit(&empty[s]);
@@ -412,6 +425,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
             else if (slot_ok(P, pc.h, blockIdx.x, 0xB003))
                 load_carry_half(P.slots, P.slot_stride, pc.h, blockIdx.x, i,
                                 hf, tS + lo, 0u, 0u, Sb, zc, ac, CAUSAL, false);
+            if (!CAUSAL && hf == 0) split_tile_put(ztile, i, zc[i]);  // the head's z for the q . z MMA
             fence_proxy_async_smem();
             tc_fence_before();
             epi_sync256();
@@ -457,29 +471,34 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
                     tc_fence_before();
                     mbar_arrive(barP);
                 }
-                if (!CAUSAL) {  // the Q tile is read below; causal chunks know it has landed from barT
-                    ok = wait_or_abort(&full[s], (it / NST) & 1, abort_flag, P.status, 0x20B);
-                    if (!ok) break;
+                float gi;
+                if (CAUSAL) {
+                    part += dot_half(st, i, hf, zc);  // q_i . z over this half's d
+                    // exchange columns alternate by chunk parity: the barrier below then orders every read of
+                    // one chunk's pair before the other half's write of the same pair two chunks later
+                    const uint32_t tXc = tX + lo + 2 * (it & 1);
+                    tmem_st1(tXc + hf, __float_as_uint(part));
+                    // g_i from both halves' partial sums
+                    tmem_st_wait();
+                    tc_fence_before();
+                    epi_sync256();
+                    tc_fence_after();
+                    uint32_t x0, x1;
+                    tmem_ld2(tXc, x0, x1);
+                    tmem_wait_ld(x0, x1);
+                    gi = (float)row0 + __uint_as_float(x0) + __uint_as_float(x1);
                 }
-                part += dot_half(st, i, hf, zc);  // q_i . z over this half's d
-                // exchange columns alternate by chunk parity: the barrier below then orders every read of
-                // one chunk's pair before the other half's write of the same pair two chunks later
-                const uint32_t tXc = tX + lo + 2 * (it & 1);
-                tmem_st1(tXc + hf, __float_as_uint(part));
-                // g_i from both halves' partial sums
-                tmem_st_wait();
-                tc_fence_before();
-                epi_sync256();
-                tc_fence_after();
-                uint32_t x0, x1;
-                tmem_ld2(tXc, x0, x1);
-                tmem_wait_ld(x0, x1);
-                const float gi = (CAUSAL ? (float)row0 : (float)P.N) + __uint_as_float(x0) + __uint_as_float(x1);
-                const float inv = 1.f / gi;
                 // output: O_i = (a + [P V + Q Sb]_i) / g_i, this half's 64 columns
                 ok = wait_or_abort(&barO[ob], ph_o, abort_flag, P.status, 0x209);
                 if (!ok) break;
                 tc_fence_after();
+                if (!CAUSAL) {  // g_i = N + q_i . z, formed by the MMA beside O
+                    uint32_t x0, x1;
+                    tmem_ld2(tQZ + 16 * ob + lo, x0, x1);
+                    tmem_wait_ld(x0, x1);
+                    gi = (float)P.N + __uint_as_float(x0) + __uint_as_float(x1);
+                }
+                const float inv = 1.f / gi;
                 const bool row_ok = i < nvalid;
                 // the O tile is staged in this stage's Q tile (Q is dead once O is complete; each thread
                 // overwrites only the row and box it read for q . z) and leaves by TMA
@@ -668,7 +687,7 @@ bool flat_heads(const Plan &p, const int *ops, int n) {
 
 constexpr size_t kSmemAgg = 3 * 2 * 2 * (size_t)tc::kBox + 2048 + 256;
 constexpr size_t kSmemFwdCausal = 2 * 3 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
-constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 1024 + 256;
+constexpr size_t kSmemFwdNonCausal = 4 * 2 * (size_t)tc::kBox + 2 * (size_t)tc::kBox + 2048 + 1024 + 256;
 static_assert(kSmemFwdCausal <= 232448, "forward kernel exceeds the shared-memory limit");
 
 bool set_smem_attrs() {

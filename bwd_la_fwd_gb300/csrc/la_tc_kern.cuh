@@ -93,6 +93,19 @@ static __device__ __forceinline__ void load_carry_half(const float *slots, long 
     if (to_tmem) tmem_st_wait();
 }
 
+// Value v of index e (0 <= e < 128) into an N = 16 MMA operand along its K dimension: two 8-row boxes of
+// 128-byte rows in the 128-byte swizzle (indices e < 64 in the first box), row 0 = bf16(v), row 1 =
+// bf16(v - row 0), rows 2-7 zero (set once by the caller).  An MMA against it puts sum_e v_e x_e, in two
+// parts that add up to ~16 significant bits of v, into output columns 0 and 1.
+__device__ __forceinline__ void split_tile_put(unsigned char *tile, int e, float v) {
+    unsigned char *bx = tile + (e >> 6) * 1024;
+    const int r = e & 63;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+    *(__nv_bfloat16 *)(bx + ((r >> 3) << 4) + (r & 7) * 2) = h;              // row 0: 16-byte group r / 8
+    *(__nv_bfloat16 *)(bx + 128 + (((r >> 3) ^ 1) << 4) + (r & 7) * 2) = l;  // row 1: group index XOR 1
+}
+
 // The same for a piece whose carried state is zero by definition (a causal piece that starts its head
 // walking forward, or ends it walking in reverse): zeros instead of a slot read.
 static __device__ __forceinline__ void zero_carry_half(int d, int hf, uint32_t tS, unsigned char *Sb, float *zc,

@@ -60,7 +60,8 @@ bool make_plan(int B, int H, int N, int D, int causal, int dtype, Plan *p) {
         p->off_flags = p->bytes_fwd;
         p->off_rowstats = p->off_flags;
         p->off_chunkye = round_up(p->off_rowstats + 2 * (size_t)BH * N * sizeof(float), 256);
-        p->bytes_bwd = round_up(p->off_chunkye + (size_t)BH * nchunk * 256 * sizeof(float), 256);
+        p->off_htot = round_up(p->off_chunkye + (size_t)BH * nchunk * 256 * sizeof(float), 256);
+        p->bytes_bwd = round_up(p->off_htot + (size_t)BH * (size_t)p->stride * sizeof(float), 256);
         return true;
     }
     if (p->use_wide) {
@@ -233,9 +234,11 @@ int la_forward_strided(const void *Q, const void *K, const void *V, int causal, 
     const void *ins[3] = {Q, K, V};
     for (int k = 0; k < 3; ++k)
         if (operands_meet(p, O, p.lay[la::kOpO], ins[k], p.lay[ops[k]], elem)) return LA_ERR_INVALID_ARG;
-    // the bytes of the workspace the forward writes: for D = 256 with a backward-sized workspace it also
-    // keeps g there for the backward
-    const size_t ws_used = p.use_wide && workspace_bytes >= p.bytes_bwd ? p.bytes_bwd : p.bytes_fwd;
+    // the bytes of the workspace the forward writes: with a backward-sized workspace, for D = 256 and for
+    // the causal tensor-core form, it also keeps g (and, causal, each head's total state) there for the
+    // backward
+    const bool keep = workspace_bytes >= p.bytes_bwd && (p.use_wide || (p.use_tc && p.causal));
+    const size_t ws_used = keep ? p.bytes_bwd : p.bytes_fwd;
     const Range ws_r = range_of(workspace, ws_used), o_r = range_of(O, (size_t)span_of(p, p.lay[la::kOpO]) * elem);
     if (overlap(o_r, ws_r)) return LA_ERR_INVALID_ARG;
     if (normaliser) {
@@ -246,9 +249,9 @@ int la_forward_strided(const void *Q, const void *K, const void *V, int causal, 
     }
     cudaStream_t s = (cudaStream_t)stream;
     unsigned char *ws = (unsigned char *)workspace;
-    cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, ws, s) : clear_state_tag(workspace, s);
+    cudaError_t e = p.use_tc ? la::tc_forward(p, Q, K, V, O, normaliser, ws, s, keep) : clear_state_tag(workspace, s);
     if (e == cudaSuccess && p.use_wide)
-        e = la::wide_forward(p, Q, K, V, O, normaliser, ws, s, workspace_bytes >= p.bytes_bwd);
+        e = la::wide_forward(p, Q, K, V, O, normaliser, ws, s, keep);
     else if (e == cudaSuccess && !p.use_tc) e = la::simt_forward(p, Q, K, V, O, normaliser, ws, s);
     return e == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
@@ -288,7 +291,7 @@ static int backward_impl(const void *Q, const void *K, const void *V, const void
     unsigned char *ws = (unsigned char *)workspace;
     cudaError_t e = cudaSuccess;
     if (p.use_tc) {
-        e = la::tc_backward(p, Q, K, V, dO, dQ, dK, dV, ws, s, reuse_fwd_state);
+        e = la::tc_backward(p, Q, K, V, O, dO, dQ, dK, dV, ws, s, reuse_fwd_state);
     } else if (p.use_wide) {
         // D = 256: the reusing backward checks the forward's record of g; the plain one recomputes g over
         // the region the forward keeps it in, so that record no longer holds

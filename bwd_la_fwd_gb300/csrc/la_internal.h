@@ -35,7 +35,9 @@ struct WsHeader {
     uint32_t info[7];     // where the first error happened (kernel id, block, step), for debugging
     uint32_t wide_skip;   // D = 256 backward: its row kernel found no matching forward record, skip the rest
     uint32_t fwd_sums_used; // a backward has put its reverse sums where the recorded forward sums were
-    uint32_t reserved[22];
+    uint32_t fwd_terms_kept; // the recorded causal forward also kept g and each head's total state (a
+                             // backward-sized workspace): the single-sweep backward can run on them
+    uint32_t reserved[21];
     uint64_t state_tag[7]; // which operands and work split the saved sums (or g) belong to, and their form
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");
@@ -62,6 +64,7 @@ struct Plan {
     size_t off_rowstats;
     size_t off_chunkye; // tensor-core causal backward: each chunk's column sums y_c, e_c
     size_t off_chunkza; // tensor-core path: each chunk's column sums z_c = sum k_j, a_c = sum v_j
+    size_t off_htot;    // tensor-core path, backward-sized: each head's total state (one slot per head)
     size_t bytes_fwd;   // workspace bytes for the forward / for the backward
     size_t bytes_bwd;
     bool use_tc;        // tcgen05 kernels for bf16 with D <= 128 rather than the SIMT kernels

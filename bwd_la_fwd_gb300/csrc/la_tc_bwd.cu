@@ -108,20 +108,6 @@ __device__ __forceinline__ void tmem_half_to_dq(uint32_t taddr, int hf, float ig
     regs_half_to_dq(x0, x1, hf, ig, dt, z, tile2, row);
 }
 
-// Multiplies row `row` of box hf of a bf16 tile by s in place.
-__device__ __forceinline__ void scale_row_half(unsigned char *tile2, int row, int hf, float s) {
-    unsigned char *tile = tile2 + hf * kBox;
-#pragma unroll
-    for (int g8 = 0; g8 < 8; ++g8) {
-        uint4 *p4 = (uint4 *)(tile + sw128_off(row, g8));
-        uint4 w = *p4;
-        uint32_t *wv = (uint32_t *)&w;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * s, bf16hi(wv[q]) * s);
-        *p4 = w;
-    }
-}
-
 // End of a dQ-walk piece: its reverse sums into its workspace slot.  Ppiece = sum_i q_i (dO_i / g_i)^T
 // from TMEM (row i, this half's 64 columns); half 1 also writes component i of y and of e.
 __device__ __forceinline__ void piece_rev_sums(const TcParams &P, const Piece &pc, uint32_t taddr, int i, int hf,
@@ -202,16 +188,6 @@ __device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h,
     *dt = in ? P.rs_dt[x] : 0.f;
     const long long yi = (h * P.sl.nchunk + c) * 256 + hf * 128 + j;
     *ye = in_range(yi, n_chunk_floats(P), P.status, 0xB008) ? P.chunk_ye[yi] : 0.f;
-}
-
-// Issues the TMA stores of a two-box output tile from shared memory (the boxes that hold the operand's
-// columns: nbox of them) and commits them.  One thread.
-template <bool FLAT>
-__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, HeadCoord hc,
-                                           int nbox) {
-    tile_store<FLAT>(map, tile2, 0, row0, hc);
-    if (nbox > 1) tile_store<FLAT>(map, tile2 + kBox, 64, row0, hc);
-    bulk_commit();
 }
 
 // ----------------------------------------------------------------------------------------------------
@@ -1328,20 +1304,29 @@ bool set_bwd_attrs() {
 
 }  // namespace
 
-cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
-                        void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state) {
+cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state) {
     if (!set_bwd_attrs()) return cudaErrorInvalidValue;
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
     if (!tc_host::fill_common(P, p, ws)) return cudaErrorInvalidDevice;
-    const int ops[7] = {kOpQ, kOpK, kOpV, kOpdO, kOpdQ, kOpdK, kOpdV};
-    const bool flat = tc_host::flat_heads(p, ops, 7);
+    // causal, reusing the forward's state: one reverse sweep per head where it is estimated faster (it
+    // also reads O, through a map of the same form as the others for its L2 prefetch)
+    const bool sweep = reuse_fwd_state && tc_sweep_chosen(p, tc_host::sm_count());
+    const int ops[8] = {kOpQ, kOpK, kOpV, kOpdO, kOpdQ, kOpdK, kOpdV, kOpO};
+    const bool flat = tc_host::flat_heads(p, ops, sweep ? 8 : 7);
     if (!tc_host::make_map(&P.tmQ, Q, p, kOpQ, flat) || !tc_host::make_map(&P.tmK, K, p, kOpK, flat) ||
         !tc_host::make_map(&P.tmV, V, p, kOpV, flat) || !tc_host::make_map(&P.tmdO, dO, p, kOpdO, flat) ||
         !tc_host::make_map(&P.tmdQ, dQ, p, kOpdQ, flat) || !tc_host::make_map(&P.tmdK, dK, p, kOpdK, flat) ||
         !tc_host::make_map(&P.tmdV, dV, p, kOpdV, flat))
         return cudaErrorInvalidValue;
     P.flat = flat ? 1 : 0;
+    P.Kp = K;
+    P.Vp = V;
+    if (sweep) {
+        if (!tc_host::make_map(&P.tmO, O, p, kOpO, flat)) return cudaErrorInvalidValue;
+        return tc_backward_sweep(p, P, O, dQ, dK, dV, ws, s);
+    }
     // The reverse sums share the slot array with the forward sums: the dQ walk reads a piece's forward
     // carry when the piece starts and writes that piece's reverse sums (same slot, same CTA) when it ends.
     P.slots_rev = (float *)(ws + p.off_states2);

@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(192, 1) tc_agg_kernel(const __grid_constant__ 
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         write_state_tag(P, P.whole_heads ? kTagTotals : kTagRaw);
         *fwd_sums_used(P) = 0u;
+        *fwd_terms_kept(P) = 0u;  // set again by the causal combine when it keeps the totals
     }
     const uint32_t tmem = *tslot;
 
@@ -518,9 +519,12 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_fwd_kernel(const __gri
 #pragma unroll
                     for (int q = 0; q < 4; ++q) *(uint4 *)(otile + sw128_off(i, 4 * half32 + q)) = w[q];
                 }
-                if (row_ok && hf == 0 && P.g) {
+                if (row_ok && hf == 0 && (P.g || P.rs_g)) {
                     const long long gix = (long long)pc.h * P.N + row0 + i;
-                    if (in_range(gix, n_row_floats(P), P.status, 0xB005)) P.g[gix] = gi;
+                    if (in_range(gix, n_row_floats(P), P.status, 0xB005)) {
+                        if (P.g) P.g[gix] = gi;
+                        if (P.rs_g) P.rs_g[gix] = gi;  // kept for the single-sweep backward
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -580,7 +584,9 @@ template __global__ void tc_fwd_kernel<false, false>(const __grid_constant__ TcP
 // one slot (its own) per piece: kCombinePrefix gives each piece the sum over the head's earlier pieces
 // (causal, chunk order), kCombineSuffix over the later ones (causal, reverse order), kCombineTotal the
 // head's total (non-causal).  grid = (ceil(kSlotF4 / 256), heads; heads beyond the grid's y extent loop);
-// thread x owns float4 x of every slot of its head, and reads each slot before it writes it.  At most 32
+// thread x owns float4 x of every slot of its head, and reads each slot before it writes it.  With
+// P.htot set (a causal forward on a backward-sized workspace), kCombinePrefix also writes each head's
+// total into slot h of P.htot, for the single-sweep backward, which walks each head from its end.  At most 32
 // registers, so that eight CTAs fit on an SM and the whole grid (17 x 64 CTAs at the standard shape) runs
 // in one wave: the kernel is a single round of loads and stores.
 // ----------------------------------------------------------------------------------------------------
@@ -590,6 +596,7 @@ __global__ void __launch_bounds__(256, 8) tc_combine_kernel(const __grid_constan
     if (P.combine_tag && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         write_state_tag(P, P.combine_tag);
         *fwd_sums_used(P) = 0u;
+        *fwd_terms_kept(P) = P.htot != nullptr && P.combine_mode == kCombinePrefix ? 1u : 0u;
     }
     const int x = blockIdx.x * 256 + threadIdx.x;
     if (x >= kSlotF4) return;
@@ -626,6 +633,9 @@ __global__ void __launch_bounds__(256, 8) tc_combine_kernel(const __grid_constan
         }
         if (mode == kCombineTotal)
             for (int k = 0; k < n; ++k) *at(k) = run;
+        else if (P.htot && mode == kCombinePrefix &&
+                 in_range(h * P.slot_stride + 4 * x + 3, n_htot_floats(P), P.status, 0xB00C))
+            ((float4 *)P.htot)[h * s4 + x] = run;
     }
 }
 
@@ -782,7 +792,7 @@ bool tc_supported(const Plan &p) { return p.dtype == 1 && (p.D == 32 || p.D == 6
 size_t tc_slot_bytes(const Plan &p) { return ((size_t)p.BH + tc::kMaxCtas) * (size_t)p.stride * sizeof(float); }
 
 cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
-                       unsigned char *ws, cudaStream_t s) {
+                       unsigned char *ws, cudaStream_t s, bool keep_terms) {
     if (!set_smem_attrs()) return cudaErrorInvalidValue;
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
@@ -797,6 +807,10 @@ cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *
     P.g = g;
     P.Kp = K;
     P.Vp = V;
+    if (keep_terms && p.causal) {
+        P.rs_g = (float *)(ws + p.off_rowstats);
+        P.htot = (float *)(ws + p.off_htot);
+    }
     cudaError_t e = launch_agg(P, s);
     if (e == cudaSuccess && !P.whole_heads)  // whole heads: the sums kernel has written the totals
         e = launch_combine(P, P.slots, p.causal ? tc::kCombinePrefix : tc::kCombineTotal,

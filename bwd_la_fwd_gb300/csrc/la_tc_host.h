@@ -42,6 +42,11 @@ struct TcParams {
     int test_drop_load;     // test hook: CTA 0 of the sums kernel issues no load for this iteration (-1: none)
     int whole_heads;        // non-causal, every slice exactly one head: its piece sums are the head's totals,
                             // and no tc_combine_kernel runs
+    float *htot;            // one slot per head: the head's total state (S, z, a).  The causal forward's
+                            // combine writes it when set; the single-sweep backward starts from it
+    Layout lay_O, lay_dQ, lay_dK, lay_dV;  // element strides (batch, head, row) of the operands that the
+                                           // single-sweep backward reads or writes row by row, not by TMA
+    uint32_t use_token;     // single-sweep backward: this launch's mark on the forward's record (>= 2)
 };
 
 // Extents, in floats, of the workspace arrays that the kernels index themselves (checked in the LA_CHECKED
@@ -52,6 +57,7 @@ __host__ __device__ inline long long n_slot_floats(const TcParams &P) {
 }
 __host__ __device__ inline long long n_chunk_floats(const TcParams &P) { return P.sl.T * 256; }
 __host__ __device__ inline long long n_row_floats(const TcParams &P) { return P.sl.T / P.sl.nchunk * P.N; }
+__host__ __device__ inline long long n_htot_floats(const TcParams &P) { return P.sl.T / P.sl.nchunk * P.slot_stride; }
 
 // Whether slot (h + b) lies wholly inside its array (and slots do not overlap); LA_CHECKED only.
 __device__ __forceinline__ bool slot_ok(const TcParams &P, long long h, int b, uint32_t where) {
@@ -99,6 +105,10 @@ __device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
 __device__ inline volatile uint32_t *fwd_sums_used(const TcParams &P) {
     return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, fwd_sums_used));
 }
+// Set with the tag by the causal forward's combine when it also kept g and the heads' totals.
+__device__ inline volatile uint32_t *fwd_terms_kept(const TcParams &P) {
+    return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, fwd_terms_kept));
+}
 #endif
 
 }  // namespace tc
@@ -124,12 +134,22 @@ cudaError_t launch_combine(tc::TcParams P, float *slots, int mode, uint64_t tag_
 bool tc_supported(const Plan &p);
 // Workspace bytes the tensor-core path needs for its state slots (one direction).
 size_t tc_slot_bytes(const Plan &p);
+// keep_terms (causal, the workspace is sized for the backward): also keep g_i and each head's total state
+// in the workspace, for the single-sweep backward.
 cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
-                       unsigned char *ws, cudaStream_t s);
+                       unsigned char *ws, cudaStream_t s, bool keep_terms);
 // reuse_fwd_state: take the per-piece K^T V sums the forward left in the workspace (tag checked on the
-// device, LA_ERR_STATE when it does not match) instead of recomputing them.
-cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *dO, void *dQ,
-                        void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state);
+// device, LA_ERR_STATE when it does not match) instead of recomputing them.  The causal form may then run
+// as one reverse sweep per head instead of the two walks (tc_sweep_chosen).
+cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O, const void *dO,
+                        void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state);
+// Whether a causal backward that reuses the forward's state runs as the single sweep (la_tc_sweep.cu):
+// D = 128 and, unless LA_TC_SWEEP says otherwise (0: never, 1: always), when its estimated time is below
+// the two walks'.
+bool tc_sweep_chosen(const Plan &p, int nsm);
+// The single sweep: one launch, one CTA per head (heads beyond the grid loop).
+cudaError_t tc_backward_sweep(const Plan &p, tc::TcParams &P, const void *O, void *dQ, void *dK, void *dV,
+                              unsigned char *ws, cudaStream_t s);
 
 // bf16 with D = 256: the tcgen05 kernels of la_tc_wide.cu (one CTA per head and 128-column output half).
 bool wide_supported(const Plan &p);

@@ -48,6 +48,16 @@ __device__ __forceinline__ void tile_store(const CUtensorMap *m, const void *src
 }
 
 
+// Issues the TMA stores of a two-box output tile from shared memory (the boxes that hold the operand's
+// columns: nbox of them) and commits them.  One thread.
+template <bool FLAT>
+__device__ __forceinline__ void store_tile(const CUtensorMap *map, const unsigned char *tile2, int row0, HeadCoord hc,
+                                           int nbox) {
+    tile_store<FLAT>(map, tile2, 0, row0, hc);
+    if (nbox > 1) tile_store<FLAT>(map, tile2 + kBox, 64, row0, hc);
+    bulk_commit();
+}
+
 constexpr int kEpiThreads = 256;  // eight epilogue warps: two per TMEM lane quarter
 __device__ __forceinline__ void epi_sync256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -104,6 +114,20 @@ __device__ __forceinline__ void split_tile_put(unsigned char *tile, int e, float
     const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
     *(__nv_bfloat16 *)(bx + ((r >> 3) << 4) + (r & 7) * 2) = h;              // row 0: 16-byte group r / 8
     *(__nv_bfloat16 *)(bx + 128 + (((r >> 3) ^ 1) << 4) + (r & 7) * 2) = l;  // row 1: group index XOR 1
+}
+
+// Multiplies row `row` of box hf of a bf16 tile by s in place.
+__device__ __forceinline__ void scale_row_half(unsigned char *tile2, int row, int hf, float s) {
+    unsigned char *tile = tile2 + hf * kBox;
+#pragma unroll
+    for (int g8 = 0; g8 < 8; ++g8) {
+        uint4 *p4 = (uint4 *)(tile + sw128_off(row, g8));
+        uint4 w = *p4;
+        uint32_t *wv = (uint32_t *)&w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wv[q] = pack_bf16(bf16lo(wv[q]) * s, bf16hi(wv[q]) * s);
+        *p4 = w;
+    }
 }
 
 // The same for a piece whose carried state is zero by definition (a causal piece that starts its head

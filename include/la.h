@@ -91,8 +91,9 @@ size_t la_workspace_bytes(int B, int H, int N, int D, int causal, int dtype, int
  *   normaliser  out: float [B,H,N] with g_i, or NULL to skip it
  *   workspace   in/out: device scratch of workspace_bytes >= la_workspace_bytes(..., backward = 0)
  * Pointers must be 16-byte aligned.  On the tensor-core paths the forward leaves in the workspace what
- * la_backward_with_forward_state reuses (the per-piece sums; for bf16 with D = 256 the normaliser, and
- * only when the workspace is backward-sized).
+ * la_backward_with_forward_state reuses: the per-piece sums; when the workspace is backward-sized
+ * (workspace_bytes >= la_workspace_bytes(..., backward = 1)) also the normaliser g and, causal with
+ * D <= 128, each head's total state, which the single-sweep causal backward starts from.
  */
 int la_forward(const void *Q, const void *K, const void *V, int causal, void *O, float *normaliser, int B, int H,
                int N, int D, int dtype, void *workspace, size_t workspace_bytes, void *stream);
@@ -123,8 +124,16 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * backward uses those sums up (it keeps its own reverse-direction sums in the same slots), so each reusing
  * backward needs a forward of its own.  The workspace records which K, V and shape its sums belong to;
  * when the record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.
- * Unchanged contents cannot be checked and are the caller's promise.  On the SIMT path (fp32 storage, or bf16 with
- * D = 16) there are no such sums to reuse and this call is la_backward.  On the wide path (bf16 with
+ * Unchanged contents cannot be checked and are the caller's promise.  Causal with bf16 and D = 128, the
+ * call may run as one reverse sweep per head ("single-sweep causal backward": dQ, dK and dV of each
+ * chunk together, Q, K, V, O and dO read once, dO . O giving the row terms) where that is estimated
+ * faster than the two walks, i.e. when the heads fill the GPU (B H of about 100 and more; the
+ * environment variable LA_TC_SWEEP = 0 or 1 forbids or forces it).  It starts from g and each head's
+ * total state, which la_forward keeps only in a backward-sized workspace: after a forward given a
+ * forward-sized workspace the sweep reports LA_ERR_STATE and computes nothing.  Its results equal
+ * la_backward's to within rounding (not bit for bit: it forms dO / g and delta from the stored O).  On
+ * the SIMT path (fp32 storage, or bf16 with D = 16) there are no such sums to reuse and this call is
+ * la_backward.  On the wide path (bf16 with
  * D = 256) the forward forms no piece sums; what is reused there is the normaliser g_i, which la_forward
  * keeps in the workspace when that workspace is backward-sized (la_workspace_bytes(..., backward = 1)),
  * under a record of Q's and K's addresses and strides, the shape and the mask.  A mismatch is

@@ -1,9 +1,10 @@
 """GPU parity at the full workload sizes, on the launch configuration the benchmark times.
 
 The benchmark times la_forward followed by la_backward_with_forward_state on the forward's workspace (the
-backward takes the forward's per-piece K^T V sums instead of recomputing them).  Every case here runs
-exactly that sequence, then the plain la_backward on the same workspace, and requires the two backward
-results to be bit-identical; the outputs are then checked against the oracle.
+backward takes what the forward left there -- its per-piece K^T V sums, and for the causal single sweep
+g and each head's total state -- instead of recomputing it).  Every case here runs exactly that
+sequence, then the plain la_backward on the same workspace; both backwards' outputs are checked against
+the oracle (the two are bit-identical when the reusing one runs as the two walks too).
 
 The explicit oracle costs O(N^2 D) per head, so at these sizes it checks sampled outputs it can compute
 one row at a time (O_i, g_i, dQ_i cost O(N D) each; dK_j, dV_j cost O((N - j) N D), so they are sampled
@@ -52,25 +53,25 @@ def _check_full(oracle_lib, B, H, N, D, seed, causal, layer=0, layers=1):
     dQ, dK, dV = la.la_backward(Q, K, V, O, dO, causal, workspace=ws, reuse_forward_state=True)
     torch.cuda.synchronize()
     assert la.la_get_status(ws) == 0
-    # the plain backward recomputes those sums: bit-identical results
+    heads = _compared_heads(B * H, N)
+    host = lambda v: v.reshape(B * H, N, -1)[heads].double().cpu().numpy().reshape(1, len(heads), N, -1)
+    got = {k: host(v) for k, v in {"O": O, "g": g, "dQ": dQ, "dK": dK, "dV": dV}.items()}
+    got["g"] = got["g"].reshape(1, len(heads), N)
+    # the plain backward recomputes those sums
     plain = la.la_backward(Q, K, V, O, dO, causal, workspace=ws)
     torch.cuda.synchronize()
     assert la.la_get_status(ws) == 0
-    for name, a, b in zip(("dQ", "dK", "dV"), (dQ, dK, dV), plain):
-        assert torch.equal(a, b), f"{name}: reused-state backward differs from the plain backward"
+    got_plain = {k: host(v) for k, v in zip(("dQ", "dK", "dV"), plain)}
     del plain
-    out = {"O": O, "g": g, "dQ": dQ, "dK": dK, "dV": dV}
-    heads = _compared_heads(B * H, N)
     f = _heads_f64(x, heads, B, H, N, D)
-    got = {k: v.reshape(B * H, N, -1)[heads].double().cpu().numpy().reshape(1, len(heads), N, -1)
-           for k, v in out.items()}
-    got["g"] = got["g"].reshape(1, len(heads), N)
 
     # whole heads against the fp64 running-state form
     rO, rg = oracle_lib.prefix_forward(f["Q"], f["K"], f["V"], causal)
     rdQ, rdK, rdV = oracle_lib.prefix_backward(f["Q"], f["K"], f["V"], f["dO"], causal)
     for name, ref in (("O", rO), ("g", rg), ("dQ", rdQ), ("dK", rdK), ("dV", rdV)):
         U.assert_close(name, got[name], ref, "bf16")
+    for name, ref in (("dQ", rdQ), ("dK", rdK), ("dV", rdV)):
+        U.assert_close(name, got_plain[name], ref, "bf16")
 
     # sampled rows of the first and last compared heads against the explicit definition
     ends = [0, len(heads) - 1]

@@ -1,8 +1,9 @@
 """la_backward_with_forward_state: the backward that takes the per-piece state sums from the forward.
 
 The forward's first kernel sums k_j v_j^T, k_j and v_j over each piece of rows; the backward needs the
-same sums.  The reusing entry point must give exactly what la_backward gives (the sums are the same
-numbers, so the gradients are bit-identical), must refuse (LA_ERR_STATE, nothing computed) when the
+same sums.  In its two-walk form (LA_TC_SWEEP = 0 here) the reusing entry point must give exactly what
+la_backward gives (the sums are the same numbers, so the gradients are bit-identical; its causal D = 128
+form may instead run as the single sweep, checked against the oracle in test_sweep.py), must refuse (LA_ERR_STATE, nothing computed) when the
 workspace holds sums of other K, V or of another work split -- or none, because a backward has since used
 them up -- and is plain la_backward on the SIMT path.
 For bf16 with D = 256 what is reused is the normaliser g_i, which the forward keeps in a backward-sized
@@ -25,9 +26,10 @@ def _tensors(B, H, N, D, dtype, seed):
 
 @pytest.mark.parametrize("causal", [1, 0])
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("bf16", 64), ("bf16", 256), ("f32", 64)])
-def test_reuse_is_bit_identical_to_la_backward(causal, dtype, D):
+def test_reuse_is_bit_identical_to_la_backward(monkeypatch, causal, dtype, D):
     import torch
     from bwd_la_fwd_gb300 import la
+    monkeypatch.setenv("LA_TC_SWEEP", "0")
     B, H, N = 2, 3, 777
     _, t = _tensors(B, H, N, D, dtype, seed=71)
     code = la.LA_BF16 if dtype == "bf16" else la.LA_F32

@@ -691,7 +691,7 @@ def run_decode(args):
 
 
 def main():
-    global N, D
+    global B, N, D
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -701,6 +701,7 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=0, help="heads per reference step (default: one per core)")
     ap.add_argument("--seq-len", type=int, default=N, help="N of the attention workload (sweeps; default 4096)")
     ap.add_argument("--head-dim", type=int, default=D, help="D of the attention workload (with --profile; default 128)")
+    ap.add_argument("--batch", type=int, default=B, help="B of the attention workload (with --profile; default 4)")
     ap.add_argument("--layout", choices=("bhnd", "bnhd"), default="bhnd",
                     help="attention operands contiguous [B,H,N,D] (default) or views of [B,N,H,D] tensors")
     ap.add_argument("--workload", choices=("attention", "decode", "sweep"), default="attention",
@@ -711,10 +712,13 @@ def main():
     args = ap.parse_args()
     N = args.seq_len
     D = args.head_dim
+    B = args.batch
     if args.layout != "bhnd" and not args.profile:
         ap.error("--layout bnhd times the hot path only: add --profile")
     if D != 128 and not args.profile:
         ap.error("--head-dim other than 128 times the hot path only: add --profile")
+    if B != 4 and not args.profile:
+        ap.error("--batch other than 4 times the hot path only: add --profile")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.workload == "decode":

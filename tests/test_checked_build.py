@@ -4,8 +4,9 @@ per-piece sums, per-chunk column sums, per-row statistics; CUDA-core path: segme
 and their per-column partials -- is checked against the array's extent, a violation being recorded as
 LA_ERR_BOUNDS instead of performed.  On odd and edge shapes of every configuration (bf16 D = 32 to 256 on
 tensor cores, fp32 and bf16 D = 16 on CUDA cores, both masks, ragged tails, one row, several chunks and
-heads per CTA) no index leaves its array (status LA_OK) and the results are bit-identical to the product
-build's.
+heads per CTA; the causal reusing backward also as the single sweep, which reads the forward's kept g
+and head totals) no index leaves its array (status LA_OK) and the results are bit-identical to the
+product build's.
 """
 import ctypes
 import os
@@ -33,6 +34,12 @@ CASES = [
     ("f32", 1, 2, 300, 128, 0, None),
     ("bf16", 2, 3, 513, 16, 1, None),
     ("f32", 1, 2, 1, 256, 1, None),
+]
+# the causal reusing backward forced to the single sweep (bf16, D = 128)
+SWEEP_CASES = [
+    ("bf16", 1, 2, 1, 128, 1, None),
+    ("bf16", 2, 3, 300, 128, 1, 2),    # several heads per CTA
+    ("bf16", 1, 2, 1000, 128, 1, None),
 ]
 
 
@@ -70,6 +77,16 @@ def _run(lib, t, B, H, N, D, causal, dt):
 
 @pytest.mark.parametrize("dtype,B,H,N,D,causal,cap", CASES)
 def test_checked_build_finds_no_index_out_of_range_and_matches(libs, monkeypatch, dtype, B, H, N, D, causal, cap):
+    _check(libs, monkeypatch, dtype, B, H, N, D, causal, cap)
+
+
+@pytest.mark.parametrize("dtype,B,H,N,D,causal,cap", SWEEP_CASES)
+def test_checked_build_single_sweep(libs, monkeypatch, dtype, B, H, N, D, causal, cap):
+    monkeypatch.setenv("LA_TC_SWEEP", "1")
+    _check(libs, monkeypatch, dtype, B, H, N, D, causal, cap)
+
+
+def _check(libs, monkeypatch, dtype, B, H, N, D, causal, cap):
     import torch
     if cap is not None:
         monkeypatch.setenv("LA_TC_MAX_CTAS", str(cap))

@@ -37,7 +37,9 @@ struct WsHeader {
     uint32_t fwd_sums_used; // a backward has put its reverse sums where the recorded forward sums were
     uint32_t fwd_terms_kept; // the recorded causal forward also kept g and each head's total state (a
                              // backward-sized workspace): the single-sweep backward can run on them
-    uint32_t reserved[21];
+    uint32_t bwd_skip;    // tensor-core backward: its dQ walk found no usable forward record, so the
+                          // dK / dV walk after it computes nothing either
+    uint32_t reserved[20];
     uint64_t state_tag[7]; // which operands and work split the saved sums (or g) belong to, and their form
 };
 static_assert(sizeof(WsHeader) <= 256, "workspace header must fit in 256 bytes");

@@ -202,9 +202,12 @@ __device__ __forceinline__ void load_chunk_stats(const TcParams &P, long long h,
 // are N = 16 MMAs against a tile of ones or of dt_i, into the columns of R1 that U' leaves free; the
 // epilogue drains them with the dQ row.  One TMA stage (Q, dO, K, V); the next chunk's tiles are
 // prefetched into L2 meanwhile, and dQ leaves through its own staging tile.
+// ROWS (the backward that reuses a forward given a backward-sized workspace): g_i is the forward's, kept
+// in the workspace, and delta_i = dO_i . O_i from the stored O, whose tile comes by TMA into the dQ
+// staging tile between two dQ stores; T, the P sums and the q . z, q . Y dots are not needed.
 // Epilogue thread u = threadIdx.x - 64: row i = 32 (warp % 4) + lane, column half hf = u / 128.
 // ----------------------------------------------------------------------------------------------------
-template <bool FLAT>
+template <bool FLAT, bool ROWS>
 __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __grid_constant__ TcParams P) {
     constexpr int D = 128, NB = D / 64;
     constexpr uint32_t TB = NB * kBox;
@@ -227,7 +230,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     uint64_t *bar = empty + 1;
     uint64_t *barT = bar, *barTr = bar + 1, *barSb = bar + 2, *barY = bar + 3, *barU = bar + 4, *barDt = bar + 5,
              *barX = bar + 6, *barR = bar + 7, *barPPf = bar + 8, *barC = bar + 9;
-    uint32_t *tslot = (uint32_t *)(bar + 10);
+    uint64_t *fullO = bar + 10;  // ROWS: the chunk's O tile has landed in the staging tile
+    uint32_t *tslot = (uint32_t *)(bar + 11);
     AbortState *abst = (AbortState *)(tslot + 2);
     volatile int *abort_flag = &abst->flag;
     if (!aligned) return;
@@ -236,8 +240,8 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     if (threadIdx.x == 0) {
         mbar_init(full, 1);
         mbar_init(empty, 1);  // the chunk's last MMA commit: every epilogue read of the stage precedes barDt
-        const uint32_t counts[10] = {1, E, E, 1, E, E, 1, E, E, 1};
-        for (int k = 0; k < 10; ++k) mbar_init(&bar[k], counts[k]);
+        const uint32_t counts[11] = {1, E, E, 1, E, E, 1, E, E, 1, 1};
+        for (int k = 0; k < 11; ++k) mbar_init(&bar[k], counts[k]);
         *abort_flag = 0;
         abst->limit_ns = P.wait_ns ? P.wait_ns : kWaitNs;
         fence_mbar_init();
@@ -256,16 +260,19 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace (and unused)?
-        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *fwd_sums_used(P))) {
+    if (P.check_tag) {  // the forward's per-piece sums (ROWS: and g) are reused: in the workspace, unused?
+        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *fwd_sums_used(P) ||
+                                 (ROWS && !*fwd_terms_kept(P)))) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
         __syncthreads();
     }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *bwd_skip(P) = *abort_flag ? 1u : 0u;  // for the dK / dV walk
     const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R0 = tmem, R1 = tmem + 128, R2 = tmem + 256, R3 = tmem + 384;
+    int o_issued = -1;  // ROWS, thread 64: the step whose O load it issued and that no wait has seen land
     // column sums of the chunk (N = 16 each; column 0 of each holds the sum, column 1 of cY the dt remainder),
     // in the R1 columns that U' (R1 + [0, 32) and R1 + [64, 96)) leaves free
     const uint32_t cY = R1 + 96, cE = R1 + 112;
@@ -336,13 +343,13 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {  // T = Q K^T ; W' = dO V^T
+                for (int k = 0; k < 8; ++k) {  // T = Q K^T (not with ROWS) ; W' = dO V^T
                     const uint32_t o = (k >> 2) * kBox + 32 * (k & 3);
-                    mma_ss(R0, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idKK, k > 0);
+                    if (!ROWS) mma_ss(R0, sdesc_sw128(qb + o, 16, 1024), sdesc_sw128(kb + o, 16, 1024), idKK, k > 0);
                     mma_ss(R1, sdesc_sw128(ob + o, 16, 1024), sdesc_sw128(vb + o, 16, 1024), idKK, k > 0);
                 }
                 mma_commit(barT);
-                ok = wait_or_abort(barTr, ph, abort_flag, P.status, 0x305);  // T has been read out of R0
+                if (!ROWS) ok = wait_or_abort(barTr, ph, abort_flag, P.status, 0x305);  // T has been read out of R0
                 if (!ok) break;
                 ok = wait_or_abort(barSb, ph, abort_flag, P.status, 0x306);
                 if (!ok) break;
@@ -412,6 +419,52 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 // this chunk's z_c[i] (half 0) or a_c[i] (half 1), from the sums kernel; used at the chunk's end
                 const long long zi = ((long long)pc.h * P.sl.nchunk + c) * 256 + hf * 128 + i;
                 const float zav = in_range(zi, n_chunk_floats(P), P.status, 0xB009) ? P.chunk_za[zi] : 0.f;
+                float gi, delta;
+                if (ROWS) {
+                    // g_i from the forward; delta_i = dO_i . O_i, O's tile in the staging tile (the first
+                    // chunk's load issued here, the others' after the previous dQ store)
+                    const HeadCoord hcur = head_coord<FLAT>(pc.h, P.H);
+                    if (u == 0 && it == 0) {
+                        mbar_arrive_expect_tx(fullO, TB);
+                        tile_load<FLAT>(dqt, &P.tmO, fullO, 0, (int)row0, hcur);
+                        tile_load<FLAT>(dqt + kBox, &P.tmO, fullO, 64, (int)row0, hcur);
+                        o_issued = it;
+                    }
+                    gi = 1.f;
+                    if (i < nvalid) {
+                        const long long x = (long long)pc.h * P.N + row0 + i;
+                        if (in_range(x, n_row_floats(P), P.status, 0xB00A)) gi = P.rs_g[x];
+                    }
+                    ok = wait_or_abort(full, ph, abort_flag, P.status, 0x310);  // dO has landed
+                    if (ok) ok = wait_or_abort(fullO, ph, abort_flag, P.status, 0x30F);
+                    if (!ok) break;
+                    if (u == 0) o_issued = -1;
+                    {
+                        const unsigned char *dt2 = ot + hf * kBox, *ot2 = dqt + hf * kBox;
+                        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+                        for (int g8 = 0; g8 < 8; ++g8) {
+                            const uint4 dv = *(const uint4 *)(dt2 + sw128_off(i, g8));
+                            const uint4 ov = *(const uint4 *)(ot2 + sw128_off(i, g8));
+                            const uint32_t w[4] = {dv.x, dv.y, dv.z, dv.w}, x[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                d0 = fmaf(bf16lo(w[q]), bf16lo(x[q]), d0);
+                                d1 = fmaf(bf16hi(w[q]), bf16hi(x[q]), d1);
+                            }
+                        }
+                        xd[hf * kC + i] = d0 + d1;
+                    }
+                    tc_fence_before();
+                    epi_sync256();
+                    tc_fence_after();
+                    delta = xd[i] + xd[kC + i];
+                    // W' (for U') and Y (the last reader of dO before it is scaled) are complete
+                    ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
+                    if (ok) ok = wait_or_abort(barY, ph, abort_flag, P.status, 0x30C);
+                    if (!ok) break;
+                    tc_fence_after();
+                } else {
                 float gpart = 0.f, dpart = 0.f;  // partial g_i and partial delta_i g_i over this half
                 {  // P, r_i and sum_j P_ij W'_ij over this half's columns j (fp32)
                     ok = wait_or_abort(barT, ph, abort_flag, P.status, 0x30B);
@@ -456,9 +509,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 tc_fence_before();
                 epi_sync256();
                 tc_fence_after();
-                const float gi = (float)row0 + xg[i] + xg[kC + i];
+                gi = (float)row0 + xg[i] + xg[kC + i];
+                delta = (xd[i] + xd[kC + i]) * (1.f / gi);
+                }
                 const float ig = 1.f / gi;
-                const float delta = (xd[i] + xd[kC + i]) * ig;
                 const float dt = delta * ig;
                 if (hf == 0 && i < nvalid) {
                     const long long x = (long long)pc.h * P.N + row0 + i;
@@ -486,7 +540,20 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
                 tmem_half_to_dq(R0 + lo, hf, ig, dt, zc, dqt, i);
                 fence_proxy_async_smem();
                 epi_sync256();  // dQ rows are staged, every read of zc for this chunk is done
-                if (u == 0) store_tile<FLAT>(&P.tmdQ, dqt, (int)row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
+                if (u == 0) {
+                    store_tile<FLAT>(&P.tmdQ, dqt, (int)row0, head_coord<FLAT>(pc.h, P.H), P.nbox);
+                    // ROWS: once the store has read the staging tile, the next chunk's O tile into it
+                    const long long nx = pc.h * P.sl.nchunk + c + 1;
+                    if (ROWS && nx < slice_lo(P.sl, blockIdx.x + 1)) {
+                        bulk_wait_read0();
+                        mbar_arrive_expect_tx(fullO, TB);
+                        const HeadCoord hn = head_coord<FLAT>(nx / P.sl.nchunk, P.H);
+                        const int nrow = (int)(nx % P.sl.nchunk) * kC;
+                        tile_load<FLAT>(dqt, &P.tmO, fullO, 0, nrow, hn);
+                        tile_load<FLAT>(dqt + kBox, &P.tmO, fullO, 64, nrow, hn);
+                        o_issued = it + 1;
+                    }
+                }
                 if (c + 1 < pc.e) {
                     tmem_half_to_tile(R2 + lo, Sb, i, hf);
                     fence_proxy_async_smem();
@@ -523,7 +590,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_kernel(const __
             mbar_arrive(barPPf);
         }
     }
-    if (threadIdx.x == 64) bulk_wait0();  // output stores complete before the CTA exits
+    if (threadIdx.x == 64) {
+        bulk_wait0();  // output stores complete before the CTA exits
+        if (ROWS && o_issued >= 0) mbar_wait(fullO, o_issued & 1, 50000000ull);  // an O load left by an abort lands
+    }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
@@ -608,6 +678,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dq_nc_kernel(const
         }
         __syncthreads();
     }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *bwd_skip(P) = *abort_flag ? 1u : 0u;  // for the dK / dV walk
     const bool skip = *abort_flag != 0;
     const uint32_t tmem = *tslot;
     const uint32_t R2 = tmem + 256, R3 = tmem + 384;
@@ -844,8 +915,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_kernel(const 
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace, and did the
+                        // dQ walk before this kernel take them?
+        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *bwd_skip(P))) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -1127,8 +1199,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads, 1) tc_bwd_dkdv_nc_kernel(con
     // the previous kernel of the stream has completed.
     griddep_wait();
     griddep_launch_dependents();
-    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace?
-        if (threadIdx.x == 0 && !state_tag_matches(P, (uint64_t)P.check_tag - 1)) {
+    if (P.check_tag) {  // the forward's per-piece sums are reused: are they in the workspace, and did the
+                        // dQ walk before this kernel take them?
+        if (threadIdx.x == 0 && (!state_tag_matches(P, (uint64_t)P.check_tag - 1) || *bwd_skip(P))) {
             *abort_flag = 1;
             report(P.status, kDevState, 0x5A7Eu);
         }
@@ -1290,7 +1363,9 @@ bool set_bwd_attrs() {
         const cudaFuncAttribute A = cudaFuncAttributeMaxDynamicSharedMemorySize;
         bool ok = true;
         for (int f = 0; f < 2 && ok; ++f)
-            ok = cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, A,
+            ok = cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true, false> : tc::tc_bwd_dq_kernel<false, false>, A,
+                                      (int)kSmemDq) == cudaSuccess &&
+                 cudaFuncSetAttribute(f ? tc::tc_bwd_dq_kernel<true, true> : tc::tc_bwd_dq_kernel<false, true>, A,
                                       (int)kSmemDq) == cudaSuccess &&
                  cudaFuncSetAttribute(f ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>, A,
                                       (int)kSmemDqNc) == cudaSuccess &&
@@ -1310,11 +1385,13 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     tc::TcParams P;
     memset(&P, 0, sizeof(P));
     if (!tc_host::fill_common(P, p, ws)) return cudaErrorInvalidDevice;
-    // causal, reusing the forward's state: one reverse sweep per head where it is estimated faster (it
-    // also reads O, through a map of the same form as the others for its L2 prefetch)
+    // causal, reusing the forward's state: one reverse sweep per head where it is estimated faster, else
+    // the two walks with the dQ walk taking g from the forward and delta from O (both read O's tiles
+    // through a map of the same form as the others)
     const bool sweep = reuse_fwd_state && tc_sweep_chosen(p, tc_host::sm_count());
+    const bool rows = reuse_fwd_state && p.causal;
     const int ops[8] = {kOpQ, kOpK, kOpV, kOpdO, kOpdQ, kOpdK, kOpdV, kOpO};
-    const bool flat = tc_host::flat_heads(p, ops, sweep ? 8 : 7);
+    const bool flat = tc_host::flat_heads(p, ops, rows ? 8 : 7);
     if (!tc_host::make_map(&P.tmQ, Q, p, kOpQ, flat) || !tc_host::make_map(&P.tmK, K, p, kOpK, flat) ||
         !tc_host::make_map(&P.tmV, V, p, kOpV, flat) || !tc_host::make_map(&P.tmdO, dO, p, kOpdO, flat) ||
         !tc_host::make_map(&P.tmdQ, dQ, p, kOpdQ, flat) || !tc_host::make_map(&P.tmdK, dK, p, kOpdK, flat) ||
@@ -1323,10 +1400,8 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
     P.flat = flat ? 1 : 0;
     P.Kp = K;
     P.Vp = V;
-    if (sweep) {
-        if (!tc_host::make_map(&P.tmO, O, p, kOpO, flat)) return cudaErrorInvalidValue;
-        return tc_backward_sweep(p, P, O, dQ, dK, dV, ws, s);
-    }
+    if (rows && !tc_host::make_map(&P.tmO, O, p, kOpO, flat)) return cudaErrorInvalidValue;
+    if (sweep) return tc_backward_sweep(p, P, O, dQ, dK, dV, ws, s);
     // The reverse sums share the slot array with the forward sums: the dQ walk reads a piece's forward
     // carry when the piece starts and writes that piece's reverse sums (same slot, same CTA) when it ends.
     P.slots_rev = (float *)(ws + p.off_states2);
@@ -1354,8 +1429,9 @@ cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void 
         }
     }
     if (e == cudaSuccess) {
-        e = p.causal ? tc_host::launch_tc(flat ? tc::tc_bwd_dq_kernel<true> : tc::tc_bwd_dq_kernel<false>, P.sl.G,
-                                          nthr, kSmemDq, s, P)
+        e = p.causal ? tc_host::launch_tc(rows ? (flat ? tc::tc_bwd_dq_kernel<true, true> : tc::tc_bwd_dq_kernel<false, true>)
+                                               : (flat ? tc::tc_bwd_dq_kernel<true, false> : tc::tc_bwd_dq_kernel<false, false>),
+                                          P.sl.G, nthr, kSmemDq, s, P)
                      : tc_host::launch_tc(flat ? tc::tc_bwd_dq_nc_kernel<true> : tc::tc_bwd_dq_nc_kernel<false>,
                                           P.sl.G, nthr, kSmemDqNc, s, P);
         ++launches;

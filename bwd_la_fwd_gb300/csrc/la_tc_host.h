@@ -105,6 +105,10 @@ __device__ inline bool state_tag_matches(const TcParams &P, uint64_t form) {
 __device__ inline volatile uint32_t *fwd_sums_used(const TcParams &P) {
     return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, fwd_sums_used));
 }
+// Set by a backward's dQ walk (CTA 0) when it refused the forward's record, read by its dK / dV walk.
+__device__ inline volatile uint32_t *bwd_skip(const TcParams &P) {
+    return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, bwd_skip));
+}
 // Set with the tag by the causal forward's combine when it also kept g and the heads' totals.
 __device__ inline volatile uint32_t *fwd_terms_kept(const TcParams &P) {
     return (volatile uint32_t *)((unsigned char *)P.status + offsetof(WsHeader, fwd_terms_kept));

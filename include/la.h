@@ -124,16 +124,17 @@ int la_backward(const void *Q, const void *K, const void *V, const void *O, cons
  * backward uses those sums up (it keeps its own reverse-direction sums in the same slots), so each reusing
  * backward needs a forward of its own.  The workspace records which K, V and shape its sums belong to;
  * when the record does not match, the kernels compute nothing and la_get_status reports LA_ERR_STATE.
- * Unchanged contents cannot be checked and are the caller's promise.  Causal with bf16 and D = 128, the
- * call may run as one reverse sweep per head ("single-sweep causal backward": dQ, dK and dV of each
- * chunk together, Q, K, V, O and dO read once, dO . O giving the row terms) where that is estimated
+ * Unchanged contents cannot be checked and are the caller's promise.  Causal on the tensor-core
+ * kernels (bf16, D = 32, 64, 128) the call also takes the normaliser g, which la_forward keeps only in a
+ * backward-sized workspace, and forms delta_i = dO_i . O_i from O: after a forward given a forward-sized
+ * workspace it reports LA_ERR_STATE and computes nothing.  With D = 128 it may run as one reverse sweep
+ * per head ("single-sweep causal backward": dQ, dK and dV of each chunk together, Q, K, V, O and dO read
+ * once, starting from each head's total state, which la_forward keeps beside g) where that is estimated
  * faster than the two walks, i.e. when the heads fill the GPU (B H of about 100 and more; the
- * environment variable LA_TC_SWEEP = 0 or 1 forbids or forces it).  It starts from g and each head's
- * total state, which la_forward keeps only in a backward-sized workspace: after a forward given a
- * forward-sized workspace the sweep reports LA_ERR_STATE and computes nothing.  Its results equal
- * la_backward's to within rounding (not bit for bit: it forms dO / g and delta from the stored O).  On
- * the SIMT path (fp32 storage, or bf16 with D = 16) there are no such sums to reuse and this call is
- * la_backward.  On the wide path (bf16 with
+ * environment variable LA_TC_SWEEP = 0 or 1 forbids or forces it).  The causal results equal
+ * la_backward's to within rounding, not bit for bit (la_backward forms g and delta from the carried
+ * state).  On the SIMT path (fp32 storage, or bf16 with D = 16) there are no such sums to reuse and
+ * this call is la_backward.  On the wide path (bf16 with
  * D = 256) the forward forms no piece sums; what is reused there is the normaliser g_i, which la_forward
  * keeps in the workspace when that workspace is backward-sized (la_workspace_bytes(..., backward = 1)),
  * under a record of Q's and K's addresses and strides, the shape and the mask.  A mismatch is

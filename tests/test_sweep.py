@@ -2,8 +2,9 @@
 
 The sweep takes g_i and each head's total state from the forward (kept in a backward-sized workspace)
 and delta_i = dO_i . O_i from the forward's output, and forms dQ, dK and dV of each chunk together, last
-chunk first.  LA_TC_SWEEP = 1 makes every eligible reusing backward run it (0: never), so that these
-cases cover it whatever the size heuristic picks.  Checked here against the oracle: ragged and exact
+chunk first.  LA_TC_SWEEP = 1 makes every eligible reusing backward run it (0: never, the two walks,
+whose dQ walk then also takes g and delta from the forward and O), so that these cases cover both forms
+whatever the size heuristic picks.  Checked here against the oracle: ragged and exact
 chunk counts, one and two rows, one chunk, several heads walked by one CTA (LA_TC_MAX_CTAS), strided operands
 (bit-identical to the contiguous call), and the refusals: a forward that kept nothing (forward-sized
 workspace), a second backward on one forward's record, another K.  The two-walk form of the same call
@@ -97,11 +98,14 @@ def test_strided_operands_are_bit_identical(monkeypatch):
         assert torch.equal(a, b), name
 
 
+@pytest.mark.parametrize("mode", ["1", "0"])
 @pytest.mark.parametrize("case", ["forward_sized_workspace", "second_backward", "other_keys"])
-def test_refusals_compute_nothing(monkeypatch, case):
+def test_refusals_compute_nothing(monkeypatch, case, mode):
+    """Both forms of the causal reusing backward (the sweep, and the two walks whose dQ walk takes g and
+    O from the forward) refuse a workspace whose forward kept nothing, was used up or had other keys."""
     import torch
     from bwd_la_fwd_gb300 import la
-    monkeypatch.setenv("LA_TC_SWEEP", "1")
+    monkeypatch.setenv("LA_TC_SWEEP", mode)
     B, H, N, D = 1, 2, 513, 128
     x = inputs.generate(B, H, N, D, seed=912, dtype="bf16")
     t = {n: U.to_device(x[n], "bf16") for n in ("Q", "K", "V", "dO")}

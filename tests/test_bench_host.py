@@ -79,3 +79,14 @@ def test_clock_summary_reports_thermal_and_hardware_slowdowns():
     assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
     assert out["sm_mhz"] == 1450  # unreadable samples are skipped
     assert bench.ClockSampler.summary(bench.ClockSampler(0), 0.0, 1.0)["samples"] == 0
+
+
+@pytest.mark.parametrize("args", [["--batch", "8"], ["--head-dim", "64"], ["--layout", "bnhd"]])
+def test_other_shapes_time_the_hot_path_only(args):
+    """The bench line is the standard workload: another batch, head size or layout is refused unless
+    --profile (the hot path alone, for profilers) is given; the refusal comes before any GPU work."""
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args, "--steps", "1"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2
+    assert "--profile" in r.stderr

@@ -9,12 +9,14 @@
 // where S_c, z_c (earlier rows) are the forward state and P_c = sum q_i dOt_i^T, y_c = sum dt_i q_i,
 // e_c = sum dOt_i run over the later rows.  Non-causal: every sum runs over the whole head.
 //
-// Launches: the per-piece K^T V sums (shared with the forward), the dQ walk in chunk order (it forms g_i
-// and delta_i from the chunk's own products and the carried state, so the stored O is not read; it also
-// writes each piece's reverse sums P, y, e and, causal, the per-row g_i, dt_i), and the dK / dV walk in
-// reverse chunk order.  Each walk adds up the slots of the head's other pieces itself when it loads the
-// state carried into a piece.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9 epilogue (two warps
-// per TMEM lane quarter, each owning 64 of the 128 columns).
+// Launches: the per-piece K^T V sums (shared with the forward, so the backward that reuses the forward's
+// workspace skips them), a combine that turns the piece slots into the carries of each piece, the dQ walk
+// in chunk order (it forms g_i and delta_i from the chunk's own products and the carried state, so the
+// stored O is not read -- except in its ROWS form, for the causal backward that reuses a forward given a
+// backward-sized workspace: g_i from the forward and delta_i = dO_i . O_i; it also writes each piece's
+// reverse sums P, y, e and, causal, the per-row g_i, dt_i), a combine of those reverse sums, and the
+// dK / dV walk in reverse chunk order.  Each kernel: warp 0 TMA, warp 1 TMEM + MMA issue, warps 2-9
+// epilogue (two warps per TMEM lane quarter, each owning 64 of the 128 columns).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>

@@ -44,8 +44,6 @@ struct TcParams {
                             // and no tc_combine_kernel runs
     float *htot;            // one slot per head: the head's total state (S, z, a).  The causal forward's
                             // combine writes it when set; the single-sweep backward starts from it
-    Layout lay_O, lay_dQ, lay_dK, lay_dV;  // element strides (batch, head, row) of the operands that the
-                                           // single-sweep backward reads or writes row by row, not by TMA
     uint32_t use_token;     // single-sweep backward: this launch's mark on the forward's record (>= 2)
 };
 
@@ -143,8 +141,9 @@ size_t tc_slot_bytes(const Plan &p);
 cudaError_t tc_forward(const Plan &p, const void *Q, const void *K, const void *V, void *O, float *g,
                        unsigned char *ws, cudaStream_t s, bool keep_terms);
 // reuse_fwd_state: take the per-piece K^T V sums the forward left in the workspace (tag checked on the
-// device, LA_ERR_STATE when it does not match) instead of recomputing them.  The causal form may then run
-// as one reverse sweep per head instead of the two walks (tc_sweep_chosen).
+// device, LA_ERR_STATE when it does not match) instead of recomputing them; causal, also the forward's g
+// (its dQ walk then forms delta from O), and the call may run as one reverse sweep per head instead of
+// the two walks (tc_sweep_chosen).
 cudaError_t tc_backward(const Plan &p, const void *Q, const void *K, const void *V, const void *O, const void *dO,
                         void *dQ, void *dK, void *dV, unsigned char *ws, cudaStream_t s, bool reuse_fwd_state);
 // Whether a causal backward that reuses the forward's state runs as the single sweep (la_tc_sweep.cu):

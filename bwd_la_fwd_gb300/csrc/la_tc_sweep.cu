@@ -1,9 +1,9 @@
 // la_tc_sweep.cu -- the causal backward as one reverse sweep per head (tcgen05 / TMA, bf16, D = 128).
 //
-// The two-walk backward (la_tc_bwd.cu) reads Q, K, V and dO twice: its dQ walk forms g_i and delta_i
-// from the carried state and leaves each piece's reverse sums for the dK / dV walk.  The sweep instead
-// takes g_i from the forward (kept in the workspace) and delta_i = dO_i . O_i from the forward's output,
-// and walks each head once, last chunk first, forming dQ, dK and dV of a chunk together: the gradient's
+// The two-walk backward (la_tc_bwd.cu) reads Q, K, V and dO twice: its dQ walk walks each piece forward
+// and leaves the piece's reverse sums for the dK / dV walk, which walks it back.  The sweep takes g_i
+// from the forward (kept in the workspace) and delta_i = dO_i . O_i from the forward's output, and walks
+// each head once, last chunk first, forming dQ, dK and dV of a chunk together: the gradient's
 // eight tensor volumes (Q, K, V, O, dO in, dQ, dK, dV out) move once ("Transformer Based Linear Attention
 // with Optimized GPU Kernel Implementation", sciencestack.ai page, TL;DR: analytical gradients and
 // minimal data movement).  With dOt_i = dO_i / g_i, dt_i = (dO_i . O_i) / g_i and, within chunk c,
@@ -49,12 +49,6 @@ namespace tc {
 using namespace sm100;
 
 namespace {
-
-// Row n of flat head bh of a bf16 operand given by its (batch, head, row) element strides.
-__device__ __forceinline__ __nv_bfloat16 *op_row(const void *base, const Layout &l, long long bh, int H, long long n) {
-    const long long b = bh / H, h = bh - b * H;
-    return (__nv_bfloat16 *)base + b * l.sb + h * l.sh + n * l.sn;
-}
 
 // This half's 64 columns of an fp32 TMEM block (lane = the thread's row) mapped through f(column, value),
 // rounded to bf16, into row `row`, box hf of a two-box 128B-swizzled tile.
@@ -559,10 +553,6 @@ cudaError_t tc_backward_sweep(const Plan &p, tc::TcParams &P, const void *O, voi
     P.dQ = dQ;
     P.dK = dK;
     P.dV = dV;
-    P.lay_O = p.lay[kOpO];
-    P.lay_dQ = p.lay[kOpdQ];
-    P.lay_dK = p.lay[kOpdK];
-    P.lay_dV = p.lay[kOpdV];
     P.rs_g = (float *)(ws + p.off_rowstats);
     P.htot = (float *)(ws + p.off_htot);
     P.check_tag = (int)tc::kTagPrefix + 1;

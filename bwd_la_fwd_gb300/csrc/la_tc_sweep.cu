@@ -536,13 +536,13 @@ bool tc_sweep_chosen(const Plan &p, int nsm) {
         if (env[0] == '1') return true;
     }
     // Times fitted to measurements on one GB300 (152 SMs; B = 4, 8, 16, H = 16, N = 1024 ... 4096): the
-    // sweep ~8.0 us per chunk a CTA walks (one CTA per head) + 20 us; the two walks ~10.7 us per chunk a CTA
-    // walks (all SMs) + 42 us (two combines, two ramps).  The sweep wins once the heads fill the GPU
+    // sweep ~8.0 us per chunk a CTA walks (one CTA per head) + 20 us; the two walks ~10.1 us per chunk a CTA
+    // walks (all SMs) + 38.5 us (two combines, two ramps).  The sweep wins once the heads fill the GPU
     // (B H >~ 100 at these lengths).
     const double nchunk = (double)(((long long)p.N + tc::kC - 1) / tc::kC);
     const double heads_per_cta = (double)((p.BH + nsm - 1) / nsm);
     const double sweep = 8.0 * heads_per_cta * nchunk + 20.0;
-    const double walks = 10.7 * (double)p.BH * nchunk / (double)nsm + 42.0;
+    const double walks = 10.1 * (double)p.BH * nchunk / (double)nsm + 38.5;
     return sweep < walks;
 }
 

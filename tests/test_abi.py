@@ -73,6 +73,17 @@ def test_workspace_sizes(lib):
     assert ws(4, 16, 65536, 128, 1, 1, 1) <= 0.2 * 16 * (8 * 4 * 16 * 65536 * 128 * 2)
 
 
+def test_backward_workspace_holds_what_the_forward_keeps(lib):
+    """On the tensor-core path a backward-sized workspace is also what a causal forward keeps its terms in
+    for the reusing backward: beyond the forward-sized part it holds the per-row g and dt (fp32), each
+    chunk's y_c, e_c (256 floats) and one total state per head (D x D + 2 D floats at D = 128)."""
+    ws = lib.la_workspace_bytes
+    for B, H, N in ((1, 1, 1), (2, 3, 549), (4, 16, 4096), (8, 16, 2048)):
+        BH, nchunk = B * H, (N + 127) // 128
+        extra = ws(B, H, N, 128, 1, 1, 1) - ws(B, H, N, 128, 1, 1, 0)
+        assert extra >= 4 * (2 * BH * N + 256 * BH * nchunk + BH * (128 * 128 + 2 * 128))
+
+
 def test_narrow_bf16_heads_take_the_tensor_core_workspace(lib):
     """bf16 with D = 32, 64 runs on the D = 128 tensor-core kernels (columns past D zero-extended): its
     workspace is the D = 128 one (state slots of 128 x 128 + 2 x 128 floats, per-row and per-chunk sums),

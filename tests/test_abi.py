@@ -119,6 +119,12 @@ def test_forward_rejects_bad_arguments_on_host(lib):
     assert _fwd(lib, wsb=16) == 3                     # workspace too small
     assert _fwd(lib, O=0x1000) == 1                   # output aliases Q
     assert _fwd(lib, g=0x6000_0000 + 64) == 1         # normaliser inside O
+    # a causal forward given a backward-sized workspace also writes its backward part (g and each head's
+    # total state for the reusing backward): an output there is refused too
+    fwd_b, bwd_b = (lib.la_workspace_bytes(1, 1, 8, 64, 1, 1, bw) for bw in (0, 1))
+    assert bwd_b > fwd_b
+    assert _fwd(lib, O=0x8000_0000 + fwd_b, wsb=bwd_b) == 1
+    assert _fwd(lib, g=0x8000_0000 + bwd_b - 256, wsb=bwd_b) == 1
 
 
 @pytest.mark.parametrize("entry", ["la_backward", "la_backward_with_forward_state"])
